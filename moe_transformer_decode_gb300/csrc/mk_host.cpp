@@ -1,0 +1,637 @@
+// Host side of libmk: context and workspace, the task scheduler, tensor maps and launches.
+//
+// Scheduling follows the task-list design of the Cohere megakernel news pages
+// (aimodeling.com "cohere-megakernel-north-mini-code-h100", section "One persistent kernel
+// for the whole decode step"; aibriefing.imbch.dev article 8171681, section "Scheduling and
+// Performance Benchmarks": a mostly static per-SM schedule built on the host). Every task
+// of a layer is listed in dependency order (router, QKV, attention, expert gate/up, O-proj,
+// expert down) and given to the SM with the least bytes assigned so far, so parallel-layer
+// work backfills SMs that would otherwise wait; each SM's list is in that global order,
+// which is what keeps the counter waits deadlock-free.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "mk_internal.h"
+
+namespace mk {
+int kernel_smem_bytes();
+cudaError_t launch_decode(const Params& p, const TensorMaps& tm, cudaStream_t st);
+cudaError_t max_blocks_per_sm(int B, int* n);
+cudaError_t configure_kernels();
+}  // namespace mk
+
+using namespace mk;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct mk_ctx {
+  mk_model_cfg cfg;
+  mk_weight_ptrs w;
+  int device, n_sm;
+  int mode;
+  std::string err;
+  // workspace (device)
+  float *xs, *q, *knew, *vnew, *attn_o, *attn_out, *rlogits, *h, *moe_out, *apart, *lm_best_v;
+  int32_t* lm_best_i;
+  int32_t* topk_ids;
+  float* topk_w;
+  Route* route;
+  float2* rope;
+  uint32_t* counters;
+  int32_t* status;
+  int32_t* status_host;  // mapped pinned copy of the status code (written by the device on error)
+  int32_t* status_host_dev;
+  int max_pos;
+  // schedule
+  bool scheduled;
+  int B;
+  const int32_t* block_table;
+  Task* d_tasks;
+  int32_t* d_sm_begin;  // megakernel: [n_sm+1]; then per-op launches, each [n_sm+1]
+  int32_t* d_cnt;
+  int32_t *d_chunk_pages, *d_n_chunks;
+  int max_chunks, n_lm_sm, n_tasks, n_counters;
+  int n_op_launches;
+  uint32_t epoch;
+  // tensor maps cache
+  void *tm_k_ptr, *tm_v_ptr;
+  int tm_pages;
+  TensorMaps tm;
+  EncodeTiledFn encode;
+  // trace
+  mk_trace_entry* trace;
+  unsigned long long* trace_count;
+  long long trace_cap;
+};
+
+static mk_status fail(mk_ctx* c, mk_status s, const std::string& msg) {
+  if (c) c->err = msg;
+  return s;
+}
+static mk_status cuda_fail(mk_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, MK_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define CK(call)                                          \
+  do {                                                    \
+    cudaError_t e_ = (call);                              \
+    if (e_ != cudaSuccess) return cuda_fail(c, e_, #call); \
+  } while (0)
+
+template <typename T>
+static cudaError_t dalloc(T** p, size_t n) {
+  *p = nullptr;
+  if (n == 0) n = 1;
+  return cudaMalloc((void**)p, n * sizeof(T));
+}
+
+static void free_schedule(mk_ctx* c) {
+  cudaFree(c->d_tasks);
+  cudaFree(c->d_sm_begin);
+  cudaFree(c->d_cnt);
+  cudaFree(c->d_chunk_pages);
+  cudaFree(c->d_n_chunks);
+  cudaFree(c->apart);
+  cudaFree(c->counters);
+  c->d_tasks = nullptr;
+  c->d_sm_begin = c->d_cnt = c->d_chunk_pages = c->d_n_chunks = nullptr;
+  c->apart = nullptr;
+  c->counters = nullptr;
+  c->scheduled = false;
+}
+
+extern "C" void mk_destroy(mk_ctx* c) {
+  if (!c) return;
+  free_schedule(c);
+  cudaFree(c->xs); cudaFree(c->q); cudaFree(c->knew); cudaFree(c->vnew); cudaFree(c->attn_o); cudaFree(c->attn_out);
+  cudaFree(c->rlogits); cudaFree(c->h); cudaFree(c->moe_out); cudaFree(c->lm_best_v); cudaFree(c->lm_best_i);
+  cudaFree(c->route); cudaFree(c->rope); cudaFree(c->status); cudaFree(c->topk_ids); cudaFree(c->topk_w);
+  if (c->status_host) cudaFreeHost(c->status_host);
+  delete c;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, mk_ctx** out) {
+  if (!cfg || !w || !out) return MK_ERR_INVALID_ARG;
+  *out = nullptr;
+  const mk_model_cfg& m = *cfg;
+  if (m.n_layers <= 0 || m.hidden <= 0 || m.n_q_heads <= 0 || m.n_kv_heads <= 0 || m.head_dim <= 0 ||
+      m.n_experts <= 0 || m.top_k <= 0 || m.top_k > m.n_experts || m.expert_inter <= 0 || m.vocab <= 0 ||
+      m.max_batch <= 0 || m.max_pages_per_seq <= 0 || m.n_q_heads % m.n_kv_heads != 0 || !(m.rms_eps >= 0.f) ||
+      !(m.rope_theta > 0.f) || m.n_layers > 65535)
+    return MK_ERR_INVALID_ARG;
+  if (!w->embed || !w->norm_gain || !w->w_qkv || !w->w_o || !w->w_router || !w->w_gate_up || !w->w_down ||
+      !w->final_gain || !w->lm_head)
+    return MK_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->embed, w->norm_gain, w->w_qkv, w->w_o, w->w_router, w->w_gate_up, w->w_down,
+                        w->final_gain, w->lm_head};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MK_ERR_INVALID_ARG;
+  const int od = m.n_q_heads * m.head_dim;
+  const bool shape_ok = (m.hidden == 256 || m.hidden == 512 || m.hidden == 1024 || m.hidden == 2048) &&
+                        (m.head_dim == 64 || m.head_dim == 128) && m.n_q_heads / m.n_kv_heads <= 8 &&
+                        od % 256 == 0 && (od <= 2048 || od % 2048 == 0) && m.expert_inter % 256 == 0 &&
+                        m.expert_inter <= 2048 && m.top_k <= kMaxK && m.max_batch <= kMaxB &&
+                        m.page_size == kPage && m.n_experts <= kMaxExperts && m.n_experts % 8 == 0 &&
+                        m.vocab % 64 == 0;
+  if (!shape_ok) return MK_ERR_UNSUPPORTED;
+
+  mk_ctx* c = new mk_ctx();  // value-initialized: every pointer starts null
+  c->cfg = m;
+  c->w = *w;
+  c->mode = MK_MODE_MEGAKERNEL;
+  c->scheduled = false;
+  c->d_tasks = nullptr;
+  c->d_sm_begin = c->d_cnt = c->d_chunk_pages = c->d_n_chunks = nullptr;
+  c->trace = nullptr;
+  c->trace_count = nullptr;
+  c->trace_cap = 0;
+  c->tm_k_ptr = c->tm_v_ptr = nullptr;
+  c->tm_pages = -1;
+  c->epoch = 0;
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e != cudaSuccess) { mk_destroy(c); return MK_ERR_CUDA; }
+  cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, c->device);
+  int coop = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
+  int smem_optin = 0;
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+  if (!coop || smem_optin < kernel_smem_bytes()) {
+    c->err = "device lacks cooperative launch or enough shared memory";
+    mk_destroy(c);
+    return MK_ERR_UNSUPPORTED;
+  }
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess || !fn) {
+    mk_destroy(c);
+    return MK_ERR_CUDA;
+  }
+  c->encode = (EncodeTiledFn)fn;
+
+  const size_t L = m.n_layers, Bm = kMaxB, H = m.hidden, d = m.head_dim;
+  c->max_pos = m.max_pages_per_seq * kPage;
+  bool okm = dalloc(&c->xs, (L + 1) * Bm * H) == cudaSuccess && dalloc(&c->q, L * Bm * m.n_q_heads * d) == cudaSuccess &&
+             dalloc(&c->knew, L * Bm * m.n_kv_heads * d) == cudaSuccess &&
+             dalloc(&c->vnew, L * Bm * m.n_kv_heads * d) == cudaSuccess && dalloc(&c->attn_o, L * Bm * od) == cudaSuccess &&
+             dalloc(&c->attn_out, L * Bm * H) == cudaSuccess && dalloc(&c->moe_out, L * Bm * H) == cudaSuccess &&
+             dalloc(&c->rlogits, L * Bm * m.n_experts) == cudaSuccess &&
+             dalloc(&c->h, L * kMaxActive * kMaxB * (size_t)m.expert_inter) == cudaSuccess &&
+             dalloc(&c->route, L) == cudaSuccess && dalloc(&c->lm_best_v, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
+             dalloc(&c->lm_best_i, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
+             dalloc(&c->rope, (size_t)c->max_pos * (d / 2)) == cudaSuccess && dalloc(&c->status, ST_WORDS) == cudaSuccess &&
+             dalloc(&c->topk_ids, L * Bm * m.top_k) == cudaSuccess && dalloc(&c->topk_w, L * Bm * m.top_k) == cudaSuccess;
+  if (!okm) {
+    cudaGetLastError();
+    mk_destroy(c);
+    return MK_ERR_OOM;
+  }
+  if (cudaHostAlloc((void**)&c->status_host, 4 * sizeof(int32_t), cudaHostAllocMapped) != cudaSuccess) {
+    c->status_host = nullptr;
+    mk_destroy(c);
+    return MK_ERR_CUDA;
+  }
+  memset(c->status_host, 0, 4 * sizeof(int32_t));
+  if (cudaHostGetDevicePointer((void**)&c->status_host_dev, c->status_host, 0) != cudaSuccess) {
+    mk_destroy(c);
+    return MK_ERR_CUDA;
+  }
+  cudaMemset(c->status, 0, ST_WORDS * sizeof(int32_t));
+  cudaMemset(c->xs, 0, (L + 1) * Bm * H * sizeof(float));
+  // RoPE table: angle pos * theta^(-2i/d), computed in fp64, stored as fp32 (cos, sin)
+  {
+    std::vector<float2> tab((size_t)c->max_pos * (d / 2));
+    for (int pos = 0; pos < c->max_pos; ++pos)
+      for (size_t i = 0; i < d / 2; ++i) {
+        const double ang = (double)pos * std::pow((double)m.rope_theta, -2.0 * (double)i / (double)d);
+        tab[(size_t)pos * (d / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    e = cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) { mk_destroy(c); return MK_ERR_CUDA; }
+  }
+  e = configure_kernels();
+  if (e != cudaSuccess) {
+    c->err = std::string("kernel configuration: ") + cudaGetErrorString(e);
+    mk_destroy(c);
+    return MK_ERR_CUDA;
+  }
+  for (int nb : {1, 2, 4, 8}) {
+    int blocks = 0;
+    e = max_blocks_per_sm(nb, &blocks);
+    if (e != cudaSuccess || blocks < 1) {
+      mk_destroy(c);
+      return MK_ERR_UNSUPPORTED;
+    }
+  }
+  *out = c;
+  return MK_OK;
+}
+
+// ------------------------------------------------------------------ scheduler
+
+namespace {
+
+struct Geo {
+  int KS, KW, RG, RS, NCS;
+};
+Geo geo_of(int K) {
+  Geo g;
+  g.KS = K < 2048 ? K : 2048;
+  g.KW = g.KS / 256;
+  g.RG = kConsumerWarps / g.KW;
+  g.RS = 8 * g.RG;
+  g.NCS = K / g.KS;
+  return g;
+}
+
+struct Assigner {
+  int n_sm;
+  std::vector<long long> load;
+  std::vector<std::vector<Task>> lists;
+  std::priority_queue<std::pair<long long, int>, std::vector<std::pair<long long, int>>, std::greater<>> heap;
+  explicit Assigner(int n) : n_sm(n), load(n, 0), lists(n) {
+    for (int s = 0; s < n; ++s) heap.push({0, s});
+  }
+  int put(const Task& t, long long bytes) {
+    auto top = heap.top();
+    heap.pop();
+    const int s = top.second;
+    lists[s].push_back(t);
+    load[s] += bytes;
+    heap.push({load[s], s});
+    return s;
+  }
+};
+
+Task mkt(int op, int layer, int a, int b, int c, int flags = 0) {
+  Task t;
+  t.op = (uint8_t)op;
+  t.flags = (uint8_t)flags;
+  t.layer = (uint16_t)layer;
+  t.a = a;
+  t.b = b;
+  t.c = c;
+  return t;
+}
+
+}  // namespace
+
+extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* seq_lens, const int32_t* block_tables) {
+  if (!c) return MK_ERR_INVALID_ARG;
+  const mk_model_cfg& m = c->cfg;
+  if (batch < 1 || batch > m.max_batch || !seq_lens || !block_tables)
+    return fail(c, MK_ERR_INVALID_ARG, "batch outside 1..max_batch or null array");
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] < 0 || seq_lens[b] >= m.max_pages_per_seq * kPage)
+      return fail(c, MK_ERR_INVALID_ARG, "sequence length negative or beyond the block table");
+  cudaDeviceSynchronize();
+  free_schedule(c);
+  const int L = m.n_layers, H = m.hidden, d = m.head_dim, nkv = m.n_kv_heads, G = m.n_q_heads / nkv;
+  const int E = m.n_experts, I = m.expert_inter, V = m.vocab, od = m.n_q_heads * d;
+  const int B = batch;
+  const int n_sm = c->n_sm;
+  const Geo gh = geo_of(H), go = geo_of(od), gi = geo_of(I);
+  const int pps = kStageBytes / (4096 * (d / 64));
+  CounterMap cmap{L, nkv, B};
+  std::vector<int32_t> cnt(cmap.count(), 0);
+
+  // attention chunks: about one (sequence, group, chunk) task per SM, whole stages each
+  long long group_pages = 0;
+  std::vector<int> npg(B);
+  for (int b = 0; b < B; ++b) {
+    npg[b] = (seq_lens[b] + kPage - 1) / kPage;
+    group_pages += (long long)npg[b] * nkv;
+  }
+  int cp = (int)((group_pages + n_sm - 1) / n_sm);
+  cp = std::max(cp, pps);
+  cp = (cp + pps - 1) / pps * pps;
+  std::vector<int32_t> chunk_pages(B, cp), n_chunks(B);
+  int max_chunks = 1;
+  for (int b = 0; b < B; ++b) {
+    n_chunks[b] = std::max(1, (npg[b] + cp - 1) / cp);
+    max_chunks = std::max(max_chunks, n_chunks[b]);
+  }
+
+  const int maxa = std::min(B * m.top_k, E);
+  const int r2 = gh.RS / 2, tiles = I / r2;
+  const int gu_per_task = std::max(1, maxa / 8);
+  const long long row_h = 2LL * H;
+  // expected live fraction of the planned expert slots (1 at batch 1)
+  const double live = maxa == m.top_k ? 1.0 : std::min(1.0, (double)E * (1.0 - std::pow(1.0 - (double)m.top_k / E, B)) / maxa);
+
+  struct Cat {
+    int op;
+    std::vector<std::pair<Task, long long>> t;
+  };
+  Assigner as(n_sm);
+  std::vector<std::vector<std::vector<Task>>> per_op;  // [launch][sm] tasks for the per-op mode
+
+  auto emit = [&](std::vector<std::pair<Task, long long>>& ts) {
+    for (auto& x : ts) as.put(x.first, x.second);
+    std::vector<std::vector<Task>> lists(n_sm);
+    for (size_t i = 0; i < ts.size(); ++i) lists[i % n_sm].push_back(ts[i].first);
+    if (!ts.empty()) per_op.push_back(std::move(lists));
+  };
+
+  for (int l = 0; l < L; ++l) {
+    std::vector<std::pair<Task, long long>> ts;
+    // router: one stage per task; the first task stores x of this layer
+    int n_router = 0;
+    for (int r0 = 0; r0 < E; r0 += gh.RS, ++n_router)
+      ts.push_back({mkt(OP_ROUTER, l, r0, std::min(gh.RS, E - r0), 0, r0 == 0 ? TF_WRITE_X : 0),
+                    std::min(gh.RS, E - r0) * row_h});
+    cnt[cmap.router_arrive(l)] = n_router;
+    cnt[cmap.route(l)] = 1;
+    emit(ts);
+    ts.clear();
+    // QKV units, group-major, one stage per task
+    const int upg = (G + 2) * (d / 8);
+    for (int g = 0; g < nkv; ++g) {
+      int n = 0;
+      for (int u = g * upg; u < (g + 1) * upg; u += gh.RG, ++n)
+        ts.push_back({mkt(OP_QKV, l, u, std::min(gh.RG, (g + 1) * upg - u), g), std::min(gh.RG, (g + 1) * upg - u) * 8 * row_h});
+      cnt[cmap.qkv(l, g)] = n;
+    }
+    emit(ts);
+    ts.clear();
+    // attention chunks
+    for (int b = 0; b < B; ++b)
+      for (int g = 0; g < nkv; ++g) {
+        for (int ch = 0; ch < n_chunks[b]; ++ch) {
+          const int p0 = ch * cp, p1 = (ch == n_chunks[b] - 1) ? npg[b] : std::min(npg[b], p0 + cp);
+          ts.push_back({mkt(OP_ATTN, l, b, g, ch), std::max(0, p1 - p0) * 2LL * kPage * d * 2});
+        }
+        cnt[cmap.attn(l, g)] = B;
+      }
+    emit(ts);
+    ts.clear();
+    // expert gate/up: units u = tile * maxa + active_rank
+    int n_gu = 0;
+    for (int u = 0; u < maxa * tiles; u += gu_per_task, ++n_gu) {
+      const int n = std::min(gu_per_task, maxa * tiles - u);
+      ts.push_back({mkt(OP_GU, l, u, n, 0), (long long)(n * live * gh.RS * row_h)});
+    }
+    cnt[cmap.gu(l)] = n_gu;
+    emit(ts);
+    ts.clear();
+    // O-proj rows
+    int n_o = 0;
+    for (int r0 = 0; r0 < H; r0 += go.RS, ++n_o)
+      ts.push_back({mkt(OP_O, l, r0, std::min(go.RS, H - r0), 0), std::min(go.RS, H - r0) * 2LL * od});
+    emit(ts);
+    ts.clear();
+    // expert down rows over all active experts
+    int n_down = 0;
+    for (int r0 = 0; r0 < H; r0 += gi.RS, ++n_down)
+      ts.push_back({mkt(OP_DOWN, l, r0, std::min(gi.RS, H - r0), 0),
+                    (long long)(std::min(gi.RS, H - r0) * 2.0 * I * maxa * live)});
+    emit(ts);
+    ts.clear();
+    cnt[cmap.layer(l)] = n_o + n_down;
+  }
+  // LM head: contiguous row ranges, whole stages, at most one task per SM
+  {
+    const int stages = (V + gh.RS - 1) / gh.RS;
+    const int per = (stages + n_sm - 1) / n_sm;
+    std::vector<std::pair<Task, long long>> ts;
+    int slot = 0;
+    for (int s0 = 0; s0 < stages; s0 += per, ++slot) {
+      const int r0 = s0 * gh.RS, r1 = std::min(V, (s0 + per) * gh.RS);
+      ts.push_back({mkt(OP_LM, L, r0, r1 - r0, slot, TF_LAST_LM | (slot == 0 ? TF_WRITE_X : 0)), (r1 - r0) * row_h});
+    }
+    c->n_lm_sm = slot;
+    cnt[cmap.lm_arrive()] = slot;
+    // the LM tasks go one per SM, on the least loaded SMs
+    emit(ts);
+  }
+
+  // flatten: megakernel lists, then per-op launches
+  std::vector<Task> all;
+  std::vector<int32_t> begin;
+  for (int s = 0; s < n_sm; ++s) {
+    begin.push_back((int32_t)all.size());
+    all.insert(all.end(), as.lists[s].begin(), as.lists[s].end());
+  }
+  begin.push_back((int32_t)all.size());
+  c->n_tasks = (int)all.size();
+  for (auto& launch : per_op) {
+    for (int s = 0; s < n_sm; ++s) {
+      begin.push_back((int32_t)all.size());
+      all.insert(all.end(), launch[s].begin(), launch[s].end());
+    }
+    begin.push_back((int32_t)all.size());
+  }
+  c->n_op_launches = (int)per_op.size();
+
+  // device upload
+  const size_t part = (size_t)L * B * nkv * max_chunks * (16 + 8 * (size_t)d);
+  bool okm = dalloc(&c->d_tasks, all.size()) == cudaSuccess && dalloc(&c->d_sm_begin, begin.size()) == cudaSuccess &&
+             dalloc(&c->d_cnt, cnt.size()) == cudaSuccess && dalloc(&c->d_chunk_pages, B) == cudaSuccess &&
+             dalloc(&c->d_n_chunks, B) == cudaSuccess && dalloc(&c->apart, part) == cudaSuccess &&
+             dalloc(&c->counters, cnt.size()) == cudaSuccess;
+  if (!okm) {
+    cudaGetLastError();
+    free_schedule(c);
+    return fail(c, MK_ERR_OOM, "schedule allocation failed");
+  }
+  CK(cudaMemcpy(c->d_tasks, all.data(), all.size() * sizeof(Task), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->d_sm_begin, begin.data(), begin.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->d_cnt, cnt.data(), cnt.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->d_chunk_pages, chunk_pages.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->d_n_chunks, n_chunks.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CK(cudaMemset(c->counters, 0, cnt.size() * sizeof(uint32_t)));
+  CK(cudaMemset(c->status, 0, ST_WORDS * sizeof(int32_t)));
+  c->n_counters = (int)cnt.size();
+  c->max_chunks = max_chunks;
+  c->B = B;
+  c->block_table = block_tables;
+  c->epoch = 0;
+  c->scheduled = true;
+  return MK_OK;
+}
+
+// ------------------------------------------------------------------ launches
+
+static mk_status tensor_maps(mk_ctx* c, const mk_kv_pages* kv) {
+  if (c->tm_k_ptr == kv->k && c->tm_v_ptr == kv->v && c->tm_pages == kv->num_pages) return MK_OK;
+  const mk_model_cfg& m = c->cfg;
+  const uint64_t rows = (uint64_t)m.n_layers * kv->num_pages * m.n_kv_heads * kPage;
+  if (rows >= (1ull << 31)) return fail(c, MK_ERR_UNSUPPORTED, "KV pool too large for 32-bit TMA coordinates");
+  cuuint64_t dims[2] = {(cuuint64_t)m.head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)m.head_dim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+  cuuint32_t estr[2] = {1, 1};
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = c->encode(i ? &c->tm.v : &c->tm.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, i ? kv->v : kv->k, dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(c, MK_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");
+  }
+  c->tm_k_ptr = kv->k;
+  c->tm_v_ptr = kv->v;
+  c->tm_pages = kv->num_pages;
+  return MK_OK;
+}
+
+static Params make_params(mk_ctx* c, const int32_t* tokens, const int32_t* positions, const mk_kv_pages* kv,
+                          float* logits, int32_t* argmax, int pos_offset) {
+  const mk_model_cfg& m = c->cfg;
+  Params p;
+  memset(&p, 0, sizeof(p));
+  p.L = m.n_layers; p.H = m.hidden; p.nq = m.n_q_heads; p.nkv = m.n_kv_heads; p.d = m.head_dim;
+  p.E = m.n_experts; p.topk = m.top_k; p.I = m.expert_inter; p.V = m.vocab; p.B = c->B;
+  p.max_pages = m.max_pages_per_seq; p.num_pages = kv->num_pages; p.n_sm = c->n_sm;
+  p.qkv_rows = (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim; p.od = m.n_q_heads * m.head_dim;
+  p.group = m.n_q_heads / m.n_kv_heads; p.max_chunks = c->max_chunks; p.n_lm_sm = c->n_lm_sm; p.max_pos = c->max_pos;
+  p.eps = m.rms_eps;
+  p.pos_offset = pos_offset;
+  p.timeout_ns = 2000000000LL;
+  p.embed = (const uint16_t*)c->w.embed; p.norm_gain = (const uint16_t*)c->w.norm_gain;
+  p.w_qkv = (const uint16_t*)c->w.w_qkv; p.w_o = (const uint16_t*)c->w.w_o; p.w_router = (const uint16_t*)c->w.w_router;
+  p.w_gate_up = (const uint16_t*)c->w.w_gate_up; p.w_down = (const uint16_t*)c->w.w_down;
+  p.final_gain = (const uint16_t*)c->w.final_gain; p.lm_head = (const uint16_t*)c->w.lm_head;
+  p.router_bias = c->w.router_bias;
+  p.rope = c->rope;
+  p.kpool = (uint16_t*)kv->k; p.vpool = (uint16_t*)kv->v; p.block_table = c->block_table;
+  p.token_ids = tokens; p.positions = positions; p.logits = logits; p.argmax_out = argmax;
+  p.tasks = c->d_tasks; p.sm_begin = c->d_sm_begin; p.cnt_per_step = c->d_cnt;
+  p.chunk_pages = c->d_chunk_pages; p.n_chunks = c->d_n_chunks;
+  p.xs = c->xs; p.q = c->q; p.knew = c->knew; p.vnew = c->vnew; p.apart = c->apart; p.attn_o = c->attn_o;
+  p.attn_out = c->attn_out; p.rlogits = c->rlogits; p.h = c->h; p.moe_out = c->moe_out; p.route = c->route;
+  p.lm_best_v = c->lm_best_v; p.lm_best_i = c->lm_best_i; p.counters = c->counters; p.status = c->status;
+  p.status_host = c->status_host_dev; p.topk_ids = c->topk_ids; p.topk_w = c->topk_w;
+  p.trace = c->trace; p.trace_count = c->trace_count; p.trace_cap = c->trace_cap;
+  return p;
+}
+
+static mk_status check_latched(mk_ctx* c) {
+  const int code = *(volatile int32_t*)c->status_host;
+  if (code != 0) return fail(c, (mk_status)code, "device error latched by an earlier step (call mk_status_sync)");
+  return MK_OK;
+}
+
+static mk_status run_step(mk_ctx* c, Params& p, cudaStream_t st) {
+  ++c->epoch;
+  p.epoch = c->epoch;
+  if (c->trace) CK(cudaMemsetAsync(c->trace_count, 0, sizeof(unsigned long long), st));
+  if (c->mode == MK_MODE_MEGAKERNEL) {
+    p.sm_begin = c->d_sm_begin;
+    CK(launch_decode(p, c->tm, st));
+  } else {
+    for (int i = 0; i < c->n_op_launches; ++i) {
+      p.sm_begin = c->d_sm_begin + (size_t)(i + 1) * (c->n_sm + 1);
+      CK(launch_decode(p, c->tm, st));
+    }
+  }
+  return MK_OK;
+}
+
+static mk_status step_checks(mk_ctx* c, const mk_kv_pages* kv) {
+  if (!c->scheduled) return fail(c, MK_ERR_NO_SCHEDULE, "mk_build_schedule has not succeeded");
+  if (!kv || !kv->k || !kv->v || kv->num_pages <= 0 || !aligned16(kv->k) || !aligned16(kv->v))
+    return fail(c, MK_ERR_INVALID_ARG, "bad KV pages");
+  mk_status s = check_latched(c);
+  if (s != MK_OK) return s;
+  return tensor_maps(c, kv);
+}
+
+extern "C" mk_status mk_decode_step(mk_ctx* c, const int32_t* token_ids, const int32_t* positions, const mk_kv_pages* kv,
+                                    float* logits_out, int32_t* argmax_out, void* stream) {
+  if (!c) return MK_ERR_INVALID_ARG;
+  if (!token_ids || !positions) return fail(c, MK_ERR_INVALID_ARG, "null token_ids or positions");
+  mk_status s = step_checks(c, kv);
+  if (s != MK_OK) return s;
+  Params p = make_params(c, token_ids, positions, kv, logits_out, argmax_out, 0);
+  return run_step(c, p, (cudaStream_t)stream);
+}
+
+extern "C" mk_status mk_decode_greedy(mk_ctx* c, int32_t n_steps, const int32_t* token_ids, const int32_t* positions,
+                                      const mk_kv_pages* kv, float* logits_out, int32_t* tokens_out, void* stream) {
+  if (!c) return MK_ERR_INVALID_ARG;
+  if (!token_ids || !positions || !tokens_out || n_steps < 1)
+    return fail(c, MK_ERR_INVALID_ARG, "null argument or n_steps < 1");
+  mk_status s = step_checks(c, kv);
+  if (s != MK_OK) return s;
+  for (int i = 0; i < n_steps; ++i) {
+    const int32_t* tok = i == 0 ? token_ids : tokens_out + (size_t)(i - 1) * c->B;
+    Params p = make_params(c, tok, positions, kv, i == n_steps - 1 ? logits_out : nullptr,
+                           tokens_out + (size_t)i * c->B, i);
+    s = run_step(c, p, (cudaStream_t)stream);
+    if (s != MK_OK) return s;
+  }
+  return MK_OK;
+}
+
+extern "C" mk_status mk_status_sync(mk_ctx* c) {
+  if (!c) return MK_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(c, e, "cudaDeviceSynchronize");
+  int32_t st[ST_WORDS];
+  e = cudaMemcpy(st, c->status, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(c, e, "status copy");
+  if (st[ST_CODE] == 0) return MK_OK;
+  char buf[160];
+  snprintf(buf, sizeof(buf), "device error %d (aux %d, %d)", st[ST_CODE], st[ST_AUX0], st[ST_AUX1]);
+  c->err = buf;
+  cudaMemset(c->status, 0, ST_WORDS * sizeof(int32_t));
+  *(volatile int32_t*)c->status_host = 0;
+  if (c->counters) cudaMemset(c->counters, 0, (size_t)c->n_counters * sizeof(uint32_t));
+  c->epoch = 0;
+  cudaDeviceSynchronize();
+  return (mk_status)st[ST_CODE];
+}
+
+extern "C" const char* mk_last_error(const mk_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+extern "C" mk_status mk_set_mode(mk_ctx* c, int mode) {
+  if (!c || (mode != MK_MODE_MEGAKERNEL && mode != MK_MODE_PER_OP)) return MK_ERR_INVALID_ARG;
+  c->mode = mode;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_enable_trace(mk_ctx* c, void* buf, size_t bytes) {
+  if (!c) return MK_ERR_INVALID_ARG;
+  if (!buf) {
+    c->trace = nullptr;
+    c->trace_count = nullptr;
+    c->trace_cap = 0;
+    return MK_OK;
+  }
+  if (bytes < 16 + sizeof(mk_trace_entry) || !aligned16(buf)) return fail(c, MK_ERR_INVALID_ARG, "trace buffer too small");
+  c->trace_count = (unsigned long long*)buf;
+  c->trace = (mk_trace_entry*)((char*)buf + 16);
+  c->trace_cap = (long long)((bytes - 16) / sizeof(mk_trace_entry));
+  return MK_OK;
+}
+
+extern "C" mk_status mk_get_activations(const mk_ctx* c, mk_activations* out) {
+  if (!c || !out) return MK_ERR_INVALID_ARG;
+  out->x = c->xs;
+  out->q = c->q;
+  out->attn = c->attn_o;
+  out->attn_out = c->attn_out;
+  out->moe_out = c->moe_out;
+  out->router = c->rlogits;
+  out->topk_ids = c->topk_ids;
+  out->topk_w = c->topk_w;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_get_launch_info(const mk_ctx* c, int32_t* n_sm, int32_t* tasks, int32_t* launches) {
+  if (!c) return MK_ERR_INVALID_ARG;
+  if (n_sm) *n_sm = c->n_sm;
+  if (tasks) *tasks = c->scheduled ? c->n_tasks : 0;
+  if (launches) *launches = c->mode == MK_MODE_MEGAKERNEL ? 1 : c->n_op_launches;
+  return MK_OK;
+}

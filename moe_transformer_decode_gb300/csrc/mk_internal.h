@@ -1,0 +1,116 @@
+// Internal layout shared by the host scheduler (mk_host.cpp) and the persistent kernel
+// (mk_kernel.cu): task descriptors, dependency counters, routing records, kernel params.
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+#include "../../include/mk.h"
+
+namespace mk {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kStageBytes = 32768;
+constexpr int kStages = 6;
+constexpr int kMaxB = 8;
+constexpr int kMaxK = 8;
+constexpr int kMaxActive = kMaxB * kMaxK;  // distinct experts a batch can route to
+constexpr int kMaxExperts = 256;
+constexpr int kPage = 16;
+
+// Opcodes of the decode graph.
+enum Op : uint8_t {
+  OP_ROUTER = 1,  // router logits for a block of experts; last one computes top-k routing
+  OP_QKV = 2,     // QKV rows + RoPE + KV append, a range of 8-row units of one KV group
+  OP_ATTN = 3,    // paged GQA attention of one (sequence, KV group, chunk); last chunk combines
+  OP_GU = 4,      // expert gate/up rows + SiLU*mul, a range of (tile, active-expert) units
+  OP_O = 5,       // O-proj rows, each warp released by its KV group's counter
+  OP_DOWN = 6,    // expert down rows over all active experts + weighted combine
+  OP_LM = 7       // LM-head rows + running argmax; the last LM task of the step reduces
+};
+enum TaskFlag : uint8_t {
+  TF_WRITE_X = 1,  // this task's block stores the residual stream x of its layer
+  TF_LAST_LM = 2   // this SM's last LM task: publish its argmax candidate
+};
+
+struct Task {
+  uint8_t op, flags;
+  uint16_t layer;
+  int32_t a, b, c;
+};
+static_assert(sizeof(Task) == 16, "task descriptor is 16 bytes");
+
+// Routing of one layer for the whole batch (written by the last router task).
+struct Route {
+  int32_t n_active;
+  int32_t pad[3];
+  int32_t expert[kMaxActive];        // distinct routed experts, ascending id
+  uint32_t mask[kMaxActive];         // bit b: token b routed to it
+  float w[kMaxActive][kMaxB];        // routing weight (0 where not routed)
+  int32_t ids[kMaxB][kMaxK];         // per token, top-k in rank order
+  float wk[kMaxB][kMaxK];
+};
+
+// Counter indices (uint32, compared wrap-safely against epoch * per-step count).
+struct CounterMap {
+  int L, nkv, B;
+  __host__ __device__ int layer(int l) const { return l; }
+  __host__ __device__ int qkv(int l, int g) const { return L + l * nkv + g; }
+  __host__ __device__ int router_arrive(int l) const { return L + L * nkv + l; }
+  __host__ __device__ int route(int l) const { return 2 * L + L * nkv + l; }
+  __host__ __device__ int gu(int l) const { return 3 * L + L * nkv + l; }
+  __host__ __device__ int attn(int l, int g) const { return 4 * L + L * nkv + l * nkv + g; }
+  __host__ __device__ int attn_arrive(int l, int b, int g) const { return 4 * L + 2 * L * nkv + (l * B + b) * nkv + g; }
+  __host__ __device__ int lm_arrive() const { return 4 * L + 2 * L * nkv + L * B * nkv; }
+  __host__ __device__ int count() const { return lm_arrive() + 1; }
+};
+
+// Device status words.
+enum { ST_CODE = 0, ST_AUX0 = 1, ST_AUX1 = 2, ST_ABORT = 3, ST_WORDS = 8 };
+
+struct Params {
+  // shape
+  int L, H, nq, nkv, d, E, topk, I, V, B, max_pages, num_pages, n_sm;
+  int qkv_rows, od, group, max_chunks, n_lm_sm, max_pos;
+  float eps;
+  uint32_t epoch;
+  int pos_offset;  // added to positions[b] (greedy loop)
+  long long timeout_ns;
+  // weights (bf16 bits)
+  const uint16_t *embed, *norm_gain, *w_qkv, *w_o, *w_router, *w_gate_up, *w_down, *final_gain, *lm_head;
+  const float* router_bias;
+  const float2* rope;  // [max_pos][d/2] (cos, sin)
+  // KV cache
+  uint16_t *kpool, *vpool;
+  const int32_t* block_table;  // [B][max_pages]
+  // step inputs / outputs
+  const int32_t* token_ids;
+  const int32_t* positions;
+  float* logits;
+  int32_t* argmax_out;
+  // schedule
+  const Task* tasks;
+  const int32_t* sm_begin;     // [n_sm + 1] offsets into tasks
+  const int32_t* cnt_per_step; // [counters] increments per step
+  const int32_t* chunk_pages;  // [B] pages per attention chunk
+  const int32_t* n_chunks;     // [B]
+  // workspace
+  float *xs, *q, *knew, *vnew, *apart, *attn_o, *attn_out, *rlogits, *h, *moe_out;
+  Route* route;
+  float* lm_best_v;
+  int32_t* lm_best_i;
+  int32_t* topk_ids;  // [L][B][topk]
+  float* topk_w;
+  uint32_t* counters;
+  int32_t* status;
+  int32_t* status_host;  // mapped host copy of the status code (written only on error)
+  mk_trace_entry* trace;
+  unsigned long long* trace_count;
+  long long trace_cap;
+};
+
+struct TensorMaps {
+  CUtensorMap k, v;  // KV pools as 2D [rows][head_dim] bf16, box {64, 16}, 128B swizzle
+};
+
+}  // namespace mk

@@ -1,0 +1,1322 @@
+// The persistent decode-step kernel for sm_103a: one CTA per SM, one producer warp that
+// streams weights and KV pages into a shared-memory ring with bulk / tensor TMA copies,
+// and eight consumer warps that run the opcodes. Dependencies between tasks on different
+// SMs are acquire/release counters in global memory with bounded waits (no grid barrier).
+//
+// Decode step and fused opcodes: Cohere megakernel news pages, aimodeling.com
+// "cohere-megakernel-north-mini-code-h100", section "One persistent kernel for the whole
+// decode step" (task list in global memory, per-producer counters, O-proj released per KV
+// group, weight prefetch ahead of dependencies, parallel-layer backfill) and
+// aibriefing.imbch.dev article 8171681, section "Key Technologies and Architecture"
+// (fused RoPE and SiLU-multiply, fixed-size task descriptors).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 1D bulk copy global -> shared, completion counted on an mbarrier (16-byte aligned, size % 16 == 0)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// 2D tiled tensor copy global -> shared (x: innermost coordinate in elements)
+__device__ __forceinline__ void tma_2d_g2s(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+// pack two floats as bf16 (lo in the low half), with their rounding residuals as a second pair
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  uint16_t h0 = f2bf(x0), h1 = f2bf(x1);
+  uint16_t l0 = f2bf(x0 - bf2f(h0)), l1 = f2bf(x1 - bf2f(h1));
+  hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
+  lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
+}
+
+// ------------------------------------------------------------------ errors and waits
+
+__device__ __noinline__ void report(const Params& p, int code, int aux0, int aux1) {
+  if (atomicCAS(&p.status[ST_CODE], 0, code) == 0) {
+    atomicExch(&p.status[ST_AUX0], aux0);
+    atomicExch(&p.status[ST_AUX1], aux1);
+    if (p.status_host) *reinterpret_cast<volatile int32_t*>(p.status_host) = code;
+  }
+  if (code == MK_ERR_DEVICE_TIMEOUT) atomicExch(&p.status[ST_ABORT], 1);
+}
+__device__ __forceinline__ bool aborted(const Params& p) {
+  return *reinterpret_cast<volatile int*>(&p.status[ST_ABORT]) != 0;
+}
+__device__ __forceinline__ uint32_t target_of(const Params& p, int idx) {
+  return p.epoch * (uint32_t)p.cnt_per_step[idx];
+}
+
+// single-thread bounded wait; false on timeout or abort
+__device__ bool wait_counter(const Params& p, int idx) {
+  const uint32_t tgt = target_of(p, idx);
+  const uint32_t* c = p.counters + idx;
+  if ((int32_t)(ld_acquire(c) - tgt) >= 0) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 0;; ++it) {
+    if ((int32_t)(ld_acquire(c) - tgt) >= 0) return true;
+    if ((it & 31) == 31) {
+      if (aborted(p)) return false;
+      if ((long long)(gtimer() - t0) > p.timeout_ns) {
+        report(p, MK_ERR_DEVICE_TIMEOUT, idx, (int)(ld_acquire(c) - (tgt - (uint32_t)p.cnt_per_step[idx])));
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+// whole-warp wait (every lane performs the acquire)
+__device__ bool warp_wait(const Params& p, int idx) {
+  const uint32_t tgt = target_of(p, idx);
+  const uint32_t* c = p.counters + idx;
+  if (__all_sync(0xffffffffu, (int32_t)(ld_acquire(c) - tgt) >= 0)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 0;; ++it) {
+    if (__all_sync(0xffffffffu, (int32_t)(ld_acquire(c) - tgt) >= 0)) return true;
+    if ((it & 31) == 31) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (aborted(p)) stop = 1;
+        else if ((long long)(gtimer() - t0) > p.timeout_ns) {
+          report(p, MK_ERR_DEVICE_TIMEOUT, idx, (int)(ld_acquire(c) - (tgt - (uint32_t)p.cnt_per_step[idx])));
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+    __nanosleep(64);
+  }
+}
+// bounded mbarrier wait
+__device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15) == 15) {
+      if (aborted(p)) return false;
+      if ((long long)(gtimer() - t0) > p.timeout_ns) {
+        report(p, MK_ERR_DEVICE_TIMEOUT, -1, (int)parity);
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ geometry
+
+// A GEMV stage is RS rows x KS columns (row-major bf16 in shared memory). Each consumer warp
+// owns 8 rows ("row group") and a 256-column slice; a lane owns 8 consecutive columns.
+struct Geo {
+  int KS, KW, RG, RS, NCS;
+};
+__device__ __forceinline__ Geo geo_of(int K) {
+  Geo g;
+  g.KS = K < 2048 ? K : 2048;
+  g.KW = g.KS / 256;
+  g.RG = kConsumerWarps / g.KW;
+  g.RS = 8 * g.RG;
+  g.NCS = K / g.KS;
+  return g;
+}
+
+// QKV unit u (8 output rows). Units are group-major: for KV group g, the q heads of g, then
+// k head g, then v head g; each q/k head has d/8 units of 4 RoPE pairs (i, i + d/2).
+struct QkvUnit {
+  int kind;   // 0 q, 1 k, 2 v
+  int head;   // q head, or kv head for k / v
+  int j;      // unit index within the head
+  int row0;   // first row in W_qkv
+};
+__device__ __forceinline__ QkvUnit qkv_unit(const Params& p, int u) {
+  const int dd8 = p.d / 8, upg = (p.group + 2) * dd8;
+  const int g = u / upg, r = u % upg;
+  QkvUnit q;
+  if (r < p.group * dd8) {
+    q.kind = 0; q.head = g * p.group + r / dd8; q.j = r % dd8; q.row0 = q.head * p.d + 4 * q.j;
+  } else if (r < (p.group + 1) * dd8) {
+    q.kind = 1; q.head = g; q.j = r - p.group * dd8; q.row0 = (p.nq + g) * p.d + 4 * q.j;
+  } else {
+    q.kind = 2; q.head = g; q.j = r - (p.group + 1) * dd8; q.row0 = (p.nq + p.nkv + g) * p.d + 8 * q.j;
+  }
+  return q;
+}
+
+__device__ __forceinline__ int pos_of(const Params& p, int b) { return p.positions[b] + p.pos_offset; }
+
+struct AttnRange {
+  int cp0, cp1, pos_end;
+};
+__device__ __forceinline__ AttnRange attn_range(const Params& p, int b, int c) {
+  const int pos = pos_of(p, b);
+  const int npg = (pos + kPage - 1) / kPage;
+  const int cpp = p.chunk_pages[b], nch = p.n_chunks[b];
+  AttnRange r;
+  r.cp0 = c * cpp;
+  r.cp1 = (c == nch - 1) ? npg : min(r.cp0 + cpp, npg);
+  if (r.cp1 < r.cp0) r.cp1 = r.cp0;
+  r.pos_end = pos;
+  return r;
+}
+__device__ __forceinline__ int attn_pps(const Params& p) { return kStageBytes / (4096 * (p.d / 64)); }
+
+__device__ __forceinline__ int max_active(const Params& p) { return min(p.B * p.topk, p.E); }
+
+// ------------------------------------------------------------------ shared memory
+
+struct Misc {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t cbar;                     // consumer-warps barrier (8 arrivals per phase)
+  float red[kConsumerWarps][64];     // cross-warp partial sums
+  float res[64 * kMaxB];             // reduced stage results [RS][B]
+  float norm[kConsumerWarps][kMaxB]; // sum of squares partials
+  int flag;
+  int n_active;
+  int route_expert[kMaxActive];
+  uint32_t route_mask[kMaxActive];
+  float route_w[kMaxActive][kMaxB];
+  uint32_t emask[kMaxExperts];
+  int erank[kMaxExperts];
+  int ids[kMaxB][kMaxK];
+  float wk[kMaxB][kMaxK];
+};
+constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + ((int)sizeof(Misc) + 127) / 128 * 128;
+
+struct Ring {
+  uint32_t data;  // shared address of stage 0
+  uint32_t full, empty;
+  uint32_t it;
+};
+__device__ __forceinline__ uint32_t slot_addr(const Ring& r) { return r.data + (r.it % kStages) * kStageBytes; }
+
+// ------------------------------------------------------------------ producer
+
+struct Producer {
+  const Params& p;
+  const TensorMaps& tm;
+  Ring r;
+  bool ok;
+  uint32_t bar, dst;
+
+  __device__ Producer(const Params& p_, const TensorMaps& tm_, Ring r_) : p(p_), tm(tm_), r(r_), ok(true) {}
+
+  __device__ bool begin(uint32_t bytes) {
+    const uint32_t s = r.it % kStages;
+    const uint32_t parity = ((r.it / kStages) & 1u) ^ 1u;
+    if (!mbar_wait(p, r.empty + 8 * s, parity)) return false;
+    bar = r.full + 8 * s;
+    dst = r.data + s * kStageBytes;
+    mbar_expect_tx(bar, bytes);
+    return true;
+  }
+  __device__ void end() { ++r.it; }
+
+  __device__ bool gemv_rows(const uint16_t* base, int rows, int row_bytes) {
+    const uint32_t bytes = (uint32_t)rows * row_bytes;
+    if (!begin(bytes)) return false;
+    bulk_g2s(dst, base, bytes, bar);
+    end();
+    return true;
+  }
+
+  __device__ bool run_task(const Task& t) {
+    const int l = t.layer;
+    switch (t.op) {
+      case OP_ROUTER:
+      case OP_LM: {
+        const Geo g = geo_of(p.H);
+        const uint16_t* W = t.op == OP_ROUTER ? p.w_router + (size_t)l * p.E * p.H : p.lm_head;
+        for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS)
+          if (!gemv_rows(W + (size_t)r0 * p.H, min(g.RS, t.a + t.b - r0), p.H * 2)) return false;
+        return true;
+      }
+      case OP_QKV: {
+        const Geo g = geo_of(p.H);
+        const int us = g.RG;  // units per stage
+        const uint16_t* W = p.w_qkv + (size_t)l * p.qkv_rows * p.H;
+        for (int u0 = t.a; u0 < t.a + t.b; u0 += us) {
+          const int nu = min(us, t.a + t.b - u0);
+          if (!begin((uint32_t)nu * 8 * p.H * 2)) return false;
+          for (int i = 0; i < nu; ++i) {
+            const QkvUnit q = qkv_unit(p, u0 + i);
+            const uint32_t d0 = dst + (uint32_t)i * 8 * p.H * 2;
+            if (q.kind == 2) {
+              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 8 * p.H * 2, bar);
+            } else {
+              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 4 * p.H * 2, bar);
+              bulk_g2s(d0 + 4 * p.H * 2, W + (size_t)(q.row0 + p.d / 2) * p.H, 4 * p.H * 2, bar);
+            }
+          }
+          end();
+        }
+        return true;
+      }
+      case OP_ATTN: {
+        const int b = t.a, g = t.b;
+        const AttnRange ar = attn_range(p, b, t.c);
+        const int pps = attn_pps(p), halves = p.d / 64;
+        for (int pg0 = ar.cp0; pg0 < ar.cp1; pg0 += pps) {
+          const int np = min(pps, ar.cp1 - pg0);
+          int good = 0;
+          int ids[8];
+          for (int i = 0; i < np; ++i) {
+            int id = (pg0 + i < p.max_pages) ? p.block_table[b * p.max_pages + pg0 + i] : -1;
+            if (id < 0 || id >= p.num_pages) {
+              report(p, MK_ERR_BAD_PAGE, b, pg0 + i);
+              id = -1;
+            } else {
+              ++good;
+            }
+            ids[i] = id;
+          }
+          if (!begin((uint32_t)good * 2 * halves * 2048)) return false;
+          for (int i = 0; i < np; ++i) {
+            if (ids[i] < 0) continue;
+            const int row = ((l * p.num_pages + ids[i]) * p.nkv + g) * kPage;
+            const uint32_t pb = dst + (uint32_t)i * 4096 * halves;
+            for (int h = 0; h < halves; ++h) {
+              tma_2d_g2s(pb + h * 2048, &tm.k, h * 64, row, bar);
+              tma_2d_g2s(pb + (halves + h) * 2048, &tm.v, h * 64, row, bar);
+            }
+          }
+          end();
+        }
+        return true;
+      }
+      case OP_GU: {
+        if (!wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l))) return false;
+        const Route* rt = p.route + l;
+        const int na = __ldcg(&rt->n_active), maxa = max_active(p);
+        const Geo g = geo_of(p.H);
+        const int r2 = g.RS / 2;
+        for (int u = t.a; u < t.a + t.b; ++u) {
+          const int a = u % maxa, tile = u / maxa;
+          if (a >= na) continue;
+          const int e = __ldcg(&rt->expert[a]);
+          const uint16_t* W = p.w_gate_up + ((size_t)l * p.E + e) * 2 * p.I * p.H;
+          if (!begin((uint32_t)g.RS * p.H * 2)) return false;
+          bulk_g2s(dst, W + (size_t)tile * r2 * p.H, r2 * p.H * 2, bar);
+          bulk_g2s(dst + r2 * p.H * 2, W + (size_t)(p.I + tile * r2) * p.H, r2 * p.H * 2, bar);
+          end();
+        }
+        return true;
+      }
+      case OP_O: {
+        const Geo g = geo_of(p.od);
+        const uint16_t* W = p.w_o + ((size_t)l * p.H + t.a) * p.od;
+        for (int cs = 0; cs < g.NCS; ++cs) {
+          if (g.NCS == 1) {
+            if (!gemv_rows(W, t.b, p.od * 2)) return false;
+          } else {
+            if (!begin((uint32_t)t.b * g.KS * 2)) return false;
+            for (int r = 0; r < t.b; ++r)
+              bulk_g2s(dst + (uint32_t)r * g.KS * 2, W + (size_t)r * p.od + cs * g.KS, g.KS * 2, bar);
+            end();
+          }
+        }
+        return true;
+      }
+      case OP_DOWN: {
+        if (!wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l))) return false;
+        const Route* rt = p.route + l;
+        const int na = __ldcg(&rt->n_active);
+        for (int a = 0; a < na; ++a) {
+          const int e = __ldcg(&rt->expert[a]);
+          const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + t.a) * p.I;
+          if (!gemv_rows(W, t.b, p.I * 2)) return false;
+        }
+        return true;
+      }
+    }
+    return true;
+  }
+
+  // Abort path: wait (bounded) until every copy this warp issued has landed.
+  __device__ void drain() {
+    const uint32_t n = r.it < (uint32_t)kStages ? r.it : (uint32_t)kStages;
+    for (uint32_t k = 0; k < n; ++k) {
+      const uint32_t it = r.it - 1 - k;
+      const uint32_t s = it % kStages, parity = (it / kStages) & 1u;
+      const uint64_t t0 = gtimer();
+      while (!mbar_try_wait(r.full + 8 * s, parity)) {
+        if ((long long)(gtimer() - t0) > p.timeout_ns) break;
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ consumer building blocks
+
+// Halving butterfly: sums v[N] over the 32 lanes. For N <= 32 the lane ends with the total
+// of index lane >> (5 - log2 N) in v[0]; for N = 64 with indices 2*lane and 2*lane+1.
+template <int C, int O>
+struct LaneReduce {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (O > 0) {
+      if constexpr (C > 1) {
+        const bool up = (lane & O) != 0;
+#pragma unroll
+        for (int i = 0; i < C / 2; ++i) {
+          const float send = up ? v[i] : v[i + C / 2];
+          const float keep = up ? v[i + C / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+        }
+        LaneReduce<C / 2, O / 2>::run(v, lane);
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+        LaneReduce<1, O / 2>::run(v, lane);
+      }
+    }
+  }
+};
+
+template <int NB>
+__device__ __forceinline__ void warp_partials_to_smem(float (&acc)[8][NB], float* red_w, int lane) {
+  constexpr int N = 8 * NB;
+  float v[N];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) v[r * NB + b] = acc[r][b];
+  LaneReduce<N, 16>::run(v, lane);
+  if constexpr (N <= 32) {
+    constexpr int rep = 32 / N;
+    if ((lane & (rep - 1)) == 0) red_w[lane / rep] = v[0];
+  } else {
+    red_w[2 * lane] = v[0];
+    red_w[2 * lane + 1] = v[1];
+  }
+}
+
+// Sum the row groups' k-slices into res[row * NB + b] for rows < rows. Caller syncs around.
+template <int NB>
+__device__ __forceinline__ void cross_warp_reduce(Misc& m, const Geo& g, int rows) {
+  for (int t = threadIdx.x; t < rows * NB; t += 256) {
+    const int r = t / NB, b = t % NB, rg = r / 8;
+    float s = 0.f;
+    for (int k = 0; k < g.KW; ++k) s += m.red[rg * g.KW + k][(r % 8) * NB + b];
+    m.res[t] = s;
+  }
+}
+
+// Accumulate one stage's rows for this warp: acc[r][b] += W[row][cols] . act[b][cols]
+template <int NB>
+__device__ __forceinline__ void gemv_stage(const uint8_t* stage, const Geo& g, int rg, int ks, int lane, int rows_valid,
+                                           const float (&act)[NB][8], float (&acc)[8][NB], uint32_t bmask) {
+  const uint8_t* base = stage + (size_t)(rg * 8) * g.KS * 2 + (size_t)(ks * 256 + lane * 8) * 2;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    if (r < rows_valid) {
+      const uint4 w = *reinterpret_cast<const uint4*>(base + (size_t)r * g.KS * 2);
+      float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y), bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (bmask & (1u << b)) {
+          float s = acc[r][b];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s = fmaf(wf[i], act[b][i], s);
+          acc[r][b] = s;
+        }
+      }
+    }
+  }
+}
+
+template <int NB>
+__device__ __forceinline__ void zero_acc(float (&acc)[8][NB]) {
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
+}
+
+__device__ __forceinline__ void load8(const float* src, float (&dst)[8]) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+  const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 1);
+  dst[0] = a.x; dst[1] = a.y; dst[2] = a.z; dst[3] = a.w;
+  dst[4] = b.x; dst[5] = b.y; dst[6] = b.z; dst[7] = b.w;
+}
+
+__device__ __forceinline__ void trace_task(const Params& p, const Task& t, uint64_t t0, uint64_t t1) {
+  if (!p.trace || threadIdx.x != 0) return;
+  const unsigned long long i = atomicAdd(p.trace_count, 1ull);
+  if ((long long)i >= p.trace_cap) return;
+  const uint64_t t2 = gtimer();
+  mk_trace_entry e;
+  e.t_start_ns = t0;
+  e.wait_ns = (uint32_t)(t1 - t0);
+  e.run_ns = (uint32_t)(t2 - t1);
+  e.sm = (uint16_t)blockIdx.x;
+  e.op = t.op;
+  e.layer = t.layer;
+  e.pad = 0;
+  e.a = t.a;
+  e.b = t.b;
+  p.trace[i] = e;
+}
+
+// ------------------------------------------------------------------ consumer
+
+template <int NB>
+struct Consumer {
+  const Params& p;
+  Misc& m;
+  Ring r;
+  CounterMap cm;
+  int warp, lane;
+  bool ok;
+  uint32_t cbar, cphase;
+  int n_layer;          // layer whose normalized input is held in `nact` (-1 none)
+  float nact[NB][8];    // this lane's 8 columns of the normalized input, per token
+  float lm_best[NB];    // running LM-head argmax (threads < B)
+  int lm_idx[NB];
+  uint64_t t_start, t_ready;
+
+  __device__ Consumer(const Params& p_, Misc& m_, Ring r_)
+      : p(p_), m(m_), r(r_), cm{p_.L, p_.nkv, p_.B}, ok(true), n_layer(-1) {
+    warp = threadIdx.x / 32;
+    lane = threadIdx.x % 32;
+    cbar = smem_addr(&m_.cbar);
+    cphase = 0;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      lm_best[b] = -INFINITY;
+      lm_idx[b] = 0x7fffffff;
+    }
+  }
+
+  __device__ const uint8_t* acquire() {
+    const uint32_t s = r.it % kStages, parity = (r.it / kStages) & 1u;
+    if (!mbar_wait(p, r.full + 8 * s, parity)) {
+      ok = false;
+      return nullptr;
+    }
+    return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(r.data + s * kStageBytes));
+  }
+  __device__ void release() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(r.empty + 8 * (r.it % kStages));
+    ++r.it;
+  }
+  __device__ uint32_t bmask_all() const { return (1u << p.B) - 1u; }
+
+  // Barrier of the 8 consumer warps on an mbarrier, with the same time limit as every other
+  // wait: a warp that gives up (timeout or abort) leaves the kernel and the rest follow.
+  __device__ bool csync() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cbar);
+    const bool done = mbar_wait(p, cbar, cphase);
+    cphase ^= 1u;
+    if (!done) ok = false;
+    return done;
+  }
+
+  // The normalized input of layer l (l == L: the final norm before the LM head), for this
+  // lane's 8 columns: x = residual stream (embedding at l = 0), n = x / rms(x) * gain.
+  __device__ void load_norm(int l, bool write_x) {
+    const Geo g = geo_of(p.H);
+    const int ks = warp % g.KW;
+    const int col = ks * 256 + lane * 8;
+    if (l > 0 && !warp_wait(p, cm.layer(l - 1))) {
+      ok = false;
+      return;
+    }
+    float x[NB][8];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[b][i] = 0.f;
+      if (b >= p.B) continue;
+      if (l == 0) {
+        int tok = p.token_ids[b];
+        if (tok < 0 || tok >= p.V) {
+          if (lane == 0 && warp == 0) report(p, MK_ERR_BAD_TOKEN, b, tok);
+          tok = 0;
+        }
+        const uint4 w = *reinterpret_cast<const uint4*>(p.embed + (size_t)tok * p.H + col);
+        x[b][0] = bf_lo(w.x); x[b][1] = bf_hi(w.x); x[b][2] = bf_lo(w.y); x[b][3] = bf_hi(w.y);
+        x[b][4] = bf_lo(w.z); x[b][5] = bf_hi(w.z); x[b][6] = bf_lo(w.w); x[b][7] = bf_hi(w.w);
+      } else {
+        float a[8], mo[8];
+        const size_t o = ((size_t)(l - 1) * p.B + b) * p.H + col;
+        load8(p.xs + o, x[b]);
+        load8(p.attn_out + o, a);
+        load8(p.moe_out + o, mo);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[b][i] = (x[b][i] + a[i]) + mo[i];
+      }
+    }
+    float ss[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s = fmaf(x[b][i], x[b][i], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      ss[b] = s;
+    }
+    if (lane == 0 && warp < g.KW)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) m.norm[warp][b] = ss[b];
+    if (!csync()) return;
+    const uint16_t* gain = (l < p.L) ? p.norm_gain + (size_t)l * p.H : p.final_gain;
+    const uint4 gw = *reinterpret_cast<const uint4*>(gain + col);
+    const float gf[8] = {bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y),
+                         bf_lo(gw.z), bf_hi(gw.z), bf_lo(gw.w), bf_hi(gw.w)};
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      float tot = 0.f;
+      for (int k = 0; k < g.KW; ++k) tot += m.norm[k][b];
+      const float rinv = 1.0f / sqrtf(tot / (float)p.H + p.eps);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nact[b][i] = x[b][i] * rinv * gf[i];
+    }
+    if (write_x && warp < g.KW) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (b >= p.B) continue;
+        float4* dst = reinterpret_cast<float4*>(p.xs + ((size_t)l * p.B + b) * p.H + col);
+        __stcg(dst, make_float4(x[b][0], x[b][1], x[b][2], x[b][3]));
+        __stcg(dst + 1, make_float4(x[b][4], x[b][5], x[b][6], x[b][7]));
+      }
+    }
+    if (!csync()) return;
+    n_layer = l;
+  }
+
+  __device__ void ensure_norm(int l, bool write_x) {
+    if (n_layer != l) load_norm(l, write_x);
+  }
+
+  // one GEMV stage against the held normalized input, reduced into m.res [rows][NB]
+  __device__ bool norm_gemv_stage(const Geo& g, int rows, uint32_t bmask) {
+    const int rg = warp / g.KW, ks = warp % g.KW;
+    float acc[8][NB];
+    zero_acc(acc);
+    const uint8_t* st = acquire();
+    if (!st) return false;
+    if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, rows - rg * 8), nact, acc, bmask);
+    release();
+    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[warp], lane);
+    if (!csync()) return false;
+    cross_warp_reduce<NB>(m, g, rows);
+    return csync();
+  }
+
+  __device__ void release_counter(int idx) {
+    if (!csync()) return;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      red_release_add(p.counters + idx, 1u);
+    }
+  }
+  // arrival on `idx`; true in every consumer thread of the task that arrived last
+  __device__ bool arrive_last(int idx, int count) {
+    if (!csync()) return false;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const uint32_t old = atom_acq_rel_add(p.counters + idx, 1u);
+      m.flag = ((old + 1u) % (uint32_t)count) == 0u;
+    }
+    if (!csync()) return false;
+    return m.flag != 0;
+  }
+
+  // ---------------------------------------------------------------- opcodes
+
+  __device__ void op_router(const Task& t) {
+    const int l = t.layer;
+    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
+    if (!ok) return;
+    t_ready = gtimer();
+    const Geo g = geo_of(p.H);
+    for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
+      const int rows = min(g.RS, t.a + t.b - r0);
+      if (!norm_gemv_stage(g, rows, bmask_all())) return;
+      for (int i = threadIdx.x; i < rows * NB; i += 256) {
+        const int rr = i / NB, b = i % NB;
+        if (b >= p.B) continue;
+        const int e = r0 + rr;
+        const float bias = p.router_bias ? p.router_bias[(size_t)l * p.E + e] : 0.f;
+        __stcg(&p.rlogits[((size_t)l * p.B + b) * p.E + e], m.res[i] + bias);
+      }
+    }
+    if (!arrive_last(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) return;
+    compute_routing(l);
+    if (ok) release_counter(cm.route(l));
+  }
+
+  // top-k per token (value descending, lower expert id first on ties), softmax over the k
+  // selected logits, then the distinct routed experts in ascending id with token masks.
+  __device__ void compute_routing(int l) {
+    for (int e = threadIdx.x; e < p.E; e += 256) m.emask[e] = 0u;
+    if (warp < p.B) {
+      const int b = warp;
+      float v[kMaxExperts / 32];
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < p.E ? __ldcg(&p.rlogits[((size_t)l * p.B + b) * p.E + e]) : -INFINITY;
+      }
+      float sel[kMaxK];
+      for (int j = 0; j < p.topk; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i) {
+          const int e = lane + 32 * i;
+          if (e < p.E && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i)
+          if (lane + 32 * i == be) v[i] = -INFINITY;
+        sel[j] = bv;
+        if (lane == 0) m.ids[b][j] = be;
+      }
+      if (lane == 0) {
+        float z = 0.f, w[kMaxK];
+        for (int j = 0; j < p.topk; ++j) { w[j] = expf(sel[j] - sel[0]); z += w[j]; }
+        for (int j = 0; j < p.topk; ++j) m.wk[b][j] = w[j] / z;
+      }
+    }
+    if (!csync()) return;
+    for (int i = threadIdx.x; i < p.B * p.topk; i += 256) atomicOr(&m.emask[m.ids[i / p.topk][i % p.topk]], 1u << (i / p.topk));
+    if (!csync()) return;
+    if (warp == 0) {  // compact: lane owns experts [8 lane, 8 lane + 8)
+      int cnt = 0;
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane * 8 + i;
+        cnt += (e < p.E && m.emask[e] != 0u);
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int pos = incl - cnt;
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane * 8 + i;
+        if (e < p.E && m.emask[e] != 0u) {
+          m.erank[e] = pos;
+          m.route_expert[pos] = e;
+          m.route_mask[pos] = m.emask[e];
+          ++pos;
+        }
+      }
+      if (lane == 31) m.n_active = incl;
+    }
+    for (int i = threadIdx.x; i < kMaxActive * kMaxB; i += 256) (&m.route_w[0][0])[i] = 0.f;
+    if (!csync()) return;
+    for (int i = threadIdx.x; i < p.B * p.topk; i += 256) {
+      const int b = i / p.topk, j = i % p.topk;
+      m.route_w[m.erank[m.ids[b][j]]][b] = m.wk[b][j];
+    }
+    if (!csync()) return;
+    Route* rt = p.route + l;
+    const int na = m.n_active;
+    if (threadIdx.x == 0) __stcg(&rt->n_active, na);
+    for (int i = threadIdx.x; i < na; i += 256) {
+      __stcg(&rt->expert[i], m.route_expert[i]);
+      __stcg(&rt->mask[i], m.route_mask[i]);
+    }
+    for (int i = threadIdx.x; i < na * kMaxB; i += 256) __stcg(&rt->w[i / kMaxB][i % kMaxB], m.route_w[i / kMaxB][i % kMaxB]);
+    for (int i = threadIdx.x; i < p.B * p.topk; i += 256) {
+      const int b = i / p.topk, j = i % p.topk;
+      __stcg(&rt->ids[b][j], m.ids[b][j]);
+      __stcg(&rt->wk[b][j], m.wk[b][j]);
+      __stcg(&p.topk_ids[((size_t)l * p.B + b) * p.topk + j], m.ids[b][j]);
+      __stcg(&p.topk_w[((size_t)l * p.B + b) * p.topk + j], m.wk[b][j]);
+    }
+  }
+
+  __device__ void op_qkv(const Task& t) {
+    const int l = t.layer;
+    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
+    if (!ok) return;
+    t_ready = gtimer();
+    const Geo g = geo_of(p.H);
+    const int hd = p.d / 2;
+    for (int u0 = t.a; u0 < t.a + t.b && ok; u0 += g.RG) {
+      const int nu = min(g.RG, t.a + t.b - u0);
+      if (!norm_gemv_stage(g, nu * 8, bmask_all())) return;
+      // epilogue: RoPE on q/k pairs, bf16 K/V append
+      for (int i = threadIdx.x; i < nu * 8 * NB; i += 256) {
+        const int unit = i / (8 * NB), rem = i % (8 * NB), tt = rem / NB, b = rem % NB;
+        if (b >= p.B) continue;
+        const QkvUnit q = qkv_unit(p, u0 + unit);
+        const int pos = pos_of(p, b);
+        if (pos < 0 || pos >= p.max_pos) {
+          if (tt == 0 && unit == 0) report(p, MK_ERR_BAD_PAGE, b, pos);
+          continue;
+        }
+        const float* res = m.res + unit * 8 * NB;
+        int page = -1;
+        if (q.kind != 0) {
+          const int pi = pos / kPage;
+          page = (pos >= 0 && pi < p.max_pages) ? p.block_table[b * p.max_pages + pi] : -1;
+          if (page < 0 || page >= p.num_pages) {
+            if (tt == 0) report(p, MK_ERR_BAD_PAGE, b, pi);
+            page = -1;
+          }
+        }
+        if (q.kind == 2) {  // v: 8 consecutive elements
+          const int e = 8 * q.j + tt;
+          const uint16_t vb = f2bf(res[tt * NB + b]);
+          __stcg(&p.vnew[(((size_t)l * p.B + b) * p.nkv + q.head) * p.d + e], bf2f(vb));
+          if (page >= 0)
+            p.vpool[((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d + e] = vb;
+          continue;
+        }
+        if (tt >= 4) continue;  // pair (tt, tt + 4) handled by the lower row
+        const int pi2 = 4 * q.j + tt;  // pair index in [0, d/2)
+        const float a = res[tt * NB + b], c = res[(tt + 4) * NB + b];
+        const float2 cs = p.rope[(size_t)pos * hd + pi2];
+        const float lo = a * cs.x - c * cs.y;
+        const float hi = a * cs.y + c * cs.x;
+        if (q.kind == 0) {
+          float* dst = p.q + (((size_t)l * p.B + b) * p.nq + q.head) * p.d;
+          __stcg(dst + pi2, lo);
+          __stcg(dst + pi2 + hd, hi);
+        } else {
+          const uint16_t kl = f2bf(lo), kh = f2bf(hi);
+          float* dst = p.knew + (((size_t)l * p.B + b) * p.nkv + q.head) * p.d;
+          __stcg(dst + pi2, bf2f(kl));
+          __stcg(dst + pi2 + hd, bf2f(kh));
+          if (page >= 0) {
+            uint16_t* kp = p.kpool + ((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d;
+            kp[pi2] = kl;
+            kp[pi2 + hd] = kh;
+          }
+        }
+      }
+    }
+    if (ok) release_counter(cm.qkv(l, t.c));
+  }
+
+  __device__ void op_gu(const Task& t) {
+    const int l = t.layer;
+    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
+    if (!ok) return;
+    if (!warp_wait(p, cm.route(l))) { ok = false; return; }
+    t_ready = gtimer();
+    const Route* rt = p.route + l;
+    const int na = __ldcg(&rt->n_active), maxa = max_active(p);
+    const Geo g = geo_of(p.H);
+    const int r2 = g.RS / 2;
+    for (int u = t.a; u < t.a + t.b && ok; ++u) {
+      const int a = u % maxa, tile = u / maxa;
+      if (a >= na) continue;
+      const uint32_t bm = __ldcg(&rt->mask[a]);
+      if (!norm_gemv_stage(g, g.RS, bm)) return;
+      for (int i = threadIdx.x; i < r2 * NB; i += 256) {
+        const int tt = i / NB, b = i % NB;
+        if (!(bm & (1u << b))) continue;
+        const float gt = m.res[tt * NB + b], up = m.res[(r2 + tt) * NB + b];
+        const float hv = gt / (1.0f + expf(-gt)) * up;
+        __stcg(&p.h[(((size_t)l * kMaxActive + a) * kMaxB + b) * p.I + tile * r2 + tt], hv);
+      }
+    }
+    if (ok) release_counter(cm.gu(l));
+  }
+
+  __device__ void op_o(const Task& t) {
+    const int l = t.layer;
+    const Geo g = geo_of(p.od);
+    const int rg = warp / g.KW, ks = warp % g.KW;
+    const int gw = p.group * p.d;  // columns per KV group
+    float acc[8][NB];
+    zero_acc(acc);
+    t_ready = 0;
+    for (int cs = 0; cs < g.NCS; ++cs) {
+      const int c0 = cs * g.KS + ks * 256;
+      float act[NB][8];
+      if (rg < g.RG) {
+        for (int gg = c0 / gw; gg <= (c0 + 255) / gw; ++gg)
+          if (!warp_wait(p, cm.attn(l, gg))) { ok = false; return; }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (b < p.B) load8(p.attn_o + ((size_t)l * p.B + b) * p.od + c0 + lane * 8, act[b]);
+          else
+#pragma unroll
+            for (int i = 0; i < 8; ++i) act[b][i] = 0.f;
+        }
+      }
+      if (!t_ready) t_ready = gtimer();
+      const uint8_t* st = acquire();
+      if (!st) return;
+      if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, t.b - rg * 8), act, acc, bmask_all());
+      release();
+    }
+    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[warp], lane);
+    if (!csync()) return;
+    cross_warp_reduce<NB>(m, g, t.b);
+    if (!csync()) return;
+    for (int i = threadIdx.x; i < t.b * NB; i += 256) {
+      const int rr = i / NB, b = i % NB;
+      if (b < p.B) __stcg(&p.attn_out[((size_t)l * p.B + b) * p.H + t.a + rr], m.res[i]);
+    }
+    release_counter(cm.layer(l));
+  }
+
+  __device__ void op_down(const Task& t) {
+    const int l = t.layer;
+    if (!warp_wait(p, cm.gu(l))) { ok = false; return; }
+    t_ready = gtimer();
+    const Geo g = geo_of(p.I);
+    const int rg = warp / g.KW, ks = warp % g.KW;
+    const Route* rt = p.route + l;
+    const int na = __ldcg(&rt->n_active);
+    float acc[8][NB];
+    zero_acc(acc);
+    for (int a = 0; a < na; ++a) {
+      const uint32_t bm = __ldcg(&rt->mask[a]);
+      float act[NB][8];
+      if (rg < g.RG) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (bm & (1u << b)) {
+            load8(p.h + (((size_t)l * kMaxActive + a) * kMaxB + b) * p.I + ks * 256 + lane * 8, act[b]);
+            const float wgt = __ldcg(&rt->w[a][b]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) act[b][i] *= wgt;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) act[b][i] = 0.f;
+          }
+        }
+      }
+      const uint8_t* st = acquire();
+      if (!st) return;
+      if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, t.b - rg * 8), act, acc, bm);
+      release();
+    }
+    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[warp], lane);
+    if (!csync()) return;
+    cross_warp_reduce<NB>(m, g, t.b);
+    if (!csync()) return;
+    for (int i = threadIdx.x; i < t.b * NB; i += 256) {
+      const int rr = i / NB, b = i % NB;
+      if (b < p.B) __stcg(&p.moe_out[((size_t)l * p.B + b) * p.H + t.a + rr], m.res[i]);
+    }
+    release_counter(cm.layer(l));
+  }
+
+  __device__ void op_lm(const Task& t) {
+    ensure_norm(p.L, (t.flags & TF_WRITE_X) != 0);
+    if (!ok) return;
+    t_ready = gtimer();
+    const Geo g = geo_of(p.H);
+    for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
+      const int rows = min(g.RS, t.a + t.b - r0);
+      if (!norm_gemv_stage(g, rows, bmask_all())) return;
+      if (p.logits)
+        for (int i = threadIdx.x; i < rows * NB; i += 256) {
+          const int rr = i / NB, b = i % NB;
+          if (b < p.B) __stcg(&p.logits[(size_t)b * p.V + r0 + rr], m.res[i]);
+        }
+      if (threadIdx.x < NB) {  // rows ascending: strict > keeps the lowest id on ties
+        const int b = threadIdx.x;
+        float bv = lm_best[b];
+        int bi = lm_idx[b];
+        for (int rr = 0; rr < rows; ++rr) {
+          const float v = m.res[rr * NB + b];
+          if (v > bv || (v == bv && r0 + rr < bi)) { bv = v; bi = r0 + rr; }
+        }
+        lm_best[b] = bv;
+        lm_idx[b] = bi;
+      }
+    }
+    if (!(t.flags & TF_LAST_LM) || !ok) return;
+    if (threadIdx.x < NB && threadIdx.x < p.B) {
+      __stcg(&p.lm_best_v[t.c * kMaxB + threadIdx.x], lm_best[threadIdx.x]);
+      __stcg(&p.lm_best_i[t.c * kMaxB + threadIdx.x], lm_idx[threadIdx.x]);
+    }
+    if (!arrive_last(cm.lm_arrive(), p.n_lm_sm)) return;
+    if (threadIdx.x < p.B) {
+      const int b = threadIdx.x;
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int s = 0; s < p.n_lm_sm; ++s) {
+        const float v = __ldcg(&p.lm_best_v[s * kMaxB + b]);
+        const int i = __ldcg(&p.lm_best_i[s * kMaxB + b]);
+        if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+      }
+      if (p.argmax_out) p.argmax_out[b] = bi;
+    }
+  }
+
+  // Paged GQA attention of one (sequence b, KV group g, chunk). The G <= 8 query heads of the
+  // group are the 16 rows of an mma A operand: rows 0..7 hold the bf16 "hi" part of q and rows
+  // 8..15 its rounding residual, so S = q K^T comes out at ~fp32 accuracy; P is split the same
+  // way for P V. K/V tiles arrive 128B-swizzled from the tensor maps (conflict-free ldmatrix).
+  __device__ void op_attn(const Task& t) {
+    const int l = t.layer, b = t.a, g = t.b;
+    if (!warp_wait(p, cm.qkv(l, g))) { ok = false; return; }
+    t_ready = gtimer();
+    const AttnRange ar = attn_range(p, b, t.c);
+    const int pps = attn_pps(p), halves = p.d / 64, ksteps = p.d / 16;
+    const int pi = warp % pps, dp = warp / pps;
+    const int head = lane >> 2, tig = lane & 3;
+    const float qscale = rsqrtf((float)p.d) * 1.4426950408889634f;  // scores in log2 units
+    uint32_t qa[8][4];
+    {
+      const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + head) * p.d;
+      const bool hv = head < p.group;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        if (kk < ksteps) {
+          const int d0 = kk * 16 + tig * 2;
+          const float x0 = hv ? __ldcg(qh + d0) * qscale : 0.f, x1 = hv ? __ldcg(qh + d0 + 1) * qscale : 0.f;
+          const float x2 = hv ? __ldcg(qh + d0 + 8) * qscale : 0.f, x3 = hv ? __ldcg(qh + d0 + 9) * qscale : 0.f;
+          split_pack(x0, x1, qa[kk][0], qa[kk][1]);
+          split_pack(x2, x3, qa[kk][2], qa[kk][3]);
+        }
+      }
+    }
+    float mrun = -INFINITY, lsum = 0.f;
+    float oacc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) oacc[i][j] = 0.f;
+
+    const int nst = (ar.cp1 - ar.cp0 + pps - 1) / pps;
+    uint32_t last_slot = 0;
+    for (int s = 0; s < nst; ++s) {
+      const uint8_t* st = acquire();
+      if (!st) return;
+      const int page = ar.cp0 + s * pps + pi;
+      if (page < ar.cp1) {
+        const uint32_t kt = smem_addr(st) + (uint32_t)pi * 4096 * halves;
+        const uint32_t vt = kt + (uint32_t)halves * 2048;
+        float sc[2][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sc[i][j] = 0.f;
+        const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          if (kk < ksteps) {
+            const int prow = (mi >> 1) * 8 + rr;           // position within the page
+            const int chunk = 2 * kk + (mi & 1);          // 16-byte chunk of the head dim
+            const uint32_t addr = kt + (chunk >> 3) * 2048 + prow * 128 + (((chunk & 7) ^ (prow & 7)) << 4);
+            uint32_t bk[4];
+            ldsm_x4(addr, bk);
+            mma_bf16(sc[0], qa[kk], bk[0], bk[1]);
+            mma_bf16(sc[1], qa[kk], bk[2], bk[3]);
+          }
+        }
+        float sv[2][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int pos = page * kPage + nt * 8 + tig * 2 + e;
+            const float s_ = sc[nt][e] + sc[nt][e + 2];
+            sv[nt][e] = pos < ar.pos_end ? s_ : -INFINITY;
+            mx = fmaxf(mx, sv[nt][e]);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mnew = fmaxf(mrun, mx);
+        if (mnew != -INFINITY) {
+          const float alpha = exp2f(mrun - mnew);
+          lsum *= alpha;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) oacc[i][j] *= alpha;
+          mrun = mnew;
+          float pr[2][2];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              pr[nt][e] = exp2f(sv[nt][e] - mnew);
+              lsum += pr[nt][e];
+            }
+          uint32_t pa[4];
+          split_pack(pr[0][0], pr[0][1], pa[0], pa[1]);
+          split_pack(pr[1][0], pr[1][1], pa[2], pa[3]);
+#pragma unroll
+          for (int c2 = 0; c2 < 4; ++c2) {  // two 8-wide d tiles per ldmatrix.x4.trans
+            const int chunk = dp * 8 + c2 * 2 + (mi >> 1);
+            const int prow = (mi & 1) * 8 + rr;
+            const uint32_t addr = vt + (chunk >> 3) * 2048 + prow * 128 + (((chunk & 7) ^ (prow & 7)) << 4);
+            uint32_t bv[4];
+            ldsm_x4_t(addr, bv);
+            mma_bf16(oacc[c2 * 2], pa, bv[0], bv[1]);
+            mma_bf16(oacc[c2 * 2 + 1], pa, bv[2], bv[3]);
+          }
+        }
+      }
+      if (s + 1 < nst) release();
+      else last_slot = smem_addr(st);
+    }
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+
+    // merge the warps that share a d range (different pages), using the last slot as scratch
+    const size_t pidx = (((size_t)l * p.B + b) * p.nkv + g) * p.max_chunks + t.c;
+    float* part = p.apart + pidx * (16 + 8 * (size_t)p.d);
+    if (nst > 0) {
+      if (!csync()) return;
+      float* scr = reinterpret_cast<float*>(__cvta_shared_to_generic(last_slot));
+      // per warp: m[8], l[8], O[8][64]
+      float* mine = scr + warp * (16 + 8 * 64);
+      if (tig == 0) { mine[head] = mrun; mine[8 + head] = lsum; }
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) mine[16 + head * 64 + nt * 8 + tig * 2 + e] = oacc[nt][e] + oacc[nt][e + 2];
+      if (!csync()) return;
+      for (int i = threadIdx.x; i < 8 * p.d; i += 256) {
+        const int h = i / p.d, dd = i % p.d, dpi = dd / 64, dl = dd % 64;
+        float M = -INFINITY;
+        for (int w = dpi * pps; w < (dpi + 1) * pps; ++w) M = fmaxf(M, scr[w * (16 + 512) + h]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY)
+          for (int w = dpi * pps; w < (dpi + 1) * pps; ++w) {
+            const float* src = scr + w * (16 + 512);
+            if (src[h] == -INFINITY) continue;
+            const float f = exp2f(src[h] - M);
+            L += src[8 + h] * f;
+            O += src[16 + h * 64 + dl] * f;
+          }
+        if (dd == 0) { __stcg(part + h, M); __stcg(part + 8 + h, L); }
+        __stcg(part + 16 + i, O);
+      }
+      if (!csync()) return;
+      release();
+    } else {
+      for (int i = threadIdx.x; i < 16 + 8 * p.d; i += 256) __stcg(part + i, i < 8 ? -INFINITY : 0.f);
+    }
+    const int arr = cm.attn_arrive(l, b, g);
+    if (!arrive_last(arr, p.n_chunks[b])) return;
+
+    // combine the chunks of (b, g) with the new token (position pos, read from knew / vnew)
+    const int nch = p.n_chunks[b];
+    const float* pbase = p.apart + (((size_t)l * p.B + b) * p.nkv + g) * p.max_chunks * (16 + 8 * (size_t)p.d);
+    // s_new per head: warp h < group
+    if (warp < p.group) {
+      const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + warp) * p.d;
+      const float* kn = p.knew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
+      float s = 0.f;
+      for (int i = lane; i < p.d; i += 32) s = fmaf(__ldcg(qh + i), __ldcg(kn + i), s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) m.res[warp] = s * qscale;
+    }
+    if (!csync()) return;
+    const float* vn = p.vnew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
+    for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
+      const int h = i / p.d, dd = i % p.d;
+      const float sn = m.res[h];
+      float M = sn;
+      for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(pbase + (size_t)c * (16 + 8 * p.d) + h));
+      float fn = exp2f(sn - M);
+      float L = fn, O = fn * __ldcg(vn + dd);
+      for (int c = 0; c < nch; ++c) {
+        const float* src = pbase + (size_t)c * (16 + 8 * p.d);
+        const float mc = __ldcg(src + h);
+        if (mc == -INFINITY) continue;
+        const float f = exp2f(mc - M);
+        L += __ldcg(src + 8 + h) * f;
+        O += __ldcg(src + 16 + h * p.d + dd) * f;
+      }
+      __stcg(&p.attn_o[((size_t)l * p.B + b) * p.od + (g * p.group + h) * p.d + dd], O / L);
+    }
+    release_counter(cm.attn(l, g));
+  }
+
+  __device__ void run_task(const Task& t) {
+    t_start = gtimer();
+    t_ready = t_start;
+    switch (t.op) {
+      case OP_ROUTER: op_router(t); break;
+      case OP_QKV: op_qkv(t); break;
+      case OP_ATTN: op_attn(t); break;
+      case OP_GU: op_gu(t); break;
+      case OP_O: op_o(t); break;
+      case OP_DOWN: op_down(t); break;
+      case OP_LM: op_lm(t); break;
+    }
+    if (ok) trace_task(p, t, t_start, t_ready ? t_ready : t_start);
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_constant__ Params p,
+                                                                const __grid_constant__ TensorMaps tm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Misc& misc = *reinterpret_cast<Misc*>(base + kStages * kStageBytes);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&misc.full[s]), 1);
+      mbar_init(smem_addr(&misc.empty[s]), kConsumerWarps);
+    }
+    mbar_init(smem_addr(&misc.cbar), kConsumerWarps);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  Ring ring;
+  ring.data = smem_addr(base);
+  ring.full = smem_addr(&misc.full[0]);
+  ring.empty = smem_addr(&misc.empty[0]);
+  ring.it = 0;
+  const int t0 = p.sm_begin[blockIdx.x], t1 = p.sm_begin[blockIdx.x + 1];
+
+  if (threadIdx.x / 32 == kConsumerWarps) {
+    if ((threadIdx.x & 31) != 0) return;
+    Producer pr(p, tm, ring);
+    for (int i = t0; i < t1; ++i) {
+      const Task t = p.tasks[i];
+      if (!pr.run_task(t)) break;
+    }
+    pr.drain();  // never leave while a copy into this CTA's shared memory is in flight
+    return;
+  }
+  Consumer<NB> c(p, misc, ring);
+  for (int i = t0; i < t1 && c.ok; ++i) {
+    const Task t = p.tasks[i];
+    c.run_task(t);
+  }
+}
+
+}  // namespace mk
+
+// ------------------------------------------------------------------ launch entry (host)
+
+namespace mk {
+int kernel_smem_bytes() { return kSmemBytes; }
+
+cudaError_t configure_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(mk_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mk_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mk_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(mk_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return e;
+}
+
+template <int NB>
+static cudaError_t launch_nb(const Params& p, const TensorMaps& tm, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_sm);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mk_decode_kernel<NB>, p, tm);
+}
+
+cudaError_t launch_decode(const Params& p, const TensorMaps& tm, cudaStream_t st) {
+  if (p.B <= 1) return launch_nb<1>(p, tm, st);
+  if (p.B <= 2) return launch_nb<2>(p, tm, st);
+  if (p.B <= 4) return launch_nb<4>(p, tm, st);
+  return launch_nb<8>(p, tm, st);
+}
+
+cudaError_t max_blocks_per_sm(int B, int* n) {
+  if (B <= 1) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, mk_decode_kernel<1>, kThreads, kSmemBytes);
+  if (B <= 2) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, mk_decode_kernel<2>, kThreads, kSmemBytes);
+  if (B <= 4) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, mk_decode_kernel<4>, kThreads, kSmemBytes);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, mk_decode_kernel<8>, kThreads, kSmemBytes);
+}
+}  // namespace mk

@@ -1,9 +1,10 @@
 """Compiles the oracle (C, OpenMP) into oracle/_lib/liboracle.so. Test infrastructure."""
 import os
+import platform
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB = os.path.join(HERE, "_lib", "liboracle.so")
+LIB = os.path.join(HERE, "_lib", platform.machine(), "liboracle.so")
 SOURCES = [os.path.join(HERE, "oracle.c"), os.path.join(HERE, "source.c"),
            os.path.join(HERE, "..", "synth", "synth_host.c")]
 

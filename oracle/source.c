@@ -113,6 +113,7 @@ typedef struct {
   uint16_t* overlay;  /* [2][L][B][nkv][max_new][d] */
   uint16_t *embed_row, *gain, *final_gain, *qkv, *o, *router, *lm;
   int qkv_l, o_l, router_l, gain_l;
+  uint16_t **qkv_all, **o_all, **router_all; /* keep_all: every layer's dense weights */
   cache_ent* experts; /* (kind, layer, expert) cache */
   int n_exp, cap_exp;
   int keep_all;       /* 0: drop cached experts of other layers */
@@ -121,6 +122,14 @@ typedef struct {
 static void gen(synth_src* s, int skind, int layer, int sub, size_t count, float sigma, float offset,
                 uint16_t* dst) {
   synth_fill_bf16(s->seed, synth_tid(skind, layer, sub), 0, count, sigma, offset, dst);
+}
+
+static const uint16_t* cached_dense(synth_src* s, uint16_t** tab, int skind, int l, size_t n) {
+  if (!tab[l]) {
+    tab[l] = (uint16_t*)malloc(sizeof(uint16_t) * n);
+    gen(s, skind, l, 0, n, 0.02f, 0.0f, tab[l]);
+  }
+  return tab[l];
 }
 
 static const uint16_t* synth_weight(void* ctx, int kind, int l, int idx) {
@@ -138,12 +147,15 @@ static const uint16_t* synth_weight(void* ctx, int kind, int l, int idx) {
       return s->gain;
     case ORC_FINAL_GAIN: return s->final_gain;
     case ORC_QKV:
+      if (s->keep_all) return cached_dense(s, s->qkv_all, SYNTH_QKV, l, qkv_rows * H);
       if (s->qkv_l != l) { gen(s, SYNTH_QKV, l, 0, qkv_rows * H, 0.02f, 0.0f, s->qkv); s->qkv_l = l; }
       return s->qkv;
     case ORC_O:
+      if (s->keep_all) return cached_dense(s, s->o_all, SYNTH_O, l, H * od);
       if (s->o_l != l) { gen(s, SYNTH_O, l, 0, H * od, 0.02f, 0.0f, s->o); s->o_l = l; }
       return s->o;
     case ORC_ROUTER:
+      if (s->keep_all) return cached_dense(s, s->router_all, SYNTH_ROUTER, l, (size_t)c->E * H);
       if (s->router_l != l) { gen(s, SYNTH_ROUTER, l, 0, (size_t)c->E * H, 0.02f, 0.0f, s->router); s->router_l = l; }
       return s->router;
     case ORC_LM:
@@ -214,7 +226,8 @@ static int synth_kv_write(void* ctx, int kind, int l, int b, int pos, int g, con
 
 /* Creates a synth source for B sequences prefilled to ctx_len[b] positions with room
  * for max_new appended tokens each. bias ([L][E] fp32) is copied; NULL = zero bias.
- * keep_all_experts != 0 keeps every generated expert (for repeat timing). */
+ * keep_all != 0 keeps every generated weight (dense per-layer weights and experts) so that
+ * a repeated step times the oracle's arithmetic rather than the generator. */
 void* orc_synth_source_create(const orc_cfg* c, uint64_t seed, int32_t B, const int32_t* ctx_len,
                               int32_t max_new, const float* bias, int32_t keep_all_experts, orc_source* out) {
   synth_src* s = (synth_src*)calloc(1, sizeof(synth_src));
@@ -239,6 +252,9 @@ void* orc_synth_source_create(const orc_cfg* c, uint64_t seed, int32_t B, const 
   s->o = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)c->nq * c->d * H);
   s->router = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)c->E * H);
   s->qkv_l = s->o_l = s->router_l = s->gain_l = -1;
+  s->qkv_all = (uint16_t**)calloc((size_t)c->L, sizeof(uint16_t*));
+  s->o_all = (uint16_t**)calloc((size_t)c->L, sizeof(uint16_t*));
+  s->router_all = (uint16_t**)calloc((size_t)c->L, sizeof(uint16_t*));
   out->ctx = s;
   out->weight = synth_weight;
   out->router_bias = synth_bias;
@@ -250,6 +266,8 @@ void orc_synth_source_destroy(void* p) {
   synth_src* s = (synth_src*)p;
   if (!s) return;
   for (int i = 0; i < s->n_exp; ++i) free(s->experts[i].data);
+  for (int l = 0; l < s->c.L; ++l) { free(s->qkv_all[l]); free(s->o_all[l]); free(s->router_all[l]); }
+  free(s->qkv_all); free(s->o_all); free(s->router_all);
   free(s->experts); free(s->ctx_len); free(s->bias); free(s->overlay); free(s->embed_row); free(s->gain);
   free(s->final_gain); free(s->qkv); free(s->o); free(s->router); free(s->lm);
   free(s);

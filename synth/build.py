@@ -1,10 +1,11 @@
 """Compiles the seeded input generator: host part (gcc) and device part (nvcc, sm_103a)."""
 import os
+import platform
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-HOST_LIB = os.path.join(HERE, "_lib", "libsynth_host.so")
-DEV_LIB = os.path.join(HERE, "_lib", "libsynth_dev.so")
+HOST_LIB = os.path.join(HERE, "_lib", platform.machine(), "libsynth_host.so")
+DEV_LIB = os.path.join(HERE, "_lib", platform.machine(), "libsynth_dev.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,80 @@
+"""Shared set-up for GPU parity tests: the same seeded workload on the GPU (device-generated)
+and in the oracle (host-generated on demand), plus the acceptance checks."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+from synth import workloads as W
+
+
+class Setup:
+    def __init__(self, w, new_tokens: int, mode: int = 0):
+        import torch
+
+        from moe_transformer_decode_gb300.context import DecodeContext
+
+        self.w = w
+        self.ctx = W.context_lengths(w)
+        self.bt, self.num_pages = W.page_tables(w, self.ctx, new_tokens)
+        self.bias = W.router_bias(w)
+        self.model = synth.device_model(w)
+        if self.bias is not None:
+            self.model["router_bias"] = torch.as_tensor(self.bias, device="cuda")
+        self.K, self.V = synth.device_kv(w, self.ctx, self.bt, self.num_pages)
+        self.dc = DecodeContext(w, self.model, max_batch=w.B, max_pages_per_seq=self.bt.shape[1])
+        self.bt_d = torch.as_tensor(self.bt, device="cuda")
+        self.dc.schedule(self.ctx, self.bt_d)
+        if mode:
+            self.dc.set_mode(mode)
+        self.oracle_src = oracle.SynthSource(w, self.ctx, new_tokens, self.bias)
+        self.logits = torch.empty((w.B, w.V), dtype=torch.float32, device="cuda")
+        self.next = torch.empty(w.B, dtype=torch.int32, device="cuda")
+
+    def gpu_step(self, tokens, positions):
+        import torch
+
+        tok = torch.as_tensor(np.asarray(tokens, np.int32), device="cuda")
+        pos = torch.as_tensor(np.asarray(positions, np.int32), device="cuda")
+        self.dc.step(tok, pos, self.K, self.V, self.logits, self.next)
+        self.dc.sync()
+        return self.logits.cpu().numpy(), self.next.cpu().numpy()
+
+    def oracle_step(self, tokens, positions, trace=True):
+        return oracle.decode_step(self.w, self.oracle_src, tokens, positions, trace=trace)
+
+    def close(self):
+        self.dc.close()
+
+
+def router_ties_ok(ref_logits_row, got_ids, ref_ids, tol=1e-3):
+    """Top-k ids must match except where the oracle's router logits tie within tol: every id
+    in the symmetric difference must lie within tol of the oracle's k-th largest logit."""
+    if list(got_ids) == list(ref_ids):
+        return True
+    if set(got_ids) == set(ref_ids):
+        order_ok = all(abs(ref_logits_row[a] - ref_logits_row[b]) <= tol for a, b in zip(got_ids, ref_ids) if a != b)
+        return order_ok
+    kth = np.sort(ref_logits_row)[::-1][len(ref_ids) - 1]
+    diff = set(got_ids) ^ set(ref_ids)
+    return all(abs(ref_logits_row[e] - kth) <= tol for e in diff)
+
+
+def check_step(w, got_logits, got_next, ref_logits, ref_next, acts=None, tr=None, rtol_logits=3e-2):
+    """Acceptance per step: max|dlogit| <= 3e-2 * std(oracle logits) per row; top-k ids equal
+    except oracle-side ties within 1e-3. Returns (argmax agreement count, report dict)."""
+    rep = {}
+    for b in range(w.B):
+        err = float(np.abs(got_logits[b] - ref_logits[b]).max())
+        tol = rtol_logits * float(ref_logits[b].std())
+        rep[f"row{b}_err"] = err
+        assert err <= tol, f"row {b}: max |dlogit| {err:.3e} > {tol:.3e}"
+    if acts is not None and tr is not None:
+        ids = acts["topk_ids"].cpu().numpy()
+        for l in range(w.L):
+            for b in range(w.B):
+                assert router_ties_ok(tr["router"][l, b], ids[l, b], tr["topk_ids"][l, b]), \
+                    f"layer {l} token {b}: top-k {ids[l, b]} vs oracle {tr['topk_ids'][l, b]}"
+    agree = int(np.sum(got_next == ref_next))
+    return agree, rep
