@@ -162,6 +162,20 @@ typedef struct {
 } mk_activations;
 mk_status mk_get_activations(const mk_ctx* ctx, mk_activations* out);
 
+/* Host-only view of the scheduler (no device needed): plans the step for `batch`
+ * sequences of lengths seq_lens (host) on n_sm SMs, as mk_build_schedule would. Writes
+ * the plan's sizes to *info; if `tasks` is non-NULL, copies the megakernel's task list
+ * (info->n_tasks 16-byte descriptors {uint8 op, uint8 flags, uint16 layer, int32 a, b, c},
+ * grouped by SM) when tasks_cap >= info->n_tasks, else returns MK_ERR_INVALID_ARG; if
+ * sm_begin is non-NULL, writes the n_sm + 1 list offsets; if sm_bytes is non-NULL, the
+ * planned bytes per SM. Opcodes: 1 router, 2 QKV, 3 attention, 4 expert gate/up, 5 O-proj,
+ * 6 expert down, 7 LM head. Errors: MK_ERR_INVALID_ARG. */
+typedef struct {
+  int32_t n_tasks, n_counters, max_chunks, n_lm_sm, n_op_launches;
+} mk_plan_info;
+mk_status mk_plan_schedule(const mk_model_cfg* cfg, int32_t n_sm, int32_t batch, const int32_t* seq_lens,
+                           mk_plan_info* info, void* tasks, int32_t tasks_cap, int32_t* sm_begin, int64_t* sm_bytes);
+
 /* Number of SMs the persistent kernel runs on and tasks per step of the current schedule. */
 mk_status mk_get_launch_info(const mk_ctx* ctx, int32_t* n_sm, int32_t* tasks_per_step, int32_t* launches_per_step);
 

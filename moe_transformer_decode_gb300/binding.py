@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_UNSUPPORTED", 3:
                 5: "MK_ERR_NO_SCHEDULE", 6: "MK_ERR_BAD_PAGE", 7: "MK_ERR_DEVICE_TIMEOUT", 8: "MK_ERR_BAD_TOKEN"}
 MK_MODE_MEGAKERNEL, MK_MODE_PER_OP = 0, 1
 
-EXPORTS = ["mk_create", "mk_build_schedule", "mk_decode_step", "mk_decode_greedy", "mk_status_sync", "mk_last_error",
+EXPORTS = ["mk_create", "mk_plan_schedule", "mk_build_schedule", "mk_decode_step", "mk_decode_greedy", "mk_status_sync", "mk_last_error",
            "mk_set_mode", "mk_enable_trace", "mk_get_activations", "mk_get_launch_info", "mk_destroy"]
 
 
@@ -42,6 +42,10 @@ class mk_kv_pages(ctypes.Structure):
 class mk_activations(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("x", "q", "attn", "attn_out", "moe_out", "router", "topk_ids",
                                                 "topk_w")]
+
+
+class mk_plan_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n_tasks", "n_counters", "max_chunks", "n_lm_sm", "n_op_launches")]
 
 
 class mk_trace_entry(ctypes.Structure):
@@ -69,6 +73,9 @@ def lib():
         vp, i32 = ctypes.c_void_p, ctypes.c_int32
         L.mk_create.restype = ctypes.c_int
         L.mk_create.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.POINTER(mk_weight_ptrs), ctypes.POINTER(vp)]
+        L.mk_plan_schedule.restype = ctypes.c_int
+        L.mk_plan_schedule.argtypes = [ctypes.POINTER(mk_model_cfg), i32, i32, vp, ctypes.POINTER(mk_plan_info), vp,
+                                       i32, vp, vp]
         L.mk_build_schedule.restype = ctypes.c_int
         L.mk_build_schedule.argtypes = [vp, i32, vp, vp]
         L.mk_decode_step.restype = ctypes.c_int
@@ -107,6 +114,25 @@ def mk_create(cfg: mk_model_cfg, weights: mk_weight_ptrs):
     out = ctypes.c_void_p()
     _check(None, lib().mk_create(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(out)))
     return out
+
+
+TASK_DTYPE = [("op", "u1"), ("flags", "u1"), ("layer", "<u2"), ("a", "<i4"), ("b", "<i4"), ("c", "<i4")]
+
+
+def mk_plan_schedule(cfg: mk_model_cfg, n_sm: int, seq_lens):
+    """Host-only plan: returns (info, tasks as a structured numpy array grouped by SM, sm_begin, sm_bytes)."""
+    import numpy as np
+
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    info = mk_plan_info()
+    _check(None, lib().mk_plan_schedule(ctypes.byref(cfg), n_sm, len(sl), sl.ctypes.data, ctypes.byref(info), None, 0,
+                                        None, None))
+    tasks = np.zeros(info.n_tasks, dtype=np.dtype(TASK_DTYPE))
+    begin = np.zeros(n_sm + 1, dtype=np.int32)
+    load = np.zeros(n_sm, dtype=np.int64)
+    _check(None, lib().mk_plan_schedule(ctypes.byref(cfg), n_sm, len(sl), sl.ctypes.data, ctypes.byref(info),
+                                        tasks.ctypes.data, info.n_tasks, begin.ctypes.data, load.ctypes.data))
+    return info, tasks, begin, load
 
 
 def mk_build_schedule(ctx, batch: int, seq_lens, block_tables) -> None:

@@ -287,24 +287,26 @@ Task mkt(int op, int layer, int a, int b, int c, int flags = 0) {
 
 }  // namespace
 
-extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* seq_lens, const int32_t* block_tables) {
-  if (!c) return MK_ERR_INVALID_ARG;
-  const mk_model_cfg& m = c->cfg;
-  if (batch < 1 || batch > m.max_batch || !seq_lens || !block_tables)
-    return fail(c, MK_ERR_INVALID_ARG, "batch outside 1..max_batch or null array");
-  for (int b = 0; b < batch; ++b)
-    if (seq_lens[b] < 0 || seq_lens[b] >= m.max_pages_per_seq * kPage)
-      return fail(c, MK_ERR_INVALID_ARG, "sequence length negative or beyond the block table");
-  cudaDeviceSynchronize();
-  free_schedule(c);
+struct Plan {
+  std::vector<Task> all;          // megakernel lists (per SM), then the per-op launches' lists
+  std::vector<int32_t> begin;     // [n_sm + 1] offsets, then [n_sm + 1] per per-op launch
+  std::vector<int32_t> cnt;       // counter increments per step
+  std::vector<int32_t> chunk_pages, n_chunks;
+  std::vector<long long> load;    // planned bytes per SM (megakernel lists)
+  int max_chunks = 1, n_lm_sm = 0, n_tasks = 0, n_op_launches = 0;
+};
+
+static mk_status plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_t* seq_lens, Plan& P) {
+  if (n_sm < 1 || B < 1 || B > m.max_batch || !seq_lens) return MK_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens[b] < 0 || seq_lens[b] >= m.max_pages_per_seq * kPage) return MK_ERR_INVALID_ARG;
   const int L = m.n_layers, H = m.hidden, d = m.head_dim, nkv = m.n_kv_heads, G = m.n_q_heads / nkv;
   const int E = m.n_experts, I = m.expert_inter, V = m.vocab, od = m.n_q_heads * d;
-  const int B = batch;
-  const int n_sm = c->n_sm;
   const Geo gh = geo_of(H), go = geo_of(od), gi = geo_of(I);
   const int pps = kStageBytes / (4096 * (d / 64));
   CounterMap cmap{L, nkv, B};
-  std::vector<int32_t> cnt(cmap.count(), 0);
+  std::vector<int32_t>& cnt = P.cnt;
+  cnt.assign(cmap.count(), 0);
 
   // attention chunks: about one (sequence, group, chunk) task per SM, whole stages each
   long long group_pages = 0;
@@ -316,11 +318,12 @@ extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* 
   int cp = (int)((group_pages + n_sm - 1) / n_sm);
   cp = std::max(cp, pps);
   cp = (cp + pps - 1) / pps * pps;
-  std::vector<int32_t> chunk_pages(B, cp), n_chunks(B);
-  int max_chunks = 1;
+  P.chunk_pages.assign(B, cp);
+  P.n_chunks.assign(B, 1);
+  P.max_chunks = 1;
   for (int b = 0; b < B; ++b) {
-    n_chunks[b] = std::max(1, (npg[b] + cp - 1) / cp);
-    max_chunks = std::max(max_chunks, n_chunks[b]);
+    P.n_chunks[b] = std::max(1, (npg[b] + cp - 1) / cp);
+    P.max_chunks = std::max(P.max_chunks, P.n_chunks[b]);
   }
 
   const int maxa = std::min(B * m.top_k, E);
@@ -330,22 +333,18 @@ extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* 
   // expected live fraction of the planned expert slots (1 at batch 1)
   const double live = maxa == m.top_k ? 1.0 : std::min(1.0, (double)E * (1.0 - std::pow(1.0 - (double)m.top_k / E, B)) / maxa);
 
-  struct Cat {
-    int op;
-    std::vector<std::pair<Task, long long>> t;
-  };
   Assigner as(n_sm);
   std::vector<std::vector<std::vector<Task>>> per_op;  // [launch][sm] tasks for the per-op mode
-
   auto emit = [&](std::vector<std::pair<Task, long long>>& ts) {
     for (auto& x : ts) as.put(x.first, x.second);
     std::vector<std::vector<Task>> lists(n_sm);
     for (size_t i = 0; i < ts.size(); ++i) lists[i % n_sm].push_back(ts[i].first);
     if (!ts.empty()) per_op.push_back(std::move(lists));
+    ts.clear();
   };
 
+  std::vector<std::pair<Task, long long>> ts;
   for (int l = 0; l < L; ++l) {
-    std::vector<std::pair<Task, long long>> ts;
     // router: one stage per task; the first task stores x of this layer
     int n_router = 0;
     for (int r0 = 0; r0 < E; r0 += gh.RS, ++n_router)
@@ -354,28 +353,25 @@ extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* 
     cnt[cmap.router_arrive(l)] = n_router;
     cnt[cmap.route(l)] = 1;
     emit(ts);
-    ts.clear();
     // QKV units, group-major, one stage per task
     const int upg = (G + 2) * (d / 8);
     for (int g = 0; g < nkv; ++g) {
       int n = 0;
       for (int u = g * upg; u < (g + 1) * upg; u += gh.RG, ++n)
-        ts.push_back({mkt(OP_QKV, l, u, std::min(gh.RG, (g + 1) * upg - u), g), std::min(gh.RG, (g + 1) * upg - u) * 8 * row_h});
+        ts.push_back({mkt(OP_QKV, l, u, std::min(gh.RG, (g + 1) * upg - u), g),
+                      std::min(gh.RG, (g + 1) * upg - u) * 8 * row_h});
       cnt[cmap.qkv(l, g)] = n;
     }
     emit(ts);
-    ts.clear();
     // attention chunks
     for (int b = 0; b < B; ++b)
-      for (int g = 0; g < nkv; ++g) {
-        for (int ch = 0; ch < n_chunks[b]; ++ch) {
-          const int p0 = ch * cp, p1 = (ch == n_chunks[b] - 1) ? npg[b] : std::min(npg[b], p0 + cp);
+      for (int g = 0; g < nkv; ++g)
+        for (int ch = 0; ch < P.n_chunks[b]; ++ch) {
+          const int p0 = ch * cp, p1 = (ch == P.n_chunks[b] - 1) ? npg[b] : std::min(npg[b], p0 + cp);
           ts.push_back({mkt(OP_ATTN, l, b, g, ch), std::max(0, p1 - p0) * 2LL * kPage * d * 2});
         }
-        cnt[cmap.attn(l, g)] = B;
-      }
+    for (int g = 0; g < nkv; ++g) cnt[cmap.attn(l, g)] = B;
     emit(ts);
-    ts.clear();
     // expert gate/up: units u = tile * maxa + active_rank
     int n_gu = 0;
     for (int u = 0; u < maxa * tiles; u += gu_per_task, ++n_gu) {
@@ -384,76 +380,121 @@ extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* 
     }
     cnt[cmap.gu(l)] = n_gu;
     emit(ts);
-    ts.clear();
     // O-proj rows
     int n_o = 0;
     for (int r0 = 0; r0 < H; r0 += go.RS, ++n_o)
       ts.push_back({mkt(OP_O, l, r0, std::min(go.RS, H - r0), 0), std::min(go.RS, H - r0) * 2LL * od});
     emit(ts);
-    ts.clear();
     // expert down rows over all active experts
     int n_down = 0;
     for (int r0 = 0; r0 < H; r0 += gi.RS, ++n_down)
       ts.push_back({mkt(OP_DOWN, l, r0, std::min(gi.RS, H - r0), 0),
                     (long long)(std::min(gi.RS, H - r0) * 2.0 * I * maxa * live)});
     emit(ts);
-    ts.clear();
     cnt[cmap.layer(l)] = n_o + n_down;
   }
-  // LM head: contiguous row ranges, whole stages, at most one task per SM
+  // LM head: contiguous row ranges of whole stages, at most one task per SM (on the least
+  // loaded SMs): the argmax takes one candidate per LM task
   {
     const int stages = (V + gh.RS - 1) / gh.RS;
     const int per = (stages + n_sm - 1) / n_sm;
-    std::vector<std::pair<Task, long long>> ts;
     int slot = 0;
     for (int s0 = 0; s0 < stages; s0 += per, ++slot) {
       const int r0 = s0 * gh.RS, r1 = std::min(V, (s0 + per) * gh.RS);
       ts.push_back({mkt(OP_LM, L, r0, r1 - r0, slot, TF_LAST_LM | (slot == 0 ? TF_WRITE_X : 0)), (r1 - r0) * row_h});
     }
-    c->n_lm_sm = slot;
+    P.n_lm_sm = slot;
     cnt[cmap.lm_arrive()] = slot;
-    // the LM tasks go one per SM, on the least loaded SMs
-    emit(ts);
+    std::vector<int> order(n_sm);
+    for (int i = 0; i < n_sm; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return as.load[x] < as.load[y]; });
+    std::vector<std::vector<Task>> lists(n_sm);
+    for (size_t i = 0; i < ts.size(); ++i) {
+      const int sm = order[i % n_sm];
+      as.lists[sm].push_back(ts[i].first);
+      as.load[sm] += ts[i].second;
+      lists[i % n_sm].push_back(ts[i].first);
+    }
+    per_op.push_back(std::move(lists));
+    ts.clear();
   }
 
   // flatten: megakernel lists, then per-op launches
-  std::vector<Task> all;
-  std::vector<int32_t> begin;
+  P.all.clear();
+  P.begin.clear();
   for (int s = 0; s < n_sm; ++s) {
-    begin.push_back((int32_t)all.size());
-    all.insert(all.end(), as.lists[s].begin(), as.lists[s].end());
+    P.begin.push_back((int32_t)P.all.size());
+    P.all.insert(P.all.end(), as.lists[s].begin(), as.lists[s].end());
   }
-  begin.push_back((int32_t)all.size());
-  c->n_tasks = (int)all.size();
+  P.begin.push_back((int32_t)P.all.size());
+  P.n_tasks = (int)P.all.size();
   for (auto& launch : per_op) {
     for (int s = 0; s < n_sm; ++s) {
-      begin.push_back((int32_t)all.size());
-      all.insert(all.end(), launch[s].begin(), launch[s].end());
+      P.begin.push_back((int32_t)P.all.size());
+      P.all.insert(P.all.end(), launch[s].begin(), launch[s].end());
     }
-    begin.push_back((int32_t)all.size());
+    P.begin.push_back((int32_t)P.all.size());
   }
-  c->n_op_launches = (int)per_op.size();
+  P.n_op_launches = (int)per_op.size();
+  P.load = as.load;
+  return MK_OK;
+}
 
-  // device upload
-  const size_t part = (size_t)L * B * nkv * max_chunks * (16 + 8 * (size_t)d);
-  bool okm = dalloc(&c->d_tasks, all.size()) == cudaSuccess && dalloc(&c->d_sm_begin, begin.size()) == cudaSuccess &&
-             dalloc(&c->d_cnt, cnt.size()) == cudaSuccess && dalloc(&c->d_chunk_pages, B) == cudaSuccess &&
+extern "C" mk_status mk_plan_schedule(const mk_model_cfg* cfg, int32_t n_sm, int32_t batch, const int32_t* seq_lens,
+                                      mk_plan_info* info, void* tasks, int32_t tasks_cap, int32_t* sm_begin,
+                                      int64_t* sm_bytes) {
+  if (!cfg || !info) return MK_ERR_INVALID_ARG;
+  Plan P;
+  mk_status s = plan_schedule(*cfg, n_sm, batch, seq_lens, P);
+  if (s != MK_OK) return s;
+  info->n_tasks = P.n_tasks;
+  info->n_counters = (int32_t)P.cnt.size();
+  info->max_chunks = P.max_chunks;
+  info->n_lm_sm = P.n_lm_sm;
+  info->n_op_launches = P.n_op_launches;
+  if (tasks) {
+    if (tasks_cap < P.n_tasks) return MK_ERR_INVALID_ARG;
+    memcpy(tasks, P.all.data(), sizeof(Task) * (size_t)P.n_tasks);
+  }
+  if (sm_begin) memcpy(sm_begin, P.begin.data(), sizeof(int32_t) * (size_t)(n_sm + 1));
+  if (sm_bytes)
+    for (int i = 0; i < n_sm; ++i) sm_bytes[i] = P.load[i];
+  return MK_OK;
+}
+
+extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* seq_lens, const int32_t* block_tables) {
+  if (!c) return MK_ERR_INVALID_ARG;
+  const mk_model_cfg& m = c->cfg;
+  if (batch < 1 || batch > m.max_batch || !seq_lens || !block_tables)
+    return fail(c, MK_ERR_INVALID_ARG, "batch outside 1..max_batch or null array");
+  Plan P;
+  if (plan_schedule(m, c->n_sm, batch, seq_lens, P) != MK_OK)
+    return fail(c, MK_ERR_INVALID_ARG, "sequence length negative or beyond the block table");
+  cudaDeviceSynchronize();
+  free_schedule(c);
+  const int B = batch;
+  const size_t part = (size_t)m.n_layers * B * m.n_kv_heads * P.max_chunks * (16 + 8 * (size_t)m.head_dim);
+  bool okm = dalloc(&c->d_tasks, P.all.size()) == cudaSuccess && dalloc(&c->d_sm_begin, P.begin.size()) == cudaSuccess &&
+             dalloc(&c->d_cnt, P.cnt.size()) == cudaSuccess && dalloc(&c->d_chunk_pages, B) == cudaSuccess &&
              dalloc(&c->d_n_chunks, B) == cudaSuccess && dalloc(&c->apart, part) == cudaSuccess &&
-             dalloc(&c->counters, cnt.size()) == cudaSuccess;
+             dalloc(&c->counters, P.cnt.size()) == cudaSuccess;
   if (!okm) {
     cudaGetLastError();
     free_schedule(c);
     return fail(c, MK_ERR_OOM, "schedule allocation failed");
   }
-  CK(cudaMemcpy(c->d_tasks, all.data(), all.size() * sizeof(Task), cudaMemcpyHostToDevice));
-  CK(cudaMemcpy(c->d_sm_begin, begin.data(), begin.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
-  CK(cudaMemcpy(c->d_cnt, cnt.data(), cnt.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
-  CK(cudaMemcpy(c->d_chunk_pages, chunk_pages.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice));
-  CK(cudaMemcpy(c->d_n_chunks, n_chunks.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice));
-  CK(cudaMemset(c->counters, 0, cnt.size() * sizeof(uint32_t)));
+  CK(cudaMemcpy(c->d_tasks, P.all.data(), P.all.size() * sizeof(Task), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->d_sm_begin, P.begin.data(), P.begin.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->d_cnt, P.cnt.data(), P.cnt.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->d_chunk_pages, P.chunk_pages.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->d_n_chunks, P.n_chunks.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CK(cudaMemset(c->counters, 0, P.cnt.size() * sizeof(uint32_t)));
   CK(cudaMemset(c->status, 0, ST_WORDS * sizeof(int32_t)));
-  c->n_counters = (int)cnt.size();
-  c->max_chunks = max_chunks;
+  c->n_tasks = P.n_tasks;
+  c->n_counters = (int)P.cnt.size();
+  c->max_chunks = P.max_chunks;
+  c->n_lm_sm = P.n_lm_sm;
+  c->n_op_launches = P.n_op_launches;
   c->B = B;
   c->block_table = block_tables;
   c->epoch = 0;

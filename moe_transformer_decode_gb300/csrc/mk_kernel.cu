@@ -685,16 +685,13 @@ struct Consumer {
 
   __device__ void release_counter(int idx) {
     if (!csync()) return;
-    if (threadIdx.x == 0) {
-      __threadfence();
-      red_release_add(p.counters + idx, 1u);
-    }
+    // the barrier orders every consumer's writes before thread 0's gpu-scope release
+    if (threadIdx.x == 0) red_release_add(p.counters + idx, 1u);
   }
   // arrival on `idx`; true in every consumer thread of the task that arrived last
   __device__ bool arrive_last(int idx, int count) {
     if (!csync()) return false;
     if (threadIdx.x == 0) {
-      __threadfence();
       const uint32_t old = atom_acq_rel_add(p.counters + idx, 1u);
       m.flag = ((old + 1u) % (uint32_t)count) == 0u;
     }

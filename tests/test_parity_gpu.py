@@ -7,6 +7,7 @@ agreement; KV append slot and page lookups bit-exact."""
 import numpy as np
 import pytest
 
+import synth
 from harness import Setup, check_step
 from synth import workloads as W
 
@@ -26,6 +27,11 @@ def _run(w, steps, per_layer=False, mode=0):
     try:
         for i in range(steps):
             pos = s.ctx + i
+            rng = np.random.default_rng(i)
+            touched = {int(s.bt[b, pos[b] // w.page]) for b in range(w.B)}
+            sample_pages = sorted(touched | set(rng.integers(0, s.num_pages, 16).tolist()))
+            K_before = {pg: _bits(s.K[:, pg]) for pg in sample_pages}
+            V_before = {pg: _bits(s.V[:, pg]) for pg in sample_pages}
             got_logits, got_next = s.gpu_step(tokens, pos)
             ref_logits, ref_next, tr = s.oracle_step(tokens, pos)
             acts = s.dc.activations()
@@ -34,15 +40,25 @@ def _run(w, steps, per_layer=False, mode=0):
             total += w.B
             if per_layer:
                 _check_layers(w, acts, tr)
-            # the appended K/V sit at (block_table[b][pos / 16], pos % 16) and match the oracle's
+            # the appended K/V sit at (block_table[b][pos / 16], pos % 16): the rest of those
+            # pages, and a sample of other pages, are unchanged (bit-exact indexing); the values
+            # match the oracle's within bf16 rounding
+            for pool, before in ((s.K, K_before), (s.V, V_before)):
+                for pg in sample_pages:
+                    after = _bits(pool[:, pg])
+                    keep = np.ones(after.shape, dtype=bool)
+                    for b in range(w.B):
+                        if s.bt[b, pos[b] // w.page] == pg:
+                            keep[:, :, pos[b] % w.page] = False
+                    assert np.array_equal(after[keep], before[pg][keep]), "KV bytes outside the new slots changed"
             for b in range(w.B):
                 pg, sl = s.bt[b, pos[b] // w.page], pos[b] % w.page
-                k_gpu = _bits(s.K[:, pg, :, sl])
-                v_gpu = _bits(s.V[:, pg, :, sl])
-                for got, ref in ((k_gpu, tr["k_new"][:, b]), (v_gpu, tr["v_new"][:, b])):
-                    diff = np.abs(got.astype(np.int32) - ref.astype(np.int32))
-                    assert diff.max() <= 1, "appended K/V differ by more than one bf16 ulp"
-                    assert (diff == 0).mean() > 0.99
+                for got, ref in ((_bits(s.K[:, pg, :, sl]), tr["k_new"][:, b]), (_bits(s.V[:, pg, :, sl]), tr["v_new"][:, b])):
+                    g32 = synth.bf16_bits_to_f32(got).astype(np.float64)
+                    r32 = synth.bf16_bits_to_f32(ref).astype(np.float64)
+                    scale = np.sqrt(np.mean(r32 ** 2, axis=-1, keepdims=True))
+                    assert np.all(np.abs(g32 - r32) <= 2.0 ** -7 * np.abs(r32) + 1e-4 * scale), \
+                        "appended K/V differ from the oracle beyond bf16 rounding"
             tokens = ref_next  # teacher forcing
     finally:
         s.close()

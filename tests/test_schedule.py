@@ -1,0 +1,82 @@
+"""Host scheduler (no GPU): every unit of work of the step is planned exactly once, each
+SM's list follows the global dependency order (so no counter wait can deadlock), and the
+bytes are spread evenly over the SMs."""
+import numpy as np
+import pytest
+
+from moe_transformer_decode_gb300 import binding as B
+from synth import workloads as W
+
+OP_ROUTER, OP_QKV, OP_ATTN, OP_GU, OP_O, OP_DOWN, OP_LM = range(1, 8)
+RANK = {OP_ROUTER: 0, OP_QKV: 1, OP_ATTN: 2, OP_GU: 3, OP_O: 4, OP_DOWN: 5, OP_LM: 6}
+
+
+def cfg_of(w, max_pages):
+    return B.mk_model_cfg(w.L, w.H, w.nq, w.nkv, w.d, w.E, w.topk, w.I, w.V, 16, w.B, max_pages, w.rope_theta, w.eps)
+
+
+def rows_per_stage(K):
+    kw = min(K, 2048) // 256
+    return 8 * (8 // kw)
+
+
+def _ranges(t):
+    return np.concatenate([np.arange(a, a + b) for a, b in zip(t["a"], t["b"])])
+
+
+@pytest.mark.parametrize("w,n_sm", [(W.TINY, 148), (W.SMALL, 152), (W.M30B_BS1, 148), (W.M30B_BS8, 152),
+                                    (W.TINY.with_(B=3, ctx_lo=0, ctx_hi=70), 7)])
+def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
+    ctx = W.context_lengths(w)
+    max_pages = int(np.max(ctx)) // 16 + 64
+    info, tasks, begin, load = B.mk_plan_schedule(cfg_of(w, max_pages), n_sm, ctx)
+    assert begin[0] == 0 and begin[-1] == info.n_tasks and np.all(np.diff(begin) >= 0)
+    # global order inside every SM list: (layer, opcode rank) never decreases
+    for s in range(n_sm):
+        t = tasks[begin[s]:begin[s + 1]]
+        key = t["layer"].astype(np.int64) * 10 + np.array([RANK[o] for o in t["op"]], dtype=np.int64)
+        assert np.all(np.diff(key) >= 0), f"SM {s} list out of order"
+    maxa = min(w.B * w.topk, w.E)
+    upg = (w.nq // w.nkv + 2) * (w.d // 8)
+    for l in range(w.L):
+        t = tasks[tasks["layer"] == l]
+        r = t[t["op"] == OP_ROUTER]
+        assert sorted(_ranges(r).tolist()) == list(range(w.E))
+        assert (r["flags"] & 1).sum() == 1  # exactly one task stores x of the layer
+        q = t[t["op"] == OP_QKV]
+        assert sorted(_ranges(q).tolist()) == list(range(w.nkv * upg))
+        assert np.all(q["a"] // upg == q["c"]) and np.all((q["a"] + q["b"] - 1) // upg == q["c"])
+        at = t[t["op"] == OP_ATTN]
+        keys = list(zip(at["a"].tolist(), at["b"].tolist(), at["c"].tolist()))
+        assert len(set(keys)) == len(keys)
+        for b in range(w.B):
+            n = None
+            for g in range(w.nkv):
+                ch = sorted(c for (bb, gg, c) in keys if bb == b and gg == g)
+                assert ch == list(range(len(ch))) and len(ch) >= 1
+                assert n is None or n == len(ch)
+                n = len(ch)
+        g = t[t["op"] == OP_GU]
+        assert sorted(_ranges(g).tolist()) == list(range(maxa * (w.I // (rows_per_stage(w.H) // 2))))
+        o = t[t["op"] == OP_O]
+        assert sorted(_ranges(o).tolist()) == list(range(w.H)) and np.all(o["b"] <= rows_per_stage(w.nq * w.d))
+        dn = t[t["op"] == OP_DOWN]
+        assert sorted(_ranges(dn).tolist()) == list(range(w.H)) and np.all(dn["b"] <= rows_per_stage(w.I))
+    lm = tasks[tasks["op"] == OP_LM]
+    assert sorted(_ranges(lm).tolist()) == list(range(w.V))
+    assert np.all(lm["flags"] & 2) and len(lm) == info.n_lm_sm and sorted(lm["c"].tolist()) == list(range(len(lm)))
+    owners = np.searchsorted(begin, np.nonzero(tasks["op"] == OP_LM)[0], side="right")
+    assert len(set(owners.tolist())) == len(lm), "two LM tasks on one SM"
+
+
+def test_plan_balances_bytes_over_sms():
+    w = W.M30B_BS1
+    info, tasks, begin, load = B.mk_plan_schedule(cfg_of(w, 600), 148, W.context_lengths(w))
+    assert load.max() / load.mean() < 1.02
+
+
+def test_plan_rejects_bad_arguments():
+    cfg = cfg_of(W.TINY, 4)
+    for n_sm, lens in ((148, [64]), (148, [-1]), (0, [3])):
+        with pytest.raises(B.MkError):
+            B.mk_plan_schedule(cfg, n_sm, np.array(lens, np.int32))
