@@ -179,6 +179,31 @@ mk_status mk_plan_schedule(const mk_model_cfg* cfg, int32_t n_sm, int32_t batch,
 /* Number of SMs the persistent kernel runs on and tasks per step of the current schedule. */
 mk_status mk_get_launch_info(const mk_ctx* ctx, int32_t* n_sm, int32_t* tasks_per_step, int32_t* launches_per_step);
 
+/* One decode step without allocating device memory. No counterpart on the pages that
+ * describe the method: this is a library convenience. For callers that cannot call
+ * cudaMalloc (a memory pool or arena that owns every device allocation, a host process
+ * that forbids allocation after start-up, code that must not take the allocator's locks or
+ * trigger its implicit synchronisation), this runs the same kernel as mk_decode_step with
+ * its whole workspace (activations, task lists, counters, RoPE table) placed in one static
+ * device array of MK_NOALLOC_SCRATCH_BYTES that every GPU loading the library reserves
+ * until the process exits. Nothing else is allocated: weights, KV pages, inputs and outputs
+ * come from the caller, with the same meaning and layout as for mk_create, mk_build_schedule
+ * and mk_decode_step (positions[b] must equal seq_lens[b], the lengths the step is planned
+ * for). The call plans the step on the host, copies the plan into the array, launches on
+ * `stream` and waits for that stream, so device errors (bad page, bad token, timeout) are
+ * returned directly. The first call on a device, with that device current, looks up the
+ * array's device address and configures the kernel; make that first call before any stream
+ * capture. Every call shares the array and overwrites it (counters and status are cleared
+ * at each call), so calls that overlap on the GPU, from any thread or stream, race and must
+ * be serialised by the caller. Workloads whose workspace exceeds the array (for example the
+ * 30B-shaped model) are rejected with MK_ERR_UNSUPPORTED; msg (may be NULL) receives a
+ * NUL-terminated explanation of at most msg_len bytes. */
+#define MK_NOALLOC_SCRATCH_BYTES (32u << 20)
+mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_ptrs* weights, int32_t batch,
+                                 const int32_t* seq_lens, const int32_t* block_tables, const int32_t* token_ids,
+                                 const int32_t* positions, const mk_kv_pages* kv, float* logits_out,
+                                 int32_t* argmax_out, void* stream, char* msg, int32_t msg_len);
+
 /* Releases the workspace. Safe on NULL. Does not free caller-owned memory. */
 void mk_destroy(mk_ctx* ctx);
 

@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_UNSUPPORTED", 3:
 MK_MODE_MEGAKERNEL, MK_MODE_PER_OP = 0, 1
 
 EXPORTS = ["mk_create", "mk_plan_schedule", "mk_build_schedule", "mk_decode_step", "mk_decode_greedy", "mk_status_sync", "mk_last_error",
-           "mk_set_mode", "mk_enable_trace", "mk_get_activations", "mk_get_launch_info", "mk_destroy"]
+           "mk_set_mode", "mk_enable_trace", "mk_get_activations", "mk_get_launch_info", "mk_decode_step_noalloc", "mk_destroy"]
 
 
 class mk_model_cfg(ctypes.Structure):
@@ -94,6 +94,9 @@ def lib():
         L.mk_get_activations.argtypes = [vp, ctypes.POINTER(mk_activations)]
         L.mk_get_launch_info.restype = ctypes.c_int
         L.mk_get_launch_info.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        L.mk_decode_step_noalloc.restype = ctypes.c_int
+        L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(mk_model_cfg), ctypes.POINTER(mk_weight_ptrs), i32, vp, vp,
+                                             vp, vp, ctypes.POINTER(mk_kv_pages), vp, vp, vp, ctypes.c_char_p, i32]
         L.mk_destroy.restype = None
         L.mk_destroy.argtypes = [vp]
         _lib = L
@@ -180,6 +183,20 @@ def mk_get_launch_info(ctx):
     n, t, l = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     _check(ctx, lib().mk_get_launch_info(ctx, ctypes.byref(n), ctypes.byref(t), ctypes.byref(l)))
     return n.value, t.value, l.value
+
+
+def mk_decode_step_noalloc(cfg: mk_model_cfg, weights: mk_weight_ptrs, seq_lens, block_tables, token_ids,
+                           positions, kv: mk_kv_pages, logits_out=None, argmax_out=None, stream=None) -> None:
+    """The decode step with its workspace in the library's static device array (no allocation)."""
+    import numpy as np
+
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    msg = ctypes.create_string_buffer(256)
+    st = lib().mk_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(weights), len(sl), sl.ctypes.data,
+                                      _ptr(block_tables), _ptr(token_ids), _ptr(positions), ctypes.byref(kv),
+                                      _ptr(logits_out), _ptr(argmax_out), stream, msg, len(msg))
+    if st != MK_OK:
+        raise MkError(st, msg.value.decode())
 
 
 def mk_destroy(ctx) -> None:

@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib", platform.machine())
 LIB = os.path.join(OUT, "libmk.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-UNITS = ["mk_kernel.cu", "mk_host.cpp"]
+UNITS = ["mk_kernel.cu", "mk_host.cpp", "mk_static.cu"]
 HEADERS = [os.path.join(CSRC, "mk_internal.h"), os.path.join(ROOT, "include", "mk.h")]
 
 

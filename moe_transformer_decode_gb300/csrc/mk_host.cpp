@@ -287,16 +287,7 @@ Task mkt(int op, int layer, int a, int b, int c, int flags = 0) {
 
 }  // namespace
 
-struct Plan {
-  std::vector<Task> all;          // megakernel lists (per SM), then the per-op launches' lists
-  std::vector<int32_t> begin;     // [n_sm + 1] offsets, then [n_sm + 1] per per-op launch
-  std::vector<int32_t> cnt;       // counter increments per step
-  std::vector<int32_t> chunk_pages, n_chunks;
-  std::vector<long long> load;    // planned bytes per SM (megakernel lists)
-  int max_chunks = 1, n_lm_sm = 0, n_tasks = 0, n_op_launches = 0;
-};
-
-static mk_status plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_t* seq_lens, Plan& P) {
+mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_t* seq_lens, Plan& P) {
   if (n_sm < 1 || B < 1 || B > m.max_batch || !seq_lens) return MK_ERR_INVALID_ARG;
   for (int b = 0; b < B; ++b)
     if (seq_lens[b] < 0 || seq_lens[b] >= m.max_pages_per_seq * kPage) return MK_ERR_INVALID_ARG;

@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "../../include/mk.h"
 
 namespace mk {
@@ -108,6 +110,17 @@ struct Params {
   unsigned long long* trace_count;
   long long trace_cap;
 };
+
+// The host scheduler's output for one batch (see mk_host.cpp).
+struct Plan {
+  std::vector<Task> all;          // megakernel lists (per SM), then the per-op launches' lists
+  std::vector<int32_t> begin;     // [n_sm + 1] offsets, then [n_sm + 1] per per-op launch
+  std::vector<int32_t> cnt;       // counter increments per step
+  std::vector<int32_t> chunk_pages, n_chunks;
+  std::vector<long long> load;    // planned bytes per SM (megakernel lists)
+  int max_chunks = 1, n_lm_sm = 0, n_tasks = 0, n_op_launches = 0;
+};
+mk_status plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_t* seq_lens, Plan& P);
 
 struct TensorMaps {
   CUtensorMap k, v;  // KV pools as 2D [rows][head_dim] bf16, box {64, 16}, 128B swizzle
