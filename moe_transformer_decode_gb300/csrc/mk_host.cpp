@@ -16,6 +16,7 @@
 #include <algorithm>
 #include <cmath>
 #include <queue>
+#include <tuple>
 #include <string>
 #include <vector>
 
@@ -255,21 +256,30 @@ Geo geo_of(int K) {
   return g;
 }
 
+// Least-loaded assignment. Loads are counted per layer (new_layer() restarts them), so each
+// layer's work, phase by phase, is spread evenly; ties go to the SM with the least bytes over
+// the whole step (`total`), so no SM takes the extra task in every layer.
 struct Assigner {
   int n_sm;
-  std::vector<long long> load;
+  std::vector<long long> load, total;
   std::vector<std::vector<Task>> lists;
-  std::priority_queue<std::pair<long long, int>, std::vector<std::pair<long long, int>>, std::greater<>> heap;
-  explicit Assigner(int n) : n_sm(n), load(n, 0), lists(n) {
-    for (int s = 0; s < n; ++s) heap.push({0, s});
+  typedef std::tuple<long long, long long, int> Key;
+  std::priority_queue<Key, std::vector<Key>, std::greater<>> heap;
+  explicit Assigner(int n) : n_sm(n), load(n, 0), total(n, 0), lists(n) { new_layer(); }
+  void new_layer() {
+    heap = decltype(heap)();
+    for (int s = 0; s < n_sm; ++s) {
+      load[s] = 0;
+      heap.push(Key(0, total[s], s));
+    }
   }
   int put(const Task& t, long long bytes) {
-    auto top = heap.top();
+    const int s = std::get<2>(heap.top());
     heap.pop();
-    const int s = top.second;
     lists[s].push_back(t);
     load[s] += bytes;
-    heap.push({load[s], s});
+    total[s] += bytes;
+    heap.push(Key(load[s], total[s], s));
     return s;
   }
 };
@@ -319,7 +329,11 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
 
   const int maxa = std::min(B * m.top_k, E);
   const int r2 = gh.RS / 2, tiles = I / r2;
-  const int gu_per_task = std::max(1, maxa / 8);
+  // about two QKV and two expert gate/up tasks per SM and layer (whole stages each)
+  const int upg_ = (G + 2) * (d / 8);
+  int qkv_per_task = std::max(1, (int)std::lround((double)nkv * upg_ / (2.0 * n_sm)));
+  qkv_per_task = std::max(gh.RG, (qkv_per_task + gh.RG - 1) / gh.RG * gh.RG);
+  const int gu_per_task = std::max(1, (int)std::lround((double)maxa * tiles / (2.0 * n_sm)));
   const long long row_h = 2LL * H;
   // expected live fraction of the planned expert slots (1 at batch 1)
   const double live = maxa == m.top_k ? 1.0 : std::min(1.0, (double)E * (1.0 - std::pow(1.0 - (double)m.top_k / E, B)) / maxa);
@@ -336,6 +350,12 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
 
   std::vector<std::pair<Task, long long>> ts;
   for (int l = 0; l < L; ++l) {
+    as.new_layer();
+    // Per layer, in an order that is a topological order of the dependencies (so no SM can
+    // wait on work listed after its own): router, QKV, expert gate/up (needs the routing),
+    // attention (needs its group's QKV), expert down (needs all gate/up), O-proj (needs
+    // attention). Expert work sits between QKV and attention so that it covers the time the
+    // QKV results take to complete everywhere.
     // router: one stage per task; the first task stores x of this layer
     int n_router = 0;
     for (int r0 = 0; r0 < E; r0 += gh.RS, ++n_router)
@@ -344,15 +364,23 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     cnt[cmap.router_arrive(l)] = n_router;
     cnt[cmap.route(l)] = 1;
     emit(ts);
-    // QKV units, group-major, one stage per task
+    // QKV units, group-major, a few stages per task
     const int upg = (G + 2) * (d / 8);
     for (int g = 0; g < nkv; ++g) {
       int n = 0;
-      for (int u = g * upg; u < (g + 1) * upg; u += gh.RG, ++n)
-        ts.push_back({mkt(OP_QKV, l, u, std::min(gh.RG, (g + 1) * upg - u), g),
-                      std::min(gh.RG, (g + 1) * upg - u) * 8 * row_h});
+      for (int u = g * upg; u < (g + 1) * upg; u += qkv_per_task, ++n)
+        ts.push_back({mkt(OP_QKV, l, u, std::min(qkv_per_task, (g + 1) * upg - u), g),
+                      std::min(qkv_per_task, (g + 1) * upg - u) * 8 * row_h});
       cnt[cmap.qkv(l, g)] = n;
     }
+    emit(ts);
+    // expert gate/up: units u = tile * maxa + active_rank
+    int n_gu = 0;
+    for (int u = 0; u < maxa * tiles; u += gu_per_task, ++n_gu) {
+      const int n = std::min(gu_per_task, maxa * tiles - u);
+      ts.push_back({mkt(OP_GU, l, u, n, 0), (long long)(n * live * gh.RS * row_h)});
+    }
+    cnt[cmap.gu(l)] = n_gu;
     emit(ts);
     // attention chunks
     for (int b = 0; b < B; ++b)
@@ -363,27 +391,20 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
         }
     for (int g = 0; g < nkv; ++g) cnt[cmap.attn(l, g)] = B;
     emit(ts);
-    // expert gate/up: units u = tile * maxa + active_rank
-    int n_gu = 0;
-    for (int u = 0; u < maxa * tiles; u += gu_per_task, ++n_gu) {
-      const int n = std::min(gu_per_task, maxa * tiles - u);
-      ts.push_back({mkt(OP_GU, l, u, n, 0), (long long)(n * live * gh.RS * row_h)});
-    }
-    cnt[cmap.gu(l)] = n_gu;
-    emit(ts);
-    // O-proj rows
-    int n_o = 0;
-    for (int r0 = 0; r0 < H; r0 += go.RS, ++n_o)
-      ts.push_back({mkt(OP_O, l, r0, std::min(go.RS, H - r0), 0), std::min(go.RS, H - r0) * 2LL * od});
-    emit(ts);
     // expert down rows over all active experts
     int n_down = 0;
     for (int r0 = 0; r0 < H; r0 += gi.RS, ++n_down)
       ts.push_back({mkt(OP_DOWN, l, r0, std::min(gi.RS, H - r0), 0),
                     (long long)(std::min(gi.RS, H - r0) * 2.0 * I * maxa * live)});
     emit(ts);
+    // O-proj rows
+    int n_o = 0;
+    for (int r0 = 0; r0 < H; r0 += go.RS, ++n_o)
+      ts.push_back({mkt(OP_O, l, r0, std::min(go.RS, H - r0), 0), std::min(go.RS, H - r0) * 2LL * od});
+    emit(ts);
     cnt[cmap.layer(l)] = n_o + n_down;
   }
+  as.new_layer();
   // LM head: contiguous row ranges of whole stages, at most one task per SM (on the least
   // loaded SMs): the argmax takes one candidate per LM task
   {
@@ -398,12 +419,13 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     cnt[cmap.lm_arrive()] = slot;
     std::vector<int> order(n_sm);
     for (int i = 0; i < n_sm; ++i) order[i] = i;
-    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return as.load[x] < as.load[y]; });
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return as.total[x] < as.total[y]; });
     std::vector<std::vector<Task>> lists(n_sm);
     for (size_t i = 0; i < ts.size(); ++i) {
       const int sm = order[i % n_sm];
       as.lists[sm].push_back(ts[i].first);
       as.load[sm] += ts[i].second;
+      as.total[sm] += ts[i].second;
       lists[i % n_sm].push_back(ts[i].first);
     }
     per_op.push_back(std::move(lists));
@@ -427,7 +449,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     P.begin.push_back((int32_t)P.all.size());
   }
   P.n_op_launches = (int)per_op.size();
-  P.load = as.load;
+  P.load = as.total;
   return MK_OK;
 }
 

@@ -12,6 +12,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "mk_internal.h"
@@ -36,6 +37,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// waits up to about `ns` nanoseconds with the warp suspended (woken when the phase completes)
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -125,59 +136,67 @@ __device__ __forceinline__ uint32_t target_of(const Params& p, int idx) {
   return p.epoch * (uint32_t)p.cnt_per_step[idx];
 }
 
+// Slow-path checks of every bounded wait are time based, on the SM cycle counter: the
+// abort flag (an L2 read) is looked at only every kAbortPollCycles of waiting, so a wait that
+// is about to succeed is not held up by that read; the time limit uses %globaltimer.
+constexpr long long kAbortPollCycles = 40000;  // ~20 us at 2 GHz
+
+struct WaitClock {
+  long long next_poll;
+  uint64_t t0;
+  bool started;
+  __device__ WaitClock() : next_poll(0), t0(0), started(false) {}
+  // false when the wait must give up (abort seen or time limit passed)
+  __device__ bool keep_going(const Params& p, int idx, int aux) {
+    const long long now = clock64();
+    if (!started) {
+      started = true;
+      next_poll = now + kAbortPollCycles;
+      t0 = gtimer();
+      return true;
+    }
+    if (now < next_poll) return true;
+    next_poll = now + kAbortPollCycles;
+    if (aborted(p)) return false;
+    if ((long long)(gtimer() - t0) > p.timeout_ns) {
+      report(p, MK_ERR_DEVICE_TIMEOUT, idx, aux);
+      return false;
+    }
+    return true;
+  }
+};
+
 // single-thread bounded wait; false on timeout or abort
 __device__ bool wait_counter(const Params& p, int idx) {
   const uint32_t tgt = target_of(p, idx);
   const uint32_t* c = p.counters + idx;
-  if ((int32_t)(ld_acquire(c) - tgt) >= 0) return true;
-  const uint64_t t0 = gtimer();
-  for (uint32_t it = 0;; ++it) {
-    if ((int32_t)(ld_acquire(c) - tgt) >= 0) return true;
-    if ((it & 31) == 31) {
-      if (aborted(p)) return false;
-      if ((long long)(gtimer() - t0) > p.timeout_ns) {
-        report(p, MK_ERR_DEVICE_TIMEOUT, idx, (int)(ld_acquire(c) - (tgt - (uint32_t)p.cnt_per_step[idx])));
-        return false;
-      }
-    }
-    __nanosleep(64);
+  WaitClock wc;
+  for (;;) {
+    const uint32_t v = ld_acquire(c);
+    if ((int32_t)(v - tgt) >= 0) return true;
+    if (!wc.keep_going(p, idx, (int)(v - (tgt - (uint32_t)p.cnt_per_step[idx])))) return false;
   }
 }
 // whole-warp wait (every lane performs the acquire)
 __device__ bool warp_wait(const Params& p, int idx) {
   const uint32_t tgt = target_of(p, idx);
   const uint32_t* c = p.counters + idx;
-  if (__all_sync(0xffffffffu, (int32_t)(ld_acquire(c) - tgt) >= 0)) return true;
-  const uint64_t t0 = gtimer();
-  for (uint32_t it = 0;; ++it) {
-    if (__all_sync(0xffffffffu, (int32_t)(ld_acquire(c) - tgt) >= 0)) return true;
-    if ((it & 31) == 31) {
-      int stop = 0;
-      if ((threadIdx.x & 31) == 0) {
-        if (aborted(p)) stop = 1;
-        else if ((long long)(gtimer() - t0) > p.timeout_ns) {
-          report(p, MK_ERR_DEVICE_TIMEOUT, idx, (int)(ld_acquire(c) - (tgt - (uint32_t)p.cnt_per_step[idx])));
-          stop = 1;
-        }
-      }
-      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-    }
-    __nanosleep(64);
+  WaitClock wc;
+  for (;;) {
+    const uint32_t v = ld_acquire(c);
+    if (__all_sync(0xffffffffu, (int32_t)(v - tgt) >= 0)) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0) stop = !wc.keep_going(p, idx, (int)(v - (tgt - (uint32_t)p.cnt_per_step[idx])));
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
   }
 }
 // bounded mbarrier wait
 __device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = gtimer();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15) == 15) {
-      if (aborted(p)) return false;
-      if ((long long)(gtimer() - t0) > p.timeout_ns) {
-        report(p, MK_ERR_DEVICE_TIMEOUT, -1, (int)parity);
-        return false;
-      }
-    }
+  WaitClock wc;
+  for (;;) {  // suspended between checks, so waiting warps leave the issue slots to working ones
+    if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
+    if (!wc.keep_going(p, -1, (int)parity)) return false;
   }
 }
 
@@ -225,10 +244,8 @@ __device__ __forceinline__ int pos_of(const Params& p, int b) { return p.positio
 struct AttnRange {
   int cp0, cp1, pos_end;
 };
-__device__ __forceinline__ AttnRange attn_range(const Params& p, int b, int c) {
-  const int pos = pos_of(p, b);
+__device__ __forceinline__ AttnRange attn_range(int pos, int cpp, int nch, int c) {
   const int npg = (pos + kPage - 1) / kPage;
-  const int cpp = p.chunk_pages[b], nch = p.n_chunks[b];
   AttnRange r;
   r.cp0 = c * cpp;
   r.cp1 = (c == nch - 1) ? npg : min(r.cp0 + cpp, npg);
@@ -246,8 +263,8 @@ struct Misc {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t cbar;                     // consumer-warps barrier (8 arrivals per phase)
-  float red[kConsumerWarps][64];     // cross-warp partial sums
-  float res[64 * kMaxB];             // reduced stage results [RS][B]
+  alignas(16) float red[2][kConsumerWarps][64];  // cross-warp partial sums, double-buffered by stage
+  alignas(16) float res[64 * kMaxB];             // reduced stage results [RS][B]
   float norm[kConsumerWarps][kMaxB]; // sum of squares partials
   int flag;
   int n_active;
@@ -258,8 +275,31 @@ struct Misc {
   int erank[kMaxExperts];
   int ids[kMaxB][kMaxK];
   float wk[kMaxB][kMaxK];
+  // per step (consumers): new token's position, page of its KV slot (-1 if invalid), RoPE at it,
+  // attention chunking
+  int st_pos[kMaxB];
+  int st_page[kMaxB];
+  int st_cpp[kMaxB];
+  int st_nch[kMaxB];
+  alignas(16) float2 st_rope[kMaxB][64];
+  // per layer (consumers): routing of layer rc_layer
+  int rc_n;
+  int rc_expert[kMaxActive];
+  uint32_t rc_mask[kMaxActive];
+  float rc_w[kMaxActive][kMaxB];
+  // producer-private: routed experts of layer pr_layer
+  int pr_n;
+  int pr_expert[kMaxActive];
+  // batch 1: the normalized input of the current layer, and per-warp LM argmax candidates
+  alignas(16) float nsm[2048];
+  float lmw_v[kConsumerWarps];
+  int lmw_i[kConsumerWarps];
 };
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + ((int)sizeof(Misc) + 127) / 128 * 128;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds the sm_103a opt-in limit");
+static_assert(offsetof(Misc, red) % 16 == 0 && offsetof(Misc, res) % 16 == 0 && offsetof(Misc, st_rope) % 16 == 0 &&
+                  offsetof(Misc, nsm) % 16 == 0,
+              "vector-accessed shared arrays must be 16-byte aligned");
 
 struct Ring {
   uint32_t data;  // shared address of stage 0
@@ -273,11 +313,33 @@ __device__ __forceinline__ uint32_t slot_addr(const Ring& r) { return r.data + (
 struct Producer {
   const Params& p;
   const TensorMaps& tm;
+  Misc& m;
   Ring r;
   bool ok;
   uint32_t bar, dst;
+  int pos[kMaxB], cpp[kMaxB], nch[kMaxB];  // per step
+  int route_layer;
 
-  __device__ Producer(const Params& p_, const TensorMaps& tm_, Ring r_) : p(p_), tm(tm_), r(r_), ok(true) {}
+  __device__ Producer(const Params& p_, const TensorMaps& tm_, Misc& m_, Ring r_)
+      : p(p_), tm(tm_), m(m_), r(r_), ok(true), route_layer(-1) {
+    for (int b = 0; b < kMaxB; ++b) {
+      pos[b] = b < p.B ? pos_of(p, b) : 0;
+      cpp[b] = b < p.B ? p.chunk_pages[b] : 1;
+      nch[b] = b < p.B ? p.n_chunks[b] : 1;
+    }
+  }
+
+  // the routed experts of layer l, loaded once per layer
+  __device__ bool route(int l) {
+    if (route_layer == l) return true;
+    if (!wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l))) return false;
+    const Route* rt = p.route + l;
+    const int na = __ldcg(&rt->n_active);
+    for (int a = 0; a < na; ++a) m.pr_expert[a] = __ldcg(&rt->expert[a]);
+    m.pr_n = na;
+    route_layer = l;
+    return true;
+  }
 
   __device__ bool begin(uint32_t bytes) {
     const uint32_t s = r.it % kStages;
@@ -332,46 +394,56 @@ struct Producer {
       }
       case OP_ATTN: {
         const int b = t.a, g = t.b;
-        const AttnRange ar = attn_range(p, b, t.c);
+        const AttnRange ar = attn_range(pos[b], cpp[b], nch[b], t.c);
         const int pps = attn_pps(p), halves = p.d / 64;
-        for (int pg0 = ar.cp0; pg0 < ar.cp1; pg0 += pps) {
-          const int np = min(pps, ar.cp1 - pg0);
-          int good = 0;
-          int ids[8];
-          for (int i = 0; i < np; ++i) {
-            int id = (pg0 + i < p.max_pages) ? p.block_table[b * p.max_pages + pg0 + i] : -1;
-            if (id < 0 || id >= p.num_pages) {
-              report(p, MK_ERR_BAD_PAGE, b, pg0 + i);
-              id = -1;
-            } else {
-              ++good;
+        int ids[64];  // page ids of up to 64 pages, loaded together (one round trip per 64 pages)
+        for (int base = ar.cp0; base < ar.cp1; base += 64) {
+          const int nb = min(64, ar.cp1 - base);
+          for (int i0 = 0; i0 < nb; i0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int pg = base + i0 + j;
+              v[j] = (i0 + j < nb && pg < p.max_pages) ? __ldg(&p.block_table[b * p.max_pages + pg]) : -1;
             }
-            ids[i] = id;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (i0 + j < nb) ids[i0 + j] = v[j];
           }
-          if (!begin((uint32_t)good * 2 * halves * 2048)) return false;
-          for (int i = 0; i < np; ++i) {
-            if (ids[i] < 0) continue;
-            const int row = ((l * p.num_pages + ids[i]) * p.nkv + g) * kPage;
-            const uint32_t pb = dst + (uint32_t)i * 4096 * halves;
-            for (int h = 0; h < halves; ++h) {
-              tma_2d_g2s(pb + h * 2048, &tm.k, h * 64, row, bar);
-              tma_2d_g2s(pb + (halves + h) * 2048, &tm.v, h * 64, row, bar);
+          for (int i = 0; i < nb; ++i)
+            if (ids[i] < 0 || ids[i] >= p.num_pages) {
+              report(p, MK_ERR_BAD_PAGE, b, base + i);
+              ids[i] = -1;
             }
+          for (int s0 = 0; s0 < nb; s0 += pps) {
+            const int np = min(pps, nb - s0);
+            int good = 0;
+            for (int i = 0; i < np; ++i) good += ids[s0 + i] >= 0;
+            if (!begin((uint32_t)good * 2 * halves * 2048)) return false;
+            for (int i = 0; i < np; ++i) {
+              const int id = ids[s0 + i];
+              if (id < 0) continue;
+              const int row = ((l * p.num_pages + id) * p.nkv + g) * kPage;
+              const uint32_t pb = dst + (uint32_t)i * 4096 * halves;
+              for (int h = 0; h < halves; ++h) {
+                tma_2d_g2s(pb + h * 2048, &tm.k, h * 64, row, bar);
+                tma_2d_g2s(pb + (halves + h) * 2048, &tm.v, h * 64, row, bar);
+              }
+            }
+            end();
           }
-          end();
         }
         return true;
       }
       case OP_GU: {
-        if (!wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l))) return false;
-        const Route* rt = p.route + l;
-        const int na = __ldcg(&rt->n_active), maxa = max_active(p);
+        if (!route(l)) return false;
+        const int na = m.pr_n, maxa = max_active(p);
         const Geo g = geo_of(p.H);
         const int r2 = g.RS / 2;
         for (int u = t.a; u < t.a + t.b; ++u) {
           const int a = u % maxa, tile = u / maxa;
           if (a >= na) continue;
-          const int e = __ldcg(&rt->expert[a]);
+          const int e = m.pr_expert[a];
           const uint16_t* W = p.w_gate_up + ((size_t)l * p.E + e) * 2 * p.I * p.H;
           if (!begin((uint32_t)g.RS * p.H * 2)) return false;
           bulk_g2s(dst, W + (size_t)tile * r2 * p.H, r2 * p.H * 2, bar);
@@ -396,11 +468,10 @@ struct Producer {
         return true;
       }
       case OP_DOWN: {
-        if (!wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l))) return false;
-        const Route* rt = p.route + l;
-        const int na = __ldcg(&rt->n_active);
+        if (!route(l)) return false;
+        const int na = m.pr_n;
         for (int a = 0; a < na; ++a) {
-          const int e = __ldcg(&rt->expert[a]);
+          const int e = m.pr_expert[a];
           const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + t.a) * p.I;
           if (!gemv_rows(W, t.b, p.I * 2)) return false;
         }
@@ -467,14 +538,18 @@ __device__ __forceinline__ void warp_partials_to_smem(float (&acc)[8][NB], float
   }
 }
 
-// Sum the row groups' k-slices into res[row * NB + b] for rows < rows. Caller syncs around.
+// Sum the row groups' k-slices of red into res[row * NB + b] for rows < rows, using threads
+// [t0, t0 + nthreads). Caller syncs around.
 template <int NB>
-__device__ __forceinline__ void cross_warp_reduce(Misc& m, const Geo& g, int rows) {
-  for (int t = threadIdx.x; t < rows * NB; t += 256) {
-    const int r = t / NB, b = t % NB, rg = r / 8;
+__device__ __forceinline__ void cross_warp_reduce(const float (*red)[64], float* res, const Geo& g, int rows, int t,
+                                                  int nthreads) {
+  for (int e = t; e < rows * NB; e += nthreads) {
+    const int r = e / NB, b = e % NB, rg = r / 8;
     float s = 0.f;
-    for (int k = 0; k < g.KW; ++k) s += m.red[rg * g.KW + k][(r % 8) * NB + b];
-    m.res[t] = s;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < g.KW) s += red[rg * g.KW + k][(r % 8) * NB + b];
+    res[e] = s;
   }
 }
 
@@ -483,18 +558,29 @@ template <int NB>
 __device__ __forceinline__ void gemv_stage(const uint8_t* stage, const Geo& g, int rg, int ks, int lane, int rows_valid,
                                            const float (&act)[NB][8], float (&acc)[8][NB], uint32_t bmask) {
   const uint8_t* base = stage + (size_t)(rg * 8) * g.KS * 2 + (size_t)(ks * 256 + lane * 8) * 2;
+  constexpr int RB = NB <= 2 ? 8 : (NB == 4 ? 4 : 2);  // rows whose loads are in flight together
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    if (r < rows_valid) {
-      const uint4 w = *reinterpret_cast<const uint4*>(base + (size_t)r * g.KS * 2);
-      float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y), bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+  for (int r0 = 0; r0 < 8; r0 += RB) {
+    uint4 w[RB];
+#pragma unroll
+    for (int j = 0; j < RB; ++j)
+      w[j] = r0 + j < rows_valid ? *reinterpret_cast<const uint4*>(base + (size_t)(r0 + j) * g.KS * 2)
+                                 : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      const int r = r0 + j;
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        if (bmask & (1u << b)) {
-          float s = acc[r][b];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) s = fmaf(wf[i], act[b][i], s);
-          acc[r][b] = s;
+        if (bmask & (1u << b)) {  // two accumulation chains per row
+          float s0 = fmaf(bf_lo(w[j].x), act[b][0], acc[r][b]);
+          float s1 = bf_hi(w[j].x) * act[b][1];
+          s0 = fmaf(bf_lo(w[j].y), act[b][2], s0);
+          s1 = fmaf(bf_hi(w[j].y), act[b][3], s1);
+          s0 = fmaf(bf_lo(w[j].z), act[b][4], s0);
+          s1 = fmaf(bf_hi(w[j].z), act[b][5], s1);
+          s0 = fmaf(bf_lo(w[j].w), act[b][6], s0);
+          s1 = fmaf(bf_hi(w[j].w), act[b][7], s1);
+          acc[r][b] = s0 + s1;
         }
       }
     }
@@ -518,9 +604,9 @@ __device__ __forceinline__ void load8(const float* src, float (&dst)[8]) {
 
 __device__ __forceinline__ void trace_task(const Params& p, const Task& t, uint64_t t0, uint64_t t1) {
   if (!p.trace || threadIdx.x != 0) return;
+  const uint64_t t2 = gtimer();
   const unsigned long long i = atomicAdd(p.trace_count, 1ull);
   if ((long long)i >= p.trace_cap) return;
-  const uint64_t t2 = gtimer();
   mk_trace_entry e;
   e.t_start_ns = t0;
   e.wait_ns = (uint32_t)(t1 - t0);
@@ -545,18 +631,25 @@ struct Consumer {
   int warp, lane;
   bool ok;
   uint32_t cbar, cphase;
+  int rpar;             // which half of m.red the next reduction uses
   int n_layer;          // layer whose normalized input is held in `nact` (-1 none)
+  int route_layer;      // layer whose routing is cached in m.rc_*
+  int gu_layer;         // layer whose expert gate/up work is known complete
+  int attn_layer;       // layer of attn_ok
+  uint32_t attn_ok;     // KV groups whose attention is known complete in attn_layer
   float nact[NB][8];    // this lane's 8 columns of the normalized input, per token
   float lm_best[NB];    // running LM-head argmax (threads < B)
   int lm_idx[NB];
   uint64_t t_start, t_ready;
 
   __device__ Consumer(const Params& p_, Misc& m_, Ring r_)
-      : p(p_), m(m_), r(r_), cm{p_.L, p_.nkv, p_.B}, ok(true), n_layer(-1) {
+      : p(p_), m(m_), r(r_), cm{p_.L, p_.nkv, p_.B}, ok(true), n_layer(-1), route_layer(-1), gu_layer(-1),
+        attn_layer(-1), attn_ok(0) {
     warp = threadIdx.x / 32;
     lane = threadIdx.x % 32;
     cbar = smem_addr(&m_.cbar);
     cphase = 0;
+    rpar = 0;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       lm_best[b] = -INFINITY;
@@ -651,6 +744,13 @@ struct Consumer {
 #pragma unroll
       for (int i = 0; i < 8; ++i) nact[b][i] = x[b][i] * rinv * gf[i];
     }
+    if constexpr (NB == 1) {
+      if (warp < g.KW) {
+        float4* dn = reinterpret_cast<float4*>(&m.nsm[col]);
+        dn[0] = make_float4(nact[0][0], nact[0][1], nact[0][2], nact[0][3]);
+        dn[1] = make_float4(nact[0][4], nact[0][5], nact[0][6], nact[0][7]);
+      }
+    }
     if (write_x && warp < g.KW) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
@@ -668,8 +768,11 @@ struct Consumer {
     if (n_layer != l) load_norm(l, write_x);
   }
 
-  // one GEMV stage against the held normalized input, reduced into m.res [rows][NB]
-  __device__ bool norm_gemv_stage(const Geo& g, int rows, uint32_t bmask) {
+  // One GEMV stage against the held normalized input. All warps add their partials to one
+  // half of m.red and meet once; warp 0 then reduces them into m.res [rows][NB] and runs
+  // `epi` (its lanes), while the other warps go on to the next stage.
+  template <typename Epi>
+  __device__ bool norm_gemv_stage(const Geo& g, int rows, uint32_t bmask, Epi&& epi) {
     const int rg = warp / g.KW, ks = warp % g.KW;
     float acc[8][NB];
     zero_acc(acc);
@@ -677,10 +780,15 @@ struct Consumer {
     if (!st) return false;
     if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, rows - rg * 8), nact, acc, bmask);
     release();
-    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[warp], lane);
+    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[rpar][warp], lane);
     if (!csync()) return false;
-    cross_warp_reduce<NB>(m, g, rows);
-    return csync();
+    if (warp == 0) {
+      cross_warp_reduce<NB>(m.red[rpar], m.res, g, rows, lane, 32);
+      __syncwarp();
+      epi();
+    }
+    rpar ^= 1;
+    return true;
   }
 
   __device__ void release_counter(int idx) {
@@ -699,6 +807,61 @@ struct Consumer {
     return m.flag != 0;
   }
 
+  // Per-step values every block needs, read once: positions, the new slots' pages, RoPE at the
+  // positions, attention chunking.
+  __device__ bool load_step_cache() {
+    const int hd = p.d / 2;
+    if (threadIdx.x < p.B) {
+      const int b = threadIdx.x;
+      const int pos = pos_of(p, b);
+      int page = -1;
+      if (pos >= 0 && pos / kPage < p.max_pages) {
+        page = p.block_table[b * p.max_pages + pos / kPage];
+        if (page < 0 || page >= p.num_pages) page = -1;
+      }
+      m.st_pos[b] = pos;
+      m.st_page[b] = page;
+      m.st_cpp[b] = p.chunk_pages[b];
+      m.st_nch[b] = p.n_chunks[b];
+    }
+    for (int i = threadIdx.x; i < p.B * hd; i += 256) {
+      const int b = i / hd, j = i % hd;
+      const int pos = pos_of(p, b);
+      m.st_rope[b][j] = (pos >= 0 && pos < p.max_pos) ? p.rope[(size_t)pos * hd + j] : make_float2(1.f, 0.f);
+    }
+    return csync();
+  }
+
+  // Routing of layer l in shared memory, loaded once per layer and block.
+  __device__ bool load_route(int l) {
+    if (route_layer == l) return true;
+    if (!warp_wait(p, cm.route(l))) { ok = false; return false; }
+    const Route* rt = p.route + l;
+    const int na = __ldcg(&rt->n_active);
+    for (int i = threadIdx.x; i < na; i += 256) {
+      m.rc_expert[i] = __ldcg(&rt->expert[i]);
+      m.rc_mask[i] = __ldcg(&rt->mask[i]);
+    }
+    for (int i = threadIdx.x; i < na * kMaxB; i += 256) m.rc_w[i / kMaxB][i % kMaxB] = __ldcg(&rt->w[i / kMaxB][i % kMaxB]);
+    if (threadIdx.x == 0) m.rc_n = na;
+    if (!csync()) return false;
+    route_layer = l;
+    return true;
+  }
+  __device__ bool wait_gu(int l) {
+    if (gu_layer == l) return true;
+    if (!warp_wait(p, cm.gu(l))) { ok = false; return false; }
+    gu_layer = l;
+    return true;
+  }
+  __device__ bool wait_attn_group(int l, int gg) {
+    if (attn_layer != l) { attn_layer = l; attn_ok = 0; }
+    if (attn_ok & (1u << gg)) return true;
+    if (!warp_wait(p, cm.attn(l, gg))) { ok = false; return false; }
+    attn_ok |= 1u << gg;
+    return true;
+  }
+
   // ---------------------------------------------------------------- opcodes
 
   __device__ void op_router(const Task& t) {
@@ -709,14 +872,16 @@ struct Consumer {
     const Geo g = geo_of(p.H);
     for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
       const int rows = min(g.RS, t.a + t.b - r0);
-      if (!norm_gemv_stage(g, rows, bmask_all())) return;
-      for (int i = threadIdx.x; i < rows * NB; i += 256) {
-        const int rr = i / NB, b = i % NB;
-        if (b >= p.B) continue;
-        const int e = r0 + rr;
-        const float bias = p.router_bias ? p.router_bias[(size_t)l * p.E + e] : 0.f;
-        __stcg(&p.rlogits[((size_t)l * p.B + b) * p.E + e], m.res[i] + bias);
-      }
+      const bool st_ok = norm_gemv_stage(g, rows, bmask_all(), [&] {
+        for (int i = lane; i < rows * NB; i += 32) {
+          const int rr = i / NB, b = i % NB;
+          if (b >= p.B) continue;
+          const int e = r0 + rr;
+          const float bias = p.router_bias ? p.router_bias[(size_t)l * p.E + e] : 0.f;
+          __stcg(&p.rlogits[((size_t)l * p.B + b) * p.E + e], m.res[i] + bias);
+        }
+      });
+      if (!st_ok) return;
     }
     if (!arrive_last(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) return;
     compute_routing(l);
@@ -822,27 +987,16 @@ struct Consumer {
     const int hd = p.d / 2;
     for (int u0 = t.a; u0 < t.a + t.b && ok; u0 += g.RG) {
       const int nu = min(g.RG, t.a + t.b - u0);
-      if (!norm_gemv_stage(g, nu * 8, bmask_all())) return;
+      const bool st_ok = norm_gemv_stage(g, nu * 8, bmask_all(), [&] {
       // epilogue: RoPE on q/k pairs, bf16 K/V append
-      for (int i = threadIdx.x; i < nu * 8 * NB; i += 256) {
+      for (int i = lane; i < nu * 8 * NB; i += 32) {
         const int unit = i / (8 * NB), rem = i % (8 * NB), tt = rem / NB, b = rem % NB;
         if (b >= p.B) continue;
         const QkvUnit q = qkv_unit(p, u0 + unit);
-        const int pos = pos_of(p, b);
-        if (pos < 0 || pos >= p.max_pos) {
-          if (tt == 0 && unit == 0) report(p, MK_ERR_BAD_PAGE, b, pos);
-          continue;
-        }
+        const int pos = m.st_pos[b];
+        const int page = q.kind != 0 ? m.st_page[b] : -1;
+        if (q.kind != 0 && page < 0 && tt == 0 && unit == 0) report(p, MK_ERR_BAD_PAGE, b, pos);
         const float* res = m.res + unit * 8 * NB;
-        int page = -1;
-        if (q.kind != 0) {
-          const int pi = pos / kPage;
-          page = (pos >= 0 && pi < p.max_pages) ? p.block_table[b * p.max_pages + pi] : -1;
-          if (page < 0 || page >= p.num_pages) {
-            if (tt == 0) report(p, MK_ERR_BAD_PAGE, b, pi);
-            page = -1;
-          }
-        }
         if (q.kind == 2) {  // v: 8 consecutive elements
           const int e = 8 * q.j + tt;
           const uint16_t vb = f2bf(res[tt * NB + b]);
@@ -854,7 +1008,7 @@ struct Consumer {
         if (tt >= 4) continue;  // pair (tt, tt + 4) handled by the lower row
         const int pi2 = 4 * q.j + tt;  // pair index in [0, d/2)
         const float a = res[tt * NB + b], c = res[(tt + 4) * NB + b];
-        const float2 cs = p.rope[(size_t)pos * hd + pi2];
+        const float2 cs = m.st_rope[b][pi2];
         const float lo = a * cs.x - c * cs.y;
         const float hi = a * cs.y + c * cs.x;
         if (q.kind == 0) {
@@ -873,6 +1027,8 @@ struct Consumer {
           }
         }
       }
+      });
+      if (!st_ok) return;
     }
     if (ok) release_counter(cm.qkv(l, t.c));
   }
@@ -881,24 +1037,25 @@ struct Consumer {
     const int l = t.layer;
     ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
     if (!ok) return;
-    if (!warp_wait(p, cm.route(l))) { ok = false; return; }
+    if (!load_route(l)) return;
     t_ready = gtimer();
-    const Route* rt = p.route + l;
-    const int na = __ldcg(&rt->n_active), maxa = max_active(p);
+    const int na = m.rc_n, maxa = max_active(p);
     const Geo g = geo_of(p.H);
     const int r2 = g.RS / 2;
     for (int u = t.a; u < t.a + t.b && ok; ++u) {
       const int a = u % maxa, tile = u / maxa;
       if (a >= na) continue;
-      const uint32_t bm = __ldcg(&rt->mask[a]);
-      if (!norm_gemv_stage(g, g.RS, bm)) return;
-      for (int i = threadIdx.x; i < r2 * NB; i += 256) {
-        const int tt = i / NB, b = i % NB;
-        if (!(bm & (1u << b))) continue;
-        const float gt = m.res[tt * NB + b], up = m.res[(r2 + tt) * NB + b];
-        const float hv = gt / (1.0f + expf(-gt)) * up;
-        __stcg(&p.h[(((size_t)l * kMaxActive + a) * kMaxB + b) * p.I + tile * r2 + tt], hv);
-      }
+      const uint32_t bm = m.rc_mask[a];
+      const bool st_ok = norm_gemv_stage(g, g.RS, bm, [&] {
+        for (int i = lane; i < r2 * NB; i += 32) {
+          const int tt = i / NB, b = i % NB;
+          if (!(bm & (1u << b))) continue;
+          const float gt = m.res[tt * NB + b], up = m.res[(r2 + tt) * NB + b];
+          const float hv = gt / (1.0f + expf(-gt)) * up;
+          __stcg(&p.h[(((size_t)l * kMaxActive + a) * kMaxB + b) * p.I + tile * r2 + tt], hv);
+        }
+      });
+      if (!st_ok) return;
     }
     if (ok) release_counter(cm.gu(l));
   }
@@ -916,7 +1073,7 @@ struct Consumer {
       float act[NB][8];
       if (rg < g.RG) {
         for (int gg = c0 / gw; gg <= (c0 + 255) / gw; ++gg)
-          if (!warp_wait(p, cm.attn(l, gg))) { ok = false; return; }
+          if (!wait_attn_group(l, gg)) return;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
           if (b < p.B) load8(p.attn_o + ((size_t)l * p.B + b) * p.od + c0 + lane * 8, act[b]);
@@ -931,9 +1088,10 @@ struct Consumer {
       if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, t.b - rg * 8), act, acc, bmask_all());
       release();
     }
-    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[warp], lane);
+    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[rpar][warp], lane);
     if (!csync()) return;
-    cross_warp_reduce<NB>(m, g, t.b);
+    cross_warp_reduce<NB>(m.red[rpar], m.res, g, t.b, threadIdx.x, 256);
+    rpar ^= 1;
     if (!csync()) return;
     for (int i = threadIdx.x; i < t.b * NB; i += 256) {
       const int rr = i / NB, b = i % NB;
@@ -944,23 +1102,22 @@ struct Consumer {
 
   __device__ void op_down(const Task& t) {
     const int l = t.layer;
-    if (!warp_wait(p, cm.gu(l))) { ok = false; return; }
+    if (!load_route(l) || !wait_gu(l)) return;
     t_ready = gtimer();
     const Geo g = geo_of(p.I);
     const int rg = warp / g.KW, ks = warp % g.KW;
-    const Route* rt = p.route + l;
-    const int na = __ldcg(&rt->n_active);
+    const int na = m.rc_n;
     float acc[8][NB];
     zero_acc(acc);
     for (int a = 0; a < na; ++a) {
-      const uint32_t bm = __ldcg(&rt->mask[a]);
+      const uint32_t bm = m.rc_mask[a];
       float act[NB][8];
       if (rg < g.RG) {
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
           if (bm & (1u << b)) {
             load8(p.h + (((size_t)l * kMaxActive + a) * kMaxB + b) * p.I + ks * 256 + lane * 8, act[b]);
-            const float wgt = __ldcg(&rt->w[a][b]);
+            const float wgt = m.rc_w[a][b];
 #pragma unroll
             for (int i = 0; i < 8; ++i) act[b][i] *= wgt;
           } else {
@@ -974,9 +1131,10 @@ struct Consumer {
       if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, t.b - rg * 8), act, acc, bm);
       release();
     }
-    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[warp], lane);
+    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[rpar][warp], lane);
     if (!csync()) return;
-    cross_warp_reduce<NB>(m, g, t.b);
+    cross_warp_reduce<NB>(m.red[rpar], m.res, g, t.b, threadIdx.x, 256);
+    rpar ^= 1;
     if (!csync()) return;
     for (int i = threadIdx.x; i < t.b * NB; i += 256) {
       const int rr = i / NB, b = i % NB;
@@ -992,28 +1150,29 @@ struct Consumer {
     const Geo g = geo_of(p.H);
     for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
       const int rows = min(g.RS, t.a + t.b - r0);
-      if (!norm_gemv_stage(g, rows, bmask_all())) return;
-      if (p.logits)
-        for (int i = threadIdx.x; i < rows * NB; i += 256) {
-          const int rr = i / NB, b = i % NB;
-          if (b < p.B) __stcg(&p.logits[(size_t)b * p.V + r0 + rr], m.res[i]);
-        }
-      if (threadIdx.x < NB) {  // rows ascending: strict > keeps the lowest id on ties
-        const int b = threadIdx.x;
-        float bv = lm_best[b];
-        int bi = lm_idx[b];
-        for (int rr = 0; rr < rows; ++rr) {
-          const float v = m.res[rr * NB + b];
+      const bool st_ok = norm_gemv_stage(g, rows, bmask_all(), [&] {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int e = lane; e < rows * NB; e += 32) {  // e % NB == lane % NB since 32 % NB == 0
+          const int rr = e / NB, b = e % NB;
+          const float v = m.res[e];
+          if (b < p.B && p.logits) __stcg(&p.logits[(size_t)b * p.V + r0 + rr], v);
           if (v > bv || (v == bv && r0 + rr < bi)) { bv = v; bi = r0 + rr; }
         }
-        lm_best[b] = bv;
-        lm_idx[b] = bi;
-      }
+#pragma unroll
+        for (int o = 16; o >= NB; o >>= 1) {  // combine lanes of the same token, lowest id on ties
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (bv > lm_best[0] || (bv == lm_best[0] && bi < lm_idx[0])) { lm_best[0] = bv; lm_idx[0] = bi; }
+      });
+      if (!st_ok) return;
     }
     if (!(t.flags & TF_LAST_LM) || !ok) return;
-    if (threadIdx.x < NB && threadIdx.x < p.B) {
-      __stcg(&p.lm_best_v[t.c * kMaxB + threadIdx.x], lm_best[threadIdx.x]);
-      __stcg(&p.lm_best_i[t.c * kMaxB + threadIdx.x], lm_idx[threadIdx.x]);
+    if (threadIdx.x < NB && threadIdx.x < p.B) {  // warp 0, lane b: token b
+      __stcg(&p.lm_best_v[t.c * kMaxB + threadIdx.x], lm_best[0]);
+      __stcg(&p.lm_best_i[t.c * kMaxB + threadIdx.x], lm_idx[0]);
     }
     if (!arrive_last(cm.lm_arrive(), p.n_lm_sm)) return;
     if (threadIdx.x < p.B) {
@@ -1029,6 +1188,217 @@ struct Consumer {
     }
   }
 
+
+  // ---------------------------------------------------------------- batch-1 row-per-warp opcodes
+  // With one token, a warp owns whole rows of a stage (all H columns, the normalized input in
+  // registers), so each row needs only a warp reduction and its epilogue runs in that warp: no
+  // block-wide barrier per stage.
+
+  // this lane's columns pp*256 + lane*8 + i of the normalized input held in m.nsm
+  __device__ __forceinline__ void rows_act(float (&a)[64]) const {
+    const int np = p.H / 256;
+#pragma unroll
+    for (int pp = 0; pp < 8; ++pp) {
+      if (pp < np) {
+        const float4 x = *reinterpret_cast<const float4*>(&m.nsm[pp * 256 + lane * 8]);
+        const float4 y = *reinterpret_cast<const float4*>(&m.nsm[pp * 256 + lane * 8 + 4]);
+        a[pp * 8 + 0] = x.x; a[pp * 8 + 1] = x.y; a[pp * 8 + 2] = x.z; a[pp * 8 + 3] = x.w;
+        a[pp * 8 + 4] = y.x; a[pp * 8 + 5] = y.y; a[pp * 8 + 6] = y.z; a[pp * 8 + 7] = y.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[pp * 8 + i] = 0.f;
+      }
+    }
+  }
+  // full-warp dot of one shared-memory row (np * 256 bf16 columns) with a
+  __device__ __forceinline__ float rdot(const uint8_t* row, int np, const float (&a)[64]) const {
+    uint4 w[8];
+#pragma unroll
+    for (int pp = 0; pp < 8; ++pp)
+      w[pp] = pp < np ? *reinterpret_cast<const uint4*>(row + (size_t)(pp * 256 + lane * 8) * 2) : make_uint4(0, 0, 0, 0);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < 8; ++pp) {
+      s0 = fmaf(bf_lo(w[pp].x), a[pp * 8 + 0], s0);
+      s1 = fmaf(bf_hi(w[pp].x), a[pp * 8 + 1], s1);
+      s0 = fmaf(bf_lo(w[pp].y), a[pp * 8 + 2], s0);
+      s1 = fmaf(bf_hi(w[pp].y), a[pp * 8 + 3], s1);
+      s0 = fmaf(bf_lo(w[pp].z), a[pp * 8 + 4], s0);
+      s1 = fmaf(bf_hi(w[pp].z), a[pp * 8 + 5], s1);
+      s0 = fmaf(bf_lo(w[pp].w), a[pp * 8 + 6], s0);
+      s1 = fmaf(bf_hi(w[pp].w), a[pp * 8 + 7], s1);
+    }
+    float s = s0 + s1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+  }
+
+  __device__ void op_router_r(const Task& t) {
+    const int l = t.layer;
+    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
+    if (!ok) return;
+    t_ready = gtimer();
+    float a[64];
+    rows_act(a);
+    const int np = p.H / 256;
+    const Geo g = geo_of(p.H);
+    for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS) {
+      const int rows = min(g.RS, t.a + t.b - r0);
+      const uint8_t* st = acquire();
+      if (!st) return;
+      for (int r = warp; r < rows; r += kConsumerWarps) {
+        const float s = rdot(st + (size_t)r * p.H * 2, np, a);
+        if (lane == 0) {
+          const int e = r0 + r;
+          const float bias = p.router_bias ? p.router_bias[(size_t)l * p.E + e] : 0.f;
+          __stcg(&p.rlogits[(size_t)l * p.E + e], s + bias);
+        }
+      }
+      release();
+    }
+    if (!arrive_last(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) return;
+    compute_routing(l);
+    if (ok) release_counter(cm.route(l));
+  }
+
+  __device__ void op_qkv_r(const Task& t) {
+    const int l = t.layer;
+    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
+    if (!ok) return;
+    t_ready = gtimer();
+    float a[64];
+    rows_act(a);
+    const Geo g = geo_of(p.H);
+    const int np = p.H / 256, hd = p.d / 2;
+    const int pos = m.st_pos[0], page = m.st_page[0];
+    for (int u0 = t.a; u0 < t.a + t.b; u0 += g.RG) {
+      const int nu = min(g.RG, t.a + t.b - u0);
+      const uint8_t* st = acquire();
+      if (!st) return;
+      int item = 0;
+      for (int i = 0; i < nu; ++i) {
+        const QkvUnit q = qkv_unit(p, u0 + i);
+        const uint8_t* ub = st + (size_t)i * 8 * p.H * 2;
+        if (q.kind == 2) {  // v: 8 rows = 8 consecutive elements of v head q.head
+          for (int tt = 0; tt < 8; ++tt, ++item) {
+            if (item % kConsumerWarps != warp) continue;
+            const float s = rdot(ub + (size_t)tt * p.H * 2, np, a);
+            if (lane == 0) {
+              const int e = 8 * q.j + tt;
+              const uint16_t vb = f2bf(s);
+              __stcg(&p.vnew[((size_t)l * p.nkv + q.head) * p.d + e], bf2f(vb));
+              if (page >= 0)
+                p.vpool[((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d + e] = vb;
+            }
+          }
+        } else {  // q or k: RoPE pair (4 j + tt, 4 j + tt + d/2) from rows tt and tt + 4
+          for (int tt = 0; tt < 4; ++tt, ++item) {
+            if (item % kConsumerWarps != warp) continue;
+            const float x0 = rdot(ub + (size_t)tt * p.H * 2, np, a);
+            const float x1 = rdot(ub + (size_t)(tt + 4) * p.H * 2, np, a);
+            if (lane == 0) {
+              const int pi2 = 4 * q.j + tt;
+              const float2 cs = m.st_rope[0][pi2];
+              const float lo = x0 * cs.x - x1 * cs.y;
+              const float hi = x0 * cs.y + x1 * cs.x;
+              if (q.kind == 0) {
+                float* dst = p.q + ((size_t)l * p.nq + q.head) * p.d;
+                __stcg(dst + pi2, lo);
+                __stcg(dst + pi2 + hd, hi);
+              } else {
+                const uint16_t kl = f2bf(lo), kh = f2bf(hi);
+                float* dst = p.knew + ((size_t)l * p.nkv + q.head) * p.d;
+                __stcg(dst + pi2, bf2f(kl));
+                __stcg(dst + pi2 + hd, bf2f(kh));
+                if (page >= 0) {
+                  uint16_t* kp = p.kpool + ((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d;
+                  kp[pi2] = kl;
+                  kp[pi2 + hd] = kh;
+                }
+              }
+            }
+          }
+        }
+      }
+      release();
+    }
+    if (page < 0 && threadIdx.x == 0) report(p, MK_ERR_BAD_PAGE, 0, pos);
+    release_counter(cm.qkv(l, t.c));
+  }
+
+  __device__ void op_gu_r(const Task& t) {
+    const int l = t.layer;
+    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
+    if (!ok || !load_route(l)) return;
+    t_ready = gtimer();
+    float a[64];
+    rows_act(a);
+    const int na = m.rc_n, maxa = max_active(p);
+    const Geo g = geo_of(p.H);
+    const int r2 = g.RS / 2, np = p.H / 256;
+    for (int u = t.a; u < t.a + t.b; ++u) {
+      const int ar = u % maxa, tile = u / maxa;
+      if (ar >= na) continue;
+      const uint8_t* st = acquire();
+      if (!st) return;
+      for (int tt = warp; tt < r2; tt += kConsumerWarps) {
+        const float gt = rdot(st + (size_t)tt * p.H * 2, np, a);
+        const float up = rdot(st + (size_t)(r2 + tt) * p.H * 2, np, a);
+        if (lane == 0)
+          __stcg(&p.h[((size_t)l * kMaxActive + ar) * kMaxB * p.I + tile * r2 + tt], gt / (1.0f + expf(-gt)) * up);
+      }
+      release();
+    }
+    release_counter(cm.gu(l));
+  }
+
+  __device__ void op_lm_r(const Task& t) {
+    ensure_norm(p.L, (t.flags & TF_WRITE_X) != 0);
+    if (!ok) return;
+    t_ready = gtimer();
+    float a[64];
+    rows_act(a);
+    const int np = p.H / 256;
+    const Geo g = geo_of(p.H);
+    for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS) {
+      const int rows = min(g.RS, t.a + t.b - r0);
+      const uint8_t* st = acquire();
+      if (!st) return;
+      for (int r = warp; r < rows; r += kConsumerWarps) {  // ascending rows per warp
+        const float s = rdot(st + (size_t)r * p.H * 2, np, a);
+        if (lane == 0) {
+          const int v = r0 + r;
+          if (p.logits) __stcg(&p.logits[v], s);
+          if (s > lm_best[0] || (s == lm_best[0] && v < lm_idx[0])) { lm_best[0] = s; lm_idx[0] = v; }
+        }
+      }
+      release();
+    }
+    if (!(t.flags & TF_LAST_LM)) return;
+    if (lane == 0) { m.lmw_v[warp] = lm_best[0]; m.lmw_i[warp] = lm_idx[0]; }
+    if (!csync()) return;
+    if (threadIdx.x == 0) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int w = 0; w < kConsumerWarps; ++w)
+        if (m.lmw_v[w] > bv || (m.lmw_v[w] == bv && m.lmw_i[w] < bi)) { bv = m.lmw_v[w]; bi = m.lmw_i[w]; }
+      __stcg(&p.lm_best_v[t.c * kMaxB], bv);
+      __stcg(&p.lm_best_i[t.c * kMaxB], bi);
+    }
+    if (!arrive_last(cm.lm_arrive(), p.n_lm_sm)) return;
+    if (threadIdx.x == 0) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int s = 0; s < p.n_lm_sm; ++s) {
+        const float v = __ldcg(&p.lm_best_v[s * kMaxB]);
+        const int i = __ldcg(&p.lm_best_i[s * kMaxB]);
+        if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+      }
+      if (p.argmax_out) p.argmax_out[0] = bi;
+    }
+  }
+
   // Paged GQA attention of one (sequence b, KV group g, chunk). The G <= 8 query heads of the
   // group are the 16 rows of an mma A operand: rows 0..7 hold the bf16 "hi" part of q and rows
   // 8..15 its rounding residual, so S = q K^T comes out at ~fp32 accuracy; P is split the same
@@ -1037,7 +1407,7 @@ struct Consumer {
     const int l = t.layer, b = t.a, g = t.b;
     if (!warp_wait(p, cm.qkv(l, g))) { ok = false; return; }
     t_ready = gtimer();
-    const AttnRange ar = attn_range(p, b, t.c);
+    const AttnRange ar = attn_range(m.st_pos[b], m.st_cpp[b], m.st_nch[b], t.c);
     const int pps = attn_pps(p), halves = p.d / 64, ksteps = p.d / 16;
     const int pi = warp % pps, dp = warp / pps;
     const int head = lane >> 2, tig = lane & 3;
@@ -1178,10 +1548,10 @@ struct Consumer {
       for (int i = threadIdx.x; i < 16 + 8 * p.d; i += 256) __stcg(part + i, i < 8 ? -INFINITY : 0.f);
     }
     const int arr = cm.attn_arrive(l, b, g);
-    if (!arrive_last(arr, p.n_chunks[b])) return;
+    if (!arrive_last(arr, m.st_nch[b])) return;
 
     // combine the chunks of (b, g) with the new token (position pos, read from knew / vnew)
-    const int nch = p.n_chunks[b];
+    const int nch = m.st_nch[b];
     const float* pbase = p.apart + (((size_t)l * p.B + b) * p.nkv + g) * p.max_chunks * (16 + 8 * (size_t)p.d);
     // s_new per head: warp h < group
     if (warp < p.group) {
@@ -1195,22 +1565,68 @@ struct Consumer {
     }
     if (!csync()) return;
     const float* vn = p.vnew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
-    for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
-      const int h = i / p.d, dd = i % p.d;
-      const float sn = m.res[h];
-      float M = sn;
-      for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(pbase + (size_t)c * (16 + 8 * p.d) + h));
-      float fn = exp2f(sn - M);
-      float L = fn, O = fn * __ldcg(vn + dd);
-      for (int c = 0; c < nch; ++c) {
-        const float* src = pbase + (size_t)c * (16 + 8 * p.d);
-        const float mc = __ldcg(src + h);
-        if (mc == -INFINITY) continue;
-        const float f = exp2f(mc - M);
-        L += __ldcg(src + 8 + h) * f;
-        O += __ldcg(src + 16 + h * p.d + dd) * f;
+    const size_t cstride = 16 + 8 * (size_t)p.d;
+    if (nch <= 64) {
+      // chunk maxima and sums in one parallel load round, scale factors in shared memory, then
+      // independent loads of the chunk outputs
+      float* sm_m = &m.red[0][0][0];  // [nch][8]: chunk max, then its scale factor
+      float* sm_l = &m.red[1][0][0];  // [nch][8]: chunk sum
+      for (int i = threadIdx.x; i < nch * 8; i += 256) {
+        const float* src = pbase + (size_t)(i / 8) * cstride;
+        sm_m[i] = __ldcg(src + (i % 8));
+        sm_l[i] = __ldcg(src + 8 + (i % 8));
       }
-      __stcg(&p.attn_o[((size_t)l * p.B + b) * p.od + (g * p.group + h) * p.d + dd], O / L);
+      if (!csync()) return;
+      if (threadIdx.x < p.group) {
+        const int h = threadIdx.x;
+        const float sn = m.res[h];
+        float M = sn;
+        for (int c = 0; c < nch; ++c) M = fmaxf(M, sm_m[c * 8 + h]);
+        const float fn = exp2f(sn - M);
+        float L = fn;
+        for (int c = 0; c < nch; ++c) {
+          const float mc = sm_m[c * 8 + h];
+          const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
+          L += sm_l[c * 8 + h] * f;
+          sm_m[c * 8 + h] = f;
+        }
+        m.res[8 + h] = fn;
+        m.res[16 + h] = 1.0f / L;
+      }
+      if (!csync()) return;
+      for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
+        const int h = i / p.d, dd = i % p.d;
+        const float* src = pbase + 16 + h * p.d + dd;
+        float O = m.res[8 + h] * __ldcg(vn + dd);
+        int c = 0;
+        for (; c + 8 <= nch; c += 8) {
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (size_t)(c + j) * cstride);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) O = fmaf(v[j], sm_m[(c + j) * 8 + h], O);
+        }
+        for (; c < nch; ++c) O = fmaf(__ldcg(src + (size_t)c * cstride), sm_m[c * 8 + h], O);
+        __stcg(&p.attn_o[((size_t)l * p.B + b) * p.od + (g * p.group + h) * p.d + dd], O * m.res[16 + h]);
+      }
+    } else {
+      for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
+        const int h = i / p.d, dd = i % p.d;
+        const float sn = m.res[h];
+        float M = sn;
+        for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(pbase + (size_t)c * cstride + h));
+        float fn = exp2f(sn - M);
+        float L = fn, O = fn * __ldcg(vn + dd);
+        for (int c = 0; c < nch; ++c) {
+          const float* src = pbase + (size_t)c * cstride;
+          const float mc = __ldcg(src + h);
+          if (mc == -INFINITY) continue;
+          const float f = exp2f(mc - M);
+          L += __ldcg(src + 8 + h) * f;
+          O += __ldcg(src + 16 + h * p.d + dd) * f;
+        }
+        __stcg(&p.attn_o[((size_t)l * p.B + b) * p.od + (g * p.group + h) * p.d + dd], O / L);
+      }
     }
     release_counter(cm.attn(l, g));
   }
@@ -1218,14 +1634,26 @@ struct Consumer {
   __device__ void run_task(const Task& t) {
     t_start = gtimer();
     t_ready = t_start;
-    switch (t.op) {
-      case OP_ROUTER: op_router(t); break;
-      case OP_QKV: op_qkv(t); break;
-      case OP_ATTN: op_attn(t); break;
-      case OP_GU: op_gu(t); break;
-      case OP_O: op_o(t); break;
-      case OP_DOWN: op_down(t); break;
-      case OP_LM: op_lm(t); break;
+    if constexpr (NB == 1) {
+      switch (t.op) {
+        case OP_ROUTER: op_router_r(t); break;
+        case OP_QKV: op_qkv_r(t); break;
+        case OP_ATTN: op_attn(t); break;
+        case OP_GU: op_gu_r(t); break;
+        case OP_O: op_o(t); break;
+        case OP_DOWN: op_down(t); break;
+        case OP_LM: op_lm_r(t); break;
+      }
+    } else {
+      switch (t.op) {
+        case OP_ROUTER: op_router(t); break;
+        case OP_QKV: op_qkv(t); break;
+        case OP_ATTN: op_attn(t); break;
+        case OP_GU: op_gu(t); break;
+        case OP_O: op_o(t); break;
+        case OP_DOWN: op_down(t); break;
+        case OP_LM: op_lm(t); break;
+      }
     }
     if (ok) trace_task(p, t, t_start, t_ready ? t_ready : t_start);
   }
@@ -1258,18 +1686,48 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
 
   if (threadIdx.x / 32 == kConsumerWarps) {
     if ((threadIdx.x & 31) != 0) return;
-    Producer pr(p, tm, ring);
-    for (int i = t0; i < t1; ++i) {
-      const Task t = p.tasks[i];
-      if (!pr.run_task(t)) break;
+    Producer pr(p, tm, misc, ring);
+    // descriptors in batches of 8, the next batch loaded while the current one runs
+    const uint4* src = reinterpret_cast<const uint4*>(p.tasks);
+    uint4 cur[8], nxt[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cur[j] = t0 + j < t1 ? __ldg(src + t0 + j) : make_uint4(0, 0, 0, 0);
+    bool fine = true;
+    for (int base = t0; base < t1 && fine; base += 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) nxt[j] = base + 8 + j < t1 ? __ldg(src + base + 8 + j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (fine && base + j < t1) {
+          const Task t = *reinterpret_cast<const Task*>(&cur[j]);
+          fine = pr.run_task(t);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
     }
     pr.drain();  // never leave while a copy into this CTA's shared memory is in flight
     return;
   }
   Consumer<NB> c(p, misc, ring);
-  for (int i = t0; i < t1 && c.ok; ++i) {
-    const Task t = p.tasks[i];
-    c.run_task(t);
+  if (!c.load_step_cache()) return;
+  // descriptors in batches of 32 (lane j holds descriptor base + j), the next batch loaded
+  // while the current one runs; each task is broadcast from its lane
+  const uint4* src = reinterpret_cast<const uint4*>(p.tasks);
+  const int lane = threadIdx.x & 31;
+  uint4 cur = t0 + lane < t1 ? __ldg(src + t0 + lane) : make_uint4(0, 0, 0, 0);
+  for (int base = t0; base < t1 && c.ok; base += 32) {
+    const uint4 nxt = base + 32 + lane < t1 ? __ldg(src + base + 32 + lane) : make_uint4(0, 0, 0, 0);
+    const int n = min(32, t1 - base);
+    for (int j = 0; j < n && c.ok; ++j) {
+      uint4 v;
+      v.x = __shfl_sync(0xffffffffu, cur.x, j);
+      v.y = __shfl_sync(0xffffffffu, cur.y, j);
+      v.z = __shfl_sync(0xffffffffu, cur.z, j);
+      v.w = __shfl_sync(0xffffffffu, cur.w, j);
+      c.run_task(*reinterpret_cast<const Task*>(&v));
+    }
+    cur = nxt;
   }
 }
 

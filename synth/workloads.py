@@ -65,8 +65,10 @@ M30B_BS1 = Workload("moe30b_a3b_bs1_ctx8k", L=48, H=2048, nq=32, nkv=4, d=128, E
 M30B_BS8 = M30B_BS1.with_(name="moe30b_a3b_bs8_ctx1k8k", B=8, ctx_lo=1024, ctx_hi=8192, seed=3)
 M30B_BS8_ZIPF = M30B_BS8.with_(name="moe30b_a3b_bs8_ctx1k8k_zipf", routing="zipf")
 M30B_256K = M30B_BS1.with_(name="moe30b_a3b_bs1_ctx256k", ctx_lo=262144, ctx_hi=262144, steps=256, seed=4)
+# the 30B-shaped layer and LM head with 4 layers: small enough (~1.8 GB) for profiler captures
+M30B_L4 = M30B_BS1.with_(name="moe30b_shape_l4_bs1_ctx8k", L=4)
 
-ALL = {w.name: w for w in (TINY, SMALL, M30B_BS1, M30B_BS8, M30B_BS8_ZIPF, M30B_256K)}
+ALL = {w.name: w for w in (TINY, SMALL, M30B_BS1, M30B_BS8, M30B_BS8_ZIPF, M30B_256K, M30B_L4)}
 
 
 def context_lengths(w: Workload) -> np.ndarray:

@@ -8,7 +8,7 @@ from moe_transformer_decode_gb300 import binding as B
 from synth import workloads as W
 
 OP_ROUTER, OP_QKV, OP_ATTN, OP_GU, OP_O, OP_DOWN, OP_LM = range(1, 8)
-RANK = {OP_ROUTER: 0, OP_QKV: 1, OP_ATTN: 2, OP_GU: 3, OP_O: 4, OP_DOWN: 5, OP_LM: 6}
+RANK = {OP_ROUTER: 0, OP_QKV: 1, OP_GU: 2, OP_ATTN: 3, OP_DOWN: 4, OP_O: 5, OP_LM: 6}
 
 
 def cfg_of(w, max_pages):
