@@ -150,7 +150,7 @@ mk_status mk_enable_trace(mk_ctx* ctx, void* dev_buf, size_t bytes);
 /* Device pointers to the library-owned per-layer activations of the last step, for
  * inspection (fp32 unless noted; valid until mk_destroy or the next mk_build_schedule):
  *   x [n_layers+1][batch][hidden]  residual stream entering layer l (x[n_layers] final)
- *   q [n_layers][batch][n_q][head_dim] after RoPE
+ *   q [n_layers][batch][n_q][head_dim] before RoPE (attention applies it when it loads q)
  *   attn [n_layers][batch][n_q][head_dim] attention output per head
  *   attn_out, moe_out [n_layers][batch][hidden]
  *   router [n_layers][batch][n_experts] logits with bias

@@ -188,7 +188,7 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
              dalloc(&c->vnew, L * Bm * m.n_kv_heads * d) == cudaSuccess && dalloc(&c->attn_o, L * Bm * od) == cudaSuccess &&
              dalloc(&c->attn_out, L * Bm * H) == cudaSuccess && dalloc(&c->moe_out, L * Bm * H) == cudaSuccess &&
              dalloc(&c->rlogits, L * Bm * m.n_experts) == cudaSuccess &&
-             dalloc(&c->h, L * kMaxActive * kMaxB * (size_t)m.expert_inter) == cudaSuccess &&
+             dalloc(&c->h, L * kMaxActive * kMaxB * 2 * (size_t)m.expert_inter) == cudaSuccess &&
              dalloc(&c->route, L) == cudaSuccess && dalloc(&c->lm_best_v, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
              dalloc(&c->lm_best_i, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
              dalloc(&c->rope, (size_t)c->max_pos * (d / 2)) == cudaSuccess && dalloc(&c->status, ST_WORDS) == cudaSuccess &&
@@ -328,7 +328,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   }
 
   const int maxa = std::min(B * m.top_k, E);
-  const int r2 = gh.RS / 2, tiles = I / r2;
+  const int tiles = 2 * I / gh.RS;  // gate/up tiles: RS consecutive rows of [gate; up]
   // about two QKV and two expert gate/up tasks per SM and layer (whole stages each)
   const int upg_ = (G + 2) * (d / 8);
   int qkv_per_task = std::max(1, (int)std::lround((double)nkv * upg_ / (2.0 * n_sm)));

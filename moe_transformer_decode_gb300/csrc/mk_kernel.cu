@@ -439,15 +439,13 @@ struct Producer {
         if (!route(l)) return false;
         const int na = m.pr_n, maxa = max_active(p);
         const Geo g = geo_of(p.H);
-        const int r2 = g.RS / 2;
         for (int u = t.a; u < t.a + t.b; ++u) {
           const int a = u % maxa, tile = u / maxa;
           if (a >= na) continue;
           const int e = m.pr_expert[a];
           const uint16_t* W = p.w_gate_up + ((size_t)l * p.E + e) * 2 * p.I * p.H;
           if (!begin((uint32_t)g.RS * p.H * 2)) return false;
-          bulk_g2s(dst, W + (size_t)tile * r2 * p.H, r2 * p.H * 2, bar);
-          bulk_g2s(dst + r2 * p.H * 2, W + (size_t)(p.I + tile * r2) * p.H, r2 * p.H * 2, bar);
+          bulk_g2s(dst, W + (size_t)tile * g.RS * p.H, (uint32_t)g.RS * p.H * 2, bar);
           end();
         }
         return true;
@@ -671,6 +669,18 @@ struct Consumer {
     ++r.it;
   }
   __device__ uint32_t bmask_all() const { return (1u << p.B) - 1u; }
+  // h holds, per (layer, active expert, token), the raw gate then up projections [2I]
+  __device__ __forceinline__ size_t h_index(int l, int a, int b) const {
+    return (((size_t)l * kMaxActive + a) * kMaxB + b) * 2 * (size_t)p.I;
+  }
+  // SiLU(gate) * up * routing weight for 8 consecutive intermediate columns
+  __device__ __forceinline__ void load_h8(int l, int a, int b, int col, float wgt, float (&dst)[8]) const {
+    float gt[8], up[8];
+    load8(p.h + h_index(l, a, b) + col, gt);
+    load8(p.h + h_index(l, a, b) + p.I + col, up);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = gt[i] / (1.0f + expf(-gt[i])) * up[i] * wgt;
+  }
 
   // Barrier of the 8 consumer warps on an mbarrier, with the same time limit as every other
   // wait: a warp that gives up (timeout or abort) leaves the kernel and the rest follow.
@@ -1005,17 +1015,18 @@ struct Consumer {
             p.vpool[((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d + e] = vb;
           continue;
         }
-        if (tt >= 4) continue;  // pair (tt, tt + 4) handled by the lower row
+        if (q.kind == 0) {  // q is stored before RoPE; attention rotates it when it loads it
+          const int e = 4 * q.j + (tt & 3) + (tt >= 4 ? hd : 0);
+          __stcg(&p.q[(((size_t)l * p.B + b) * p.nq + q.head) * p.d + e], res[tt * NB + b]);
+          continue;
+        }
+        if (tt >= 4) continue;  // k pair (tt, tt + 4) handled by the lower row
         const int pi2 = 4 * q.j + tt;  // pair index in [0, d/2)
         const float a = res[tt * NB + b], c = res[(tt + 4) * NB + b];
         const float2 cs = m.st_rope[b][pi2];
         const float lo = a * cs.x - c * cs.y;
         const float hi = a * cs.y + c * cs.x;
-        if (q.kind == 0) {
-          float* dst = p.q + (((size_t)l * p.B + b) * p.nq + q.head) * p.d;
-          __stcg(dst + pi2, lo);
-          __stcg(dst + pi2 + hd, hi);
-        } else {
+        {
           const uint16_t kl = f2bf(lo), kh = f2bf(hi);
           float* dst = p.knew + (((size_t)l * p.B + b) * p.nkv + q.head) * p.d;
           __stcg(dst + pi2, bf2f(kl));
@@ -1041,18 +1052,14 @@ struct Consumer {
     t_ready = gtimer();
     const int na = m.rc_n, maxa = max_active(p);
     const Geo g = geo_of(p.H);
-    const int r2 = g.RS / 2;
     for (int u = t.a; u < t.a + t.b && ok; ++u) {
       const int a = u % maxa, tile = u / maxa;
       if (a >= na) continue;
       const uint32_t bm = m.rc_mask[a];
       const bool st_ok = norm_gemv_stage(g, g.RS, bm, [&] {
-        for (int i = lane; i < r2 * NB; i += 32) {
-          const int tt = i / NB, b = i % NB;
-          if (!(bm & (1u << b))) continue;
-          const float gt = m.res[tt * NB + b], up = m.res[(r2 + tt) * NB + b];
-          const float hv = gt / (1.0f + expf(-gt)) * up;
-          __stcg(&p.h[(((size_t)l * kMaxActive + a) * kMaxB + b) * p.I + tile * r2 + tt], hv);
+        for (int i = lane; i < g.RS * NB; i += 32) {
+          const int rr = i / NB, b = i % NB;
+          if (bm & (1u << b)) __stcg(&p.h[h_index(l, a, b) + tile * g.RS + rr], m.res[i]);
         }
       });
       if (!st_ok) return;
@@ -1116,10 +1123,7 @@ struct Consumer {
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
           if (bm & (1u << b)) {
-            load8(p.h + (((size_t)l * kMaxActive + a) * kMaxB + b) * p.I + ks * 256 + lane * 8, act[b]);
-            const float wgt = m.rc_w[a][b];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) act[b][i] *= wgt;
+            load_h8(l, a, b, ks * 256 + lane * 8, m.rc_w[a][b], act[b]);
           } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) act[b][i] = 0.f;
@@ -1280,7 +1284,13 @@ struct Consumer {
       for (int i = 0; i < nu; ++i) {
         const QkvUnit q = qkv_unit(p, u0 + i);
         const uint8_t* ub = st + (size_t)i * 8 * p.H * 2;
-        if (q.kind == 2) {  // v: 8 rows = 8 consecutive elements of v head q.head
+        if (q.kind == 0) {  // q: 8 rows, stored before RoPE (attention rotates q when it loads it)
+          for (int tt = 0; tt < 8; ++tt, ++item) {
+            if (item % kConsumerWarps != warp) continue;
+            const float s = rdot(ub + (size_t)tt * p.H * 2, np, a);
+            if (lane == 0) __stcg(&p.q[((size_t)l * p.nq + q.head) * p.d + 4 * q.j + (tt & 3) + (tt >= 4 ? hd : 0)], s);
+          }
+        } else if (q.kind == 2) {  // v: 8 rows = 8 consecutive elements of v head q.head
           for (int tt = 0; tt < 8; ++tt, ++item) {
             if (item % kConsumerWarps != warp) continue;
             const float s = rdot(ub + (size_t)tt * p.H * 2, np, a);
@@ -1292,7 +1302,7 @@ struct Consumer {
                 p.vpool[((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d + e] = vb;
             }
           }
-        } else {  // q or k: RoPE pair (4 j + tt, 4 j + tt + d/2) from rows tt and tt + 4
+        } else {  // k: RoPE pair (4 j + tt, 4 j + tt + d/2) from rows tt and tt + 4, for the cache
           for (int tt = 0; tt < 4; ++tt, ++item) {
             if (item % kConsumerWarps != warp) continue;
             const float x0 = rdot(ub + (size_t)tt * p.H * 2, np, a);
@@ -1302,11 +1312,7 @@ struct Consumer {
               const float2 cs = m.st_rope[0][pi2];
               const float lo = x0 * cs.x - x1 * cs.y;
               const float hi = x0 * cs.y + x1 * cs.x;
-              if (q.kind == 0) {
-                float* dst = p.q + ((size_t)l * p.nq + q.head) * p.d;
-                __stcg(dst + pi2, lo);
-                __stcg(dst + pi2 + hd, hi);
-              } else {
+              {
                 const uint16_t kl = f2bf(lo), kh = f2bf(hi);
                 float* dst = p.knew + ((size_t)l * p.nkv + q.head) * p.d;
                 __stcg(dst + pi2, bf2f(kl));
@@ -1336,17 +1342,15 @@ struct Consumer {
     rows_act(a);
     const int na = m.rc_n, maxa = max_active(p);
     const Geo g = geo_of(p.H);
-    const int r2 = g.RS / 2, np = p.H / 256;
+    const int np = p.H / 256;
     for (int u = t.a; u < t.a + t.b; ++u) {
       const int ar = u % maxa, tile = u / maxa;
       if (ar >= na) continue;
       const uint8_t* st = acquire();
       if (!st) return;
-      for (int tt = warp; tt < r2; tt += kConsumerWarps) {
-        const float gt = rdot(st + (size_t)tt * p.H * 2, np, a);
-        const float up = rdot(st + (size_t)(r2 + tt) * p.H * 2, np, a);
-        if (lane == 0)
-          __stcg(&p.h[((size_t)l * kMaxActive + ar) * kMaxB * p.I + tile * r2 + tt], gt / (1.0f + expf(-gt)) * up);
+      for (int rr = warp; rr < g.RS; rr += kConsumerWarps) {
+        const float s = rdot(st + (size_t)rr * p.H * 2, np, a);
+        if (lane == 0) __stcg(&p.h[h_index(l, ar, 0) + tile * g.RS + rr], s);
       }
       release();
     }
@@ -1414,16 +1418,37 @@ struct Consumer {
     const float qscale = rsqrtf((float)p.d) * 1.4426950408889634f;  // scores in log2 units
     uint32_t qa[8][4];
     {
+      // q arrives before RoPE: element d pairs with d + d/2, which this lane also holds (k-step
+      // kk + ksteps/2), so the rotation happens here in registers
       const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + head) * p.d;
       const bool hv = head < p.group;
+      float x[8][4];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int d0 = kk * 16 + tig * 2;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[kk][e] = (kk < ksteps && hv) ? __ldcg(qh + d0 + (e & 1) + (e >> 1) * 8) : 0.f;
+      }
+      const int half = ksteps / 2, hd = p.d / 2;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        if (kk < half) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d0 = kk * 16 + tig * 2 + (e & 1) + (e >> 1) * 8;  // < d/2
+            const float2 cs = m.st_rope[b][d0];
+            const float lo = x[kk][e], hi = x[kk + half][e];
+            x[kk][e] = lo * cs.x - hi * cs.y;
+            x[kk + half][e] = lo * cs.y + hi * cs.x;
+          }
+        }
+      }
+      (void)hd;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         if (kk < ksteps) {
-          const int d0 = kk * 16 + tig * 2;
-          const float x0 = hv ? __ldcg(qh + d0) * qscale : 0.f, x1 = hv ? __ldcg(qh + d0 + 1) * qscale : 0.f;
-          const float x2 = hv ? __ldcg(qh + d0 + 8) * qscale : 0.f, x3 = hv ? __ldcg(qh + d0 + 9) * qscale : 0.f;
-          split_pack(x0, x1, qa[kk][0], qa[kk][1]);
-          split_pack(x2, x3, qa[kk][2], qa[kk][3]);
+          split_pack(x[kk][0] * qscale, x[kk][1] * qscale, qa[kk][0], qa[kk][1]);
+          split_pack(x[kk][2] * qscale, x[kk][3] * qscale, qa[kk][2], qa[kk][3]);
         }
       }
     }
@@ -1558,7 +1583,13 @@ struct Consumer {
       const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + warp) * p.d;
       const float* kn = p.knew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
       float s = 0.f;
-      for (int i = lane; i < p.d; i += 32) s = fmaf(__ldcg(qh + i), __ldcg(kn + i), s);
+      const int hd = p.d / 2;
+      for (int i = lane; i < hd; i += 32) {  // q before RoPE: rotate pair (i, i + d/2)
+        const float2 cs = m.st_rope[b][i];
+        const float q0 = __ldcg(qh + i), q1 = __ldcg(qh + i + hd);
+        s = fmaf(q0 * cs.x - q1 * cs.y, __ldcg(kn + i), s);
+        s = fmaf(q0 * cs.y + q1 * cs.x, __ldcg(kn + i + hd), s);
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       if (lane == 0) m.res[warp] = s * qscale;

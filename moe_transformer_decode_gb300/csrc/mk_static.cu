@@ -156,7 +156,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_we
   const size_t o_apart = cv.take<float>(L * B * nkv * P.max_chunks * (16 + 8 * d));
   const size_t o_attn_o = cv.take<float>(L * B * od), o_attn_out = cv.take<float>(L * B * H);
   const size_t o_rl = cv.take<float>(L * B * m.n_experts);
-  const size_t o_h = cv.take<float>(L * kMaxActive * kMaxB * (size_t)m.expert_inter);
+  const size_t o_h = cv.take<float>(L * kMaxActive * kMaxB * 2 * (size_t)m.expert_inter);
   const size_t o_moe = cv.take<float>(L * B * H), o_route = cv.take<Route>(L);
   const size_t o_lmv = cv.take<float>((size_t)ds.n_sm * kMaxB), o_lmi = cv.take<int32_t>((size_t)ds.n_sm * kMaxB);
   const size_t o_tki = cv.take<int32_t>(L * B * m.top_k), o_tkw = cv.take<float>(L * B * m.top_k);

@@ -7,6 +7,7 @@ agreement; KV append slot and page lookups bit-exact."""
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from harness import Setup, check_step
 from synth import workloads as W
@@ -39,7 +40,7 @@ def _run(w, steps, per_layer=False, mode=0):
             agree += a
             total += w.B
             if per_layer:
-                _check_layers(w, acts, tr)
+                _check_layers(w, acts, tr, pos)
             # the appended K/V sit at (block_table[b][pos / 16], pos % 16): the rest of those
             # pages, and a sample of other pages, are unchanged (bit-exact indexing); the values
             # match the oracle's within bf16 rounding
@@ -65,7 +66,7 @@ def _run(w, steps, per_layer=False, mode=0):
     assert agree >= 0.99 * total, f"greedy agreement {agree}/{total}"
 
 
-def _check_layers(w, acts, tr):
+def _check_layers(w, acts, tr, pos):
     x = acts["x"].cpu().numpy()
     for name, tol in (("x", 2e-4), ("attn_out", 2e-3), ("moe_out", 2e-3)):
         got = acts[name].cpu().numpy()
@@ -73,7 +74,11 @@ def _check_layers(w, acts, tr):
         scale = np.abs(ref).max()
         err = np.abs(got - ref).max()
         assert err <= tol * max(scale, 1e-6), f"{name}: max err {err:.3e} vs scale {scale:.3e}"
-    q = acts["q"].cpu().numpy()
+    q = acts["q"].cpu().numpy().astype(np.float64)  # before RoPE: rotate with the oracle's RoPE
+    for l in range(w.L):
+        for b in range(w.B):
+            for h in range(w.nq):
+                q[l, b, h] = oracle.rope(q[l, b, h], int(pos[b]), w.rope_theta)
     np.testing.assert_allclose(q, tr["q"], rtol=0, atol=2e-4 * np.abs(tr["q"]).max())
     att = acts["attn"].cpu().numpy()
     np.testing.assert_allclose(att, tr["attn"], rtol=0, atol=2e-3 * np.abs(tr["attn"]).max())
