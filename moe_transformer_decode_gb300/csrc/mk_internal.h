@@ -11,7 +11,14 @@
 namespace mk {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+// Two consumer warpgroups and one producer warpgroup (one thread of it issues the copies).
+// Whole warpgroups let the producer hand its registers to the consumers (setmaxnreg).
+constexpr int kThreads = (kConsumerWarps + 4) * 32;
+constexpr int kProducerRegs = 88;
+constexpr int kConsumerRegs = 208;
+static_assert(kConsumerWarps == 8, "two consumer warpgroups");
+static_assert(kProducerRegs * 128 + kConsumerRegs * 256 <= (65536 / kThreads) / 8 * 8 * kThreads,
+              "register split exceeds the launch's allotment");
 constexpr int kStageBytes = 32768;
 constexpr int kStages = 6;
 constexpr int kMaxB = 8;

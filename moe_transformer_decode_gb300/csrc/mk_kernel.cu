@@ -1715,31 +1715,34 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
   ring.it = 0;
   const int t0 = p.sm_begin[blockIdx.x], t1 = p.sm_begin[blockIdx.x + 1];
 
-  if (threadIdx.x / 32 == kConsumerWarps) {
-    if ((threadIdx.x & 31) != 0) return;
+  if (threadIdx.x / 32 >= kConsumerWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    if (threadIdx.x != kConsumerWarps * 32) return;
     Producer pr(p, tm, misc, ring);
-    // descriptors in batches of 8, the next batch loaded while the current one runs
+    // descriptors in batches of kPB, the next batch loaded while the current one runs
+    constexpr int kPB = 4;
     const uint4* src = reinterpret_cast<const uint4*>(p.tasks);
-    uint4 cur[8], nxt[8];
+    uint4 cur[kPB], nxt[kPB];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) cur[j] = t0 + j < t1 ? __ldg(src + t0 + j) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < kPB; ++j) cur[j] = t0 + j < t1 ? __ldg(src + t0 + j) : make_uint4(0, 0, 0, 0);
     bool fine = true;
-    for (int base = t0; base < t1 && fine; base += 8) {
+    for (int base = t0; base < t1 && fine; base += kPB) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) nxt[j] = base + 8 + j < t1 ? __ldg(src + base + 8 + j) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < kPB; ++j) nxt[j] = base + kPB + j < t1 ? __ldg(src + base + kPB + j) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kPB; ++j) {
         if (fine && base + j < t1) {
           const Task t = *reinterpret_cast<const Task*>(&cur[j]);
           fine = pr.run_task(t);
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+      for (int j = 0; j < kPB; ++j) cur[j] = nxt[j];
     }
     pr.drain();  // never leave while a copy into this CTA's shared memory is in flight
     return;
   }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
   Consumer<NB> c(p, misc, ring);
   if (!c.load_step_cache()) return;
   // descriptors in batches of 32 (lane j holds descriptor base + j), the next batch loaded
