@@ -58,18 +58,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// 1D bulk copy global -> shared, completion counted on an mbarrier (16-byte aligned, size % 16 == 0)
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-// 2D tiled tensor copy global -> shared (x: innermost coordinate in elements)
-__device__ __forceinline__ void tma_2d_g2s(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// 1D bulk copy global -> shared, completion counted on an mbarrier (16-byte aligned, size % 16 == 0),
+// with an L2 cache policy
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
       : "memory");
+}
+// 2D tiled tensor copy global -> shared (x: innermost coordinate in elements), with an L2 cache policy
+__device__ __forceinline__ void tma_2d_g2s(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+// L2 policy for data read once per step (weights, KV pages): evicted first, so that the code,
+// activations and counters the step keeps touching stay resident
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -200,6 +209,16 @@ __device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity) {
   }
 }
 
+// For the consumer warps' own barrier: re-test with the default short blocking wait instead of
+// a long suspend, so the warps resume as soon as the last one arrives.
+__device__ bool mbar_wait_cta(const Params& p, uint32_t bar, uint32_t parity) {
+  WaitClock wc;
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (!wc.keep_going(p, -1, (int)parity)) return false;
+  }
+}
+
 // ------------------------------------------------------------------ geometry
 
 // A GEMV stage is RS rows x KS columns (row-major bf16 in shared memory). Each consumer warp
@@ -267,12 +286,7 @@ struct Misc {
   alignas(16) float res[64 * kMaxB];             // reduced stage results [RS][B]
   float norm[kConsumerWarps][kMaxB]; // sum of squares partials
   int flag;
-  int n_active;
-  int route_expert[kMaxActive];
-  uint32_t route_mask[kMaxActive];
-  float route_w[kMaxActive][kMaxB];
-  uint32_t emask[kMaxExperts];
-  int erank[kMaxExperts];
+  // routing scratch of the warp that computes a layer's routing
   int ids[kMaxB][kMaxK];
   float wk[kMaxB][kMaxK];
   // per step (consumers): new token's position, page of its KV slot (-1 if invalid), RoPE at it,
@@ -319,9 +333,11 @@ struct Producer {
   uint32_t bar, dst;
   int pos[kMaxB], cpp[kMaxB], nch[kMaxB];  // per step
   int route_layer;
+  uint64_t pol;  // L2 policy of every copy
 
   __device__ Producer(const Params& p_, const TensorMaps& tm_, Misc& m_, Ring r_)
       : p(p_), tm(tm_), m(m_), r(r_), ok(true), route_layer(-1) {
+    pol = policy_evict_first();
     for (int b = 0; b < kMaxB; ++b) {
       pos[b] = b < p.B ? pos_of(p, b) : 0;
       cpp[b] = b < p.B ? p.chunk_pages[b] : 1;
@@ -355,7 +371,7 @@ struct Producer {
   __device__ bool gemv_rows(const uint16_t* base, int rows, int row_bytes) {
     const uint32_t bytes = (uint32_t)rows * row_bytes;
     if (!begin(bytes)) return false;
-    bulk_g2s(dst, base, bytes, bar);
+    bulk_g2s(dst, base, bytes, bar, pol);
     end();
     return true;
   }
@@ -382,10 +398,10 @@ struct Producer {
             const QkvUnit q = qkv_unit(p, u0 + i);
             const uint32_t d0 = dst + (uint32_t)i * 8 * p.H * 2;
             if (q.kind == 2) {
-              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 8 * p.H * 2, bar);
+              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 8 * p.H * 2, bar, pol);
             } else {
-              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 4 * p.H * 2, bar);
-              bulk_g2s(d0 + 4 * p.H * 2, W + (size_t)(q.row0 + p.d / 2) * p.H, 4 * p.H * 2, bar);
+              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 4 * p.H * 2, bar, pol);
+              bulk_g2s(d0 + 4 * p.H * 2, W + (size_t)(q.row0 + p.d / 2) * p.H, 4 * p.H * 2, bar, pol);
             }
           }
           end();
@@ -426,8 +442,8 @@ struct Producer {
               const int row = ((l * p.num_pages + id) * p.nkv + g) * kPage;
               const uint32_t pb = dst + (uint32_t)i * 4096 * halves;
               for (int h = 0; h < halves; ++h) {
-                tma_2d_g2s(pb + h * 2048, &tm.k, h * 64, row, bar);
-                tma_2d_g2s(pb + (halves + h) * 2048, &tm.v, h * 64, row, bar);
+                tma_2d_g2s(pb + h * 2048, &tm.k, h * 64, row, bar, pol);
+                tma_2d_g2s(pb + (halves + h) * 2048, &tm.v, h * 64, row, bar, pol);
               }
             }
             end();
@@ -445,7 +461,7 @@ struct Producer {
           const int e = m.pr_expert[a];
           const uint16_t* W = p.w_gate_up + ((size_t)l * p.E + e) * 2 * p.I * p.H;
           if (!begin((uint32_t)g.RS * p.H * 2)) return false;
-          bulk_g2s(dst, W + (size_t)tile * g.RS * p.H, (uint32_t)g.RS * p.H * 2, bar);
+          bulk_g2s(dst, W + (size_t)tile * g.RS * p.H, (uint32_t)g.RS * p.H * 2, bar, pol);
           end();
         }
         return true;
@@ -459,7 +475,7 @@ struct Producer {
           } else {
             if (!begin((uint32_t)t.b * g.KS * 2)) return false;
             for (int r = 0; r < t.b; ++r)
-              bulk_g2s(dst + (uint32_t)r * g.KS * 2, W + (size_t)r * p.od + cs * g.KS, g.KS * 2, bar);
+              bulk_g2s(dst + (uint32_t)r * g.KS * 2, W + (size_t)r * p.od + cs * g.KS, g.KS * 2, bar, pol);
             end();
           }
         }
@@ -687,7 +703,7 @@ struct Consumer {
   __device__ bool csync() {
     __syncwarp();
     if (lane == 0) mbar_arrive(cbar);
-    const bool done = mbar_wait(p, cbar, cphase);
+    const bool done = mbar_wait_cta(p, cbar, cphase);
     cphase ^= 1u;
     if (!done) ok = false;
     return done;
@@ -893,31 +909,48 @@ struct Consumer {
       });
       if (!st_ok) return;
     }
-    if (!arrive_last(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) return;
-    compute_routing(l);
-    if (ok) release_counter(cm.route(l));
+    if (arrive_last_w0(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) publish_routing(l);
   }
 
-  // top-k per token (value descending, lower expert id first on ties), softmax over the k
-  // selected logits, then the distinct routed experts in ascending id with token masks.
-  __device__ void compute_routing(int l) {
-    for (int e = threadIdx.x; e < p.E; e += 256) m.emask[e] = 0u;
-    if (warp < p.B) {
-      const int b = warp;
-      float v[kMaxExperts / 32];
+  // Arrival on `idx` once every consumer warp's writes are done; true in warp 0 of the task
+  // that arrived last (the other warps get false and go on to their next task).
+  __device__ bool arrive_last_w0(int idx, int count) {
+    if (!csync()) return false;
+    if (warp != 0) return false;
+    uint32_t last = 0;
+    if (lane == 0) last = ((atom_acq_rel_add(p.counters + idx, 1u) + 1u) % (uint32_t)count) == 0u;
+    return __shfl_sync(0xffffffffu, last, 0) != 0u;
+  }
+
+  // Routing of layer l by warp 0 alone, then published with one release of the route counter.
+  // Per token: top-k (value descending, lower expert id first on ties), softmax over the k
+  // selected logits. Then the distinct routed experts in ascending id, each with its token
+  // mask and per-token weights. Lane owns experts lane + 32 i.
+  __device__ void publish_routing(int l) {
+    constexpr int NE = kMaxExperts / 32;
+    const int E = p.E, K = p.topk, B = p.B;
+    float v[NB][NE];
 #pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int i = 0; i < NE; ++i) {
         const int e = lane + 32 * i;
-        v[i] = e < p.E ? __ldcg(&p.rlogits[((size_t)l * p.B + b) * p.E + e]) : -INFINITY;
+        v[b][i] = (b < B && e < E) ? __ldcg(&p.rlogits[((size_t)l * B + b) * E + e]) : -INFINITY;
       }
-      float sel[kMaxK];
-      for (int j = 0; j < p.topk; ++j) {
+    uint32_t emask[NE];
+#pragma unroll
+    for (int i = 0; i < NE; ++i) emask[i] = 0u;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (b >= B) break;
+      float top0 = 0.f, z = 0.f;
+      for (int j = 0; j < K; ++j) {
         float bv = -INFINITY;
         int be = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
+        for (int i = 0; i < NE; ++i) {
           const int e = lane + 32 * i;
-          if (e < p.E && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
+          if (e < E && (v[b][i] > bv || (v[b][i] == bv && e < be))) { bv = v[b][i]; be = e; }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -926,66 +959,46 @@ struct Consumer {
           if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
         }
 #pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i)
-          if (lane + 32 * i == be) v[i] = -INFINITY;
-        sel[j] = bv;
-        if (lane == 0) m.ids[b][j] = be;
+        for (int i = 0; i < NE; ++i)
+          if (lane + 32 * i == be) { v[b][i] = -INFINITY; emask[i] |= 1u << b; }
+        if (j == 0) top0 = bv;
+        const float w = expf(bv - top0);
+        z += w;
+        if (lane == 0) { m.ids[b][j] = be; m.wk[b][j] = w; }
       }
-      if (lane == 0) {
-        float z = 0.f, w[kMaxK];
-        for (int j = 0; j < p.topk; ++j) { w[j] = expf(sel[j] - sel[0]); z += w[j]; }
-        for (int j = 0; j < p.topk; ++j) m.wk[b][j] = w[j] / z;
-      }
+      __syncwarp();
+      if (lane < K) m.wk[b][lane] /= z;
     }
-    if (!csync()) return;
-    for (int i = threadIdx.x; i < p.B * p.topk; i += 256) atomicOr(&m.emask[m.ids[i / p.topk][i % p.topk]], 1u << (i / p.topk));
-    if (!csync()) return;
-    if (warp == 0) {  // compact: lane owns experts [8 lane, 8 lane + 8)
-      int cnt = 0;
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane * 8 + i;
-        cnt += (e < p.E && m.emask[e] != 0u);
-      }
-      int incl = cnt;
+    __syncwarp();
+    Route* rt = p.route + l;
+    int na = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int pos = incl - cnt;
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane * 8 + i;
-        if (e < p.E && m.emask[e] != 0u) {
-          m.erank[e] = pos;
-          m.route_expert[pos] = e;
-          m.route_mask[pos] = m.emask[e];
-          ++pos;
+    for (int i = 0; i < NE; ++i) {
+      const uint32_t act = __ballot_sync(0xffffffffu, emask[i] != 0u);
+      if (emask[i] != 0u) {
+        const int e = lane + 32 * i;
+        const int r = na + __popc(act & ((1u << lane) - 1u));
+        __stcg(&rt->expert[r], e);
+        __stcg(&rt->mask[r], emask[i]);
+        for (int b = 0; b < kMaxB; ++b) {
+          float w = 0.f;
+          if (emask[i] & (1u << b))
+            for (int j = 0; j < K; ++j) w = m.ids[b][j] == e ? m.wk[b][j] : w;
+          __stcg(&rt->w[r][b], w);
         }
       }
-      if (lane == 31) m.n_active = incl;
+      na += __popc(act);
     }
-    for (int i = threadIdx.x; i < kMaxActive * kMaxB; i += 256) (&m.route_w[0][0])[i] = 0.f;
-    if (!csync()) return;
-    for (int i = threadIdx.x; i < p.B * p.topk; i += 256) {
-      const int b = i / p.topk, j = i % p.topk;
-      m.route_w[m.erank[m.ids[b][j]]][b] = m.wk[b][j];
-    }
-    if (!csync()) return;
-    Route* rt = p.route + l;
-    const int na = m.n_active;
-    if (threadIdx.x == 0) __stcg(&rt->n_active, na);
-    for (int i = threadIdx.x; i < na; i += 256) {
-      __stcg(&rt->expert[i], m.route_expert[i]);
-      __stcg(&rt->mask[i], m.route_mask[i]);
-    }
-    for (int i = threadIdx.x; i < na * kMaxB; i += 256) __stcg(&rt->w[i / kMaxB][i % kMaxB], m.route_w[i / kMaxB][i % kMaxB]);
-    for (int i = threadIdx.x; i < p.B * p.topk; i += 256) {
-      const int b = i / p.topk, j = i % p.topk;
+    if (lane == 0) __stcg(&rt->n_active, na);
+    for (int i = lane; i < B * K; i += 32) {
+      const int b = i / K, j = i % K;
       __stcg(&rt->ids[b][j], m.ids[b][j]);
       __stcg(&rt->wk[b][j], m.wk[b][j]);
-      __stcg(&p.topk_ids[((size_t)l * p.B + b) * p.topk + j], m.ids[b][j]);
-      __stcg(&p.topk_w[((size_t)l * p.B + b) * p.topk + j], m.wk[b][j]);
+      __stcg(&p.topk_ids[((size_t)l * B + b) * K + j], m.ids[b][j]);
+      __stcg(&p.topk_w[((size_t)l * B + b) * K + j], m.wk[b][j]);
     }
+    __syncwarp();
+    if (lane == 0) red_release_add(p.counters + cm.route(l), 1u);
   }
 
   __device__ void op_qkv(const Task& t) {
@@ -1261,9 +1274,7 @@ struct Consumer {
       }
       release();
     }
-    if (!arrive_last(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) return;
-    compute_routing(l);
-    if (ok) release_counter(cm.route(l));
+    if (arrive_last_w0(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) publish_routing(l);
   }
 
   __device__ void op_qkv_r(const Task& t) {
@@ -1719,25 +1730,20 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (threadIdx.x != kConsumerWarps * 32) return;
     Producer pr(p, tm, misc, ring);
-    // descriptors in batches of kPB, the next batch loaded while the current one runs
-    constexpr int kPB = 4;
+    // descriptors in a 4-deep register queue, refilled as tasks are taken (one call site, so
+    // the task code is inlined once)
     const uint4* src = reinterpret_cast<const uint4*>(p.tasks);
-    uint4 cur[kPB], nxt[kPB];
-#pragma unroll
-    for (int j = 0; j < kPB; ++j) cur[j] = t0 + j < t1 ? __ldg(src + t0 + j) : make_uint4(0, 0, 0, 0);
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    uint4 q0 = t0 < t1 ? __ldg(src + t0) : zero, q1 = t0 + 1 < t1 ? __ldg(src + t0 + 1) : zero;
+    uint4 q2 = t0 + 2 < t1 ? __ldg(src + t0 + 2) : zero, q3 = t0 + 3 < t1 ? __ldg(src + t0 + 3) : zero;
     bool fine = true;
-    for (int base = t0; base < t1 && fine; base += kPB) {
-#pragma unroll
-      for (int j = 0; j < kPB; ++j) nxt[j] = base + kPB + j < t1 ? __ldg(src + base + kPB + j) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int j = 0; j < kPB; ++j) {
-        if (fine && base + j < t1) {
-          const Task t = *reinterpret_cast<const Task*>(&cur[j]);
-          fine = pr.run_task(t);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kPB; ++j) cur[j] = nxt[j];
+    for (int i = t0; i < t1 && fine; ++i) {
+      const uint4 nx = i + 4 < t1 ? __ldg(src + i + 4) : zero;
+      fine = pr.run_task(*reinterpret_cast<const Task*>(&q0));
+      q0 = q1;
+      q1 = q2;
+      q2 = q3;
+      q3 = nx;
     }
     pr.drain();  // never leave while a copy into this CTA's shared memory is in flight
     return;
