@@ -169,9 +169,12 @@ mk_status mk_get_activations(const mk_ctx* ctx, mk_activations* out);
  * grouped by SM) when tasks_cap >= info->n_tasks, else returns MK_ERR_INVALID_ARG; if
  * sm_begin is non-NULL, writes the n_sm + 1 list offsets; if sm_bytes is non-NULL, the
  * planned bytes per SM. Opcodes: 1 router, 2 QKV, 3 attention, 4 expert gate/up, 5 O-proj,
- * 6 expert down, 7 LM head. Errors: MK_ERR_INVALID_ARG. */
+ * 6 expert down, 7 LM head. The two branches of each layer run on disjoint SM partitions:
+ * SMs [0, n_attn_sm) take QKV, attention and O-proj, the others router, gate/up and down
+ * (n_attn_sm == n_sm: every SM takes both, as for very small n_sm). The LM head spreads over
+ * all SMs. Errors: MK_ERR_INVALID_ARG. */
 typedef struct {
-  int32_t n_tasks, n_counters, max_chunks, n_lm_sm, n_op_launches;
+  int32_t n_tasks, n_counters, max_chunks, n_lm_sm, n_op_launches, n_attn_sm;
 } mk_plan_info;
 mk_status mk_plan_schedule(const mk_model_cfg* cfg, int32_t n_sm, int32_t batch, const int32_t* seq_lens,
                            mk_plan_info* info, void* tasks, int32_t tasks_cap, int32_t* sm_begin, int64_t* sm_bytes);

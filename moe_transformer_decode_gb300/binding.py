@@ -45,7 +45,8 @@ class mk_activations(ctypes.Structure):
 
 
 class mk_plan_info(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("n_tasks", "n_counters", "max_chunks", "n_lm_sm", "n_op_launches")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("n_tasks", "n_counters", "max_chunks", "n_lm_sm", "n_op_launches",
+                                                       "n_attn_sm")]
 
 
 class mk_trace_entry(ctypes.Structure):

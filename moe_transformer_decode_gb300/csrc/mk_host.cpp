@@ -42,7 +42,8 @@ struct mk_ctx {
   int mode;
   std::string err;
   // workspace (device)
-  float *xs, *q, *knew, *vnew, *attn_o, *attn_out, *rlogits, *h, *moe_out, *apart, *lm_best_v;
+  float *xs, *q, *knew, *vnew, *attn_o, *attn_out, *rlogits, *moe_out, *apart, *lm_best_v;
+  uint16_t *attn_hl, *h;
   int32_t* lm_best_i;
   int32_t* topk_ids;
   float* topk_w;
@@ -115,7 +116,7 @@ extern "C" void mk_destroy(mk_ctx* c) {
   if (!c) return;
   free_schedule(c);
   cudaFree(c->xs); cudaFree(c->q); cudaFree(c->knew); cudaFree(c->vnew); cudaFree(c->attn_o); cudaFree(c->attn_out);
-  cudaFree(c->rlogits); cudaFree(c->h); cudaFree(c->moe_out); cudaFree(c->lm_best_v); cudaFree(c->lm_best_i);
+  cudaFree(c->rlogits); cudaFree(c->h); cudaFree(c->attn_hl); cudaFree(c->moe_out); cudaFree(c->lm_best_v); cudaFree(c->lm_best_i);
   cudaFree(c->route); cudaFree(c->rope); cudaFree(c->status); cudaFree(c->topk_ids); cudaFree(c->topk_w);
   if (c->status_host) cudaFreeHost(c->status_host);
   delete c;
@@ -185,10 +186,10 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
   c->max_pos = m.max_pages_per_seq * kPage;
   bool okm = dalloc(&c->xs, (L + 1) * Bm * H) == cudaSuccess && dalloc(&c->q, L * Bm * m.n_q_heads * d) == cudaSuccess &&
              dalloc(&c->knew, L * Bm * m.n_kv_heads * d) == cudaSuccess &&
-             dalloc(&c->vnew, L * Bm * m.n_kv_heads * d) == cudaSuccess && dalloc(&c->attn_o, L * Bm * od) == cudaSuccess &&
+             dalloc(&c->vnew, L * Bm * m.n_kv_heads * d) == cudaSuccess && dalloc(&c->attn_o, L * Bm * od) == cudaSuccess && dalloc(&c->attn_hl, L * 2 * Bm * od) == cudaSuccess &&
              dalloc(&c->attn_out, L * Bm * H) == cudaSuccess && dalloc(&c->moe_out, L * Bm * H) == cudaSuccess &&
              dalloc(&c->rlogits, L * Bm * m.n_experts) == cudaSuccess &&
-             dalloc(&c->h, L * kMaxActive * kMaxB * 2 * (size_t)m.expert_inter) == cudaSuccess &&
+             dalloc(&c->h, L * kMaxActive * 2 * kMaxB * (size_t)m.expert_inter) == cudaSuccess &&
              dalloc(&c->route, L) == cudaSuccess && dalloc(&c->lm_best_v, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
              dalloc(&c->lm_best_i, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
              dalloc(&c->rope, (size_t)c->max_pos * (d / 2)) == cudaSuccess && dalloc(&c->status, ST_WORDS) == cudaSuccess &&
@@ -256,24 +257,45 @@ Geo geo_of(int K) {
   return g;
 }
 
-// Least-loaded assignment. Loads are counted per layer (new_layer() restarts them), so each
-// layer's work, phase by phase, is spread evenly; ties go to the SM with the least bytes over
-// the whole step (`total`), so no SM takes the extra task in every layer.
+// Least-loaded assignment within a partition of the SMs. Loads are counted per layer
+// (new_layer() restarts them), so each layer's work, phase by phase, is spread evenly over the
+// partition; ties go to the SM with the least bytes over the whole step (`total`), so no SM
+// takes the extra task in every layer.
 struct Assigner {
   int n_sm;
+  std::vector<int> part;  // partition of each SM
   std::vector<long long> load, total;
   std::vector<std::vector<Task>> lists;
   typedef std::tuple<long long, long long, int> Key;
-  std::priority_queue<Key, std::vector<Key>, std::greater<>> heap;
-  explicit Assigner(int n) : n_sm(n), load(n, 0), total(n, 0), lists(n) { new_layer(); }
+  std::vector<std::priority_queue<Key, std::vector<Key>, std::greater<>>> heaps;
+  Assigner(int n, std::vector<int> part_, int n_parts)
+      : n_sm(n), part(std::move(part_)), load(n, 0), total(n, 0), lists(n), heaps(n_parts) {
+    new_layer();
+  }
   void new_layer() {
-    heap = decltype(heap)();
+    for (auto& h : heaps) h = std::priority_queue<Key, std::vector<Key>, std::greater<>>();
     for (int s = 0; s < n_sm; ++s) {
       load[s] = 0;
-      heap.push(Key(0, total[s], s));
+      heaps[part[s]].push(Key(0, total[s], s));
     }
   }
-  int put(const Task& t, long long bytes) {
+  // onto SM s (kept in s's heap position)
+  void put_on(const Task& t, long long bytes, int s) {
+    lists[s].push_back(t);
+    load[s] += bytes;
+    total[s] += bytes;
+    auto& heap = heaps[part[s]];
+    std::vector<Key> keep;
+    while (!heap.empty()) {
+      Key k = heap.top();
+      heap.pop();
+      if (std::get<2>(k) == s) k = Key(load[s], total[s], s);
+      keep.push_back(k);
+    }
+    for (auto& k : keep) heap.push(k);
+  }
+  int put(const Task& t, long long bytes, int pt) {
+    auto& heap = heaps[pt];
     const int s = std::get<2>(heap.top());
     heap.pop();
     lists[s].push_back(t);
@@ -304,19 +326,40 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   const int L = m.n_layers, H = m.hidden, d = m.head_dim, nkv = m.n_kv_heads, G = m.n_q_heads / nkv;
   const int E = m.n_experts, I = m.expert_inter, V = m.vocab, od = m.n_q_heads * d;
   const Geo gh = geo_of(H), go = geo_of(od), gi = geo_of(I);
-  const int pps = kStageBytes / (4096 * (d / 64));
+  const int pps = kStagePayload / (4096 * (d / 64));
   CounterMap cmap{L, nkv, B};
   std::vector<int32_t>& cnt = P.cnt;
   cnt.assign(cmap.count(), 0);
 
-  // attention chunks: about one (sequence, group, chunk) task per SM, whole stages each
   long long group_pages = 0;
   std::vector<int> npg(B);
   for (int b = 0; b < B; ++b) {
     npg[b] = (seq_lens[b] + kPage - 1) / kPage;
     group_pages += (long long)npg[b] * nkv;
   }
-  int cp = (int)((group_pages + n_sm - 1) / n_sm);
+  const int maxa = std::min(B * m.top_k, E);
+  // expected live fraction of the planned expert slots (1 at batch 1)
+  const double live = maxa == m.top_k ? 1.0 : std::min(1.0, (double)E * (1.0 - std::pow(1.0 - (double)m.top_k / E, B)) / maxa);
+
+  // The two branches of a layer (attention: QKV, attention, O-proj; experts: router, gate/up,
+  // down) only meet at the residual, so they run on disjoint SM partitions sized by their bytes
+  // per layer: neither branch's tasks queue behind the other's on an SM.
+  const double attn_bytes = (double)(m.n_q_heads + 2 * nkv) * d * H * 2 + (double)H * od * 2 +
+                            (double)group_pages * 2 * kPage * d * 2;
+  const double moe_bytes = (double)E * H * 2 + live * maxa * 3.0 * I * H * 2;
+  int n_attn = n_sm;  // too few SMs to split: every SM takes both branches
+  if (n_sm >= 8) {
+    n_attn = (int)std::lround(n_sm * attn_bytes / (attn_bytes + moe_bytes));
+    n_attn = std::min(std::max(n_attn, 1), n_sm - 1);
+  }
+  std::vector<int> part(n_sm, 0);
+  for (int s = n_attn; s < n_sm; ++s) part[s] = 1;
+  const int PA = 0, PM = n_attn < n_sm ? 1 : 0;
+  const int n_moe = n_attn < n_sm ? n_sm - n_attn : n_sm;
+  P.n_attn_sm = n_attn;
+
+  // attention chunks: about one (sequence, group, chunk) task per attention SM, whole stages each
+  int cp = (int)((group_pages + n_attn - 1) / n_attn);
   cp = std::max(cp, pps);
   cp = (cp + pps - 1) / pps * pps;
   P.chunk_pages.assign(B, cp);
@@ -327,21 +370,19 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     P.max_chunks = std::max(P.max_chunks, P.n_chunks[b]);
   }
 
-  const int maxa = std::min(B * m.top_k, E);
   const int tiles = 2 * I / gh.RS;  // gate/up tiles: RS consecutive rows of [gate; up]
-  // about two QKV and two expert gate/up tasks per SM and layer (whole stages each)
+  // about two QKV tasks per attention SM and two expert gate/up tasks per expert SM, per layer
+  // (whole stages each)
   const int upg_ = (G + 2) * (d / 8);
-  int qkv_per_task = std::max(1, (int)std::lround((double)nkv * upg_ / (2.0 * n_sm)));
+  int qkv_per_task = std::max(1, (int)std::lround((double)nkv * upg_ / (2.0 * n_attn)));
   qkv_per_task = std::max(gh.RG, (qkv_per_task + gh.RG - 1) / gh.RG * gh.RG);
-  const int gu_per_task = std::max(1, (int)std::lround((double)maxa * tiles / (2.0 * n_sm)));
+  const int gu_per_task = std::max(1, (int)std::lround((double)maxa * tiles / (2.0 * n_moe)));
   const long long row_h = 2LL * H;
-  // expected live fraction of the planned expert slots (1 at batch 1)
-  const double live = maxa == m.top_k ? 1.0 : std::min(1.0, (double)E * (1.0 - std::pow(1.0 - (double)m.top_k / E, B)) / maxa);
 
-  Assigner as(n_sm);
+  Assigner as(n_sm, part, PM + 1);
   std::vector<std::vector<std::vector<Task>>> per_op;  // [launch][sm] tasks for the per-op mode
-  auto emit = [&](std::vector<std::pair<Task, long long>>& ts) {
-    for (auto& x : ts) as.put(x.first, x.second);
+  auto emit = [&](std::vector<std::pair<Task, long long>>& ts, int pt) {
+    for (auto& x : ts) as.put(x.first, x.second, pt);
     std::vector<std::vector<Task>> lists(n_sm);
     for (size_t i = 0; i < ts.size(); ++i) lists[i % n_sm].push_back(ts[i].first);
     if (!ts.empty()) per_op.push_back(std::move(lists));
@@ -363,7 +404,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
                     std::min(gh.RS, E - r0) * row_h});
     cnt[cmap.router_arrive(l)] = n_router;
     cnt[cmap.route(l)] = 1;
-    emit(ts);
+    emit(ts, PM);
     // QKV units, group-major, a few stages per task
     const int upg = (G + 2) * (d / 8);
     for (int g = 0; g < nkv; ++g) {
@@ -373,7 +414,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
                       std::min(qkv_per_task, (g + 1) * upg - u) * 8 * row_h});
       cnt[cmap.qkv(l, g)] = n;
     }
-    emit(ts);
+    emit(ts, PA);
     // expert gate/up: units u = tile * maxa + active_rank
     int n_gu = 0;
     for (int u = 0; u < maxa * tiles; u += gu_per_task, ++n_gu) {
@@ -381,27 +422,34 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
       ts.push_back({mkt(OP_GU, l, u, n, 0), (long long)(n * live * gh.RS * row_h)});
     }
     cnt[cmap.gu(l)] = n_gu;
-    emit(ts);
-    // attention chunks
-    for (int b = 0; b < B; ++b)
-      for (int g = 0; g < nkv; ++g)
-        for (int ch = 0; ch < P.n_chunks[b]; ++ch) {
-          const int p0 = ch * cp, p1 = (ch == P.n_chunks[b] - 1) ? npg[b] : std::min(npg[b], p0 + cp);
-          ts.push_back({mkt(OP_ATTN, l, b, g, ch), std::max(0, p1 - p0) * 2LL * kPage * d * 2});
-        }
+    emit(ts, PM);
+    // attention chunks: task i of every layer on the same attention SM (i mod n_attn), which then
+    // reads the same pages, so their ids stay cached there
+    {
+      int i = 0;
+      std::vector<std::vector<Task>> lists(n_sm);
+      for (int b = 0; b < B; ++b)
+        for (int g = 0; g < nkv; ++g)
+          for (int ch = 0; ch < P.n_chunks[b]; ++ch, ++i) {
+            const int p0 = ch * cp, p1 = (ch == P.n_chunks[b] - 1) ? npg[b] : std::min(npg[b], p0 + cp);
+            const Task t = mkt(OP_ATTN, l, b, g, ch);
+            as.put_on(t, std::max(0, p1 - p0) * 2LL * kPage * d * 2, i % n_attn);
+            lists[i % n_sm].push_back(t);
+          }
+      per_op.push_back(std::move(lists));
+    }
     for (int g = 0; g < nkv; ++g) cnt[cmap.attn(l, g)] = B;
-    emit(ts);
     // expert down rows over all active experts
     int n_down = 0;
     for (int r0 = 0; r0 < H; r0 += gi.RS, ++n_down)
       ts.push_back({mkt(OP_DOWN, l, r0, std::min(gi.RS, H - r0), 0),
                     (long long)(std::min(gi.RS, H - r0) * 2.0 * I * maxa * live)});
-    emit(ts);
+    emit(ts, PM);
     // O-proj rows
     int n_o = 0;
     for (int r0 = 0; r0 < H; r0 += go.RS, ++n_o)
       ts.push_back({mkt(OP_O, l, r0, std::min(go.RS, H - r0), 0), std::min(go.RS, H - r0) * 2LL * od});
-    emit(ts);
+    emit(ts, PA);
     cnt[cmap.layer(l)] = n_o + n_down;
   }
   as.new_layer();
@@ -464,6 +512,7 @@ extern "C" mk_status mk_plan_schedule(const mk_model_cfg* cfg, int32_t n_sm, int
   info->n_counters = (int32_t)P.cnt.size();
   info->max_chunks = P.max_chunks;
   info->n_lm_sm = P.n_lm_sm;
+  info->n_attn_sm = P.n_attn_sm;
   info->n_op_launches = P.n_op_launches;
   if (tasks) {
     if (tasks_cap < P.n_tasks) return MK_ERR_INVALID_ARG;
@@ -562,7 +611,7 @@ static Params make_params(mk_ctx* c, const int32_t* tokens, const int32_t* posit
   p.tasks = c->d_tasks; p.sm_begin = c->d_sm_begin; p.cnt_per_step = c->d_cnt;
   p.chunk_pages = c->d_chunk_pages; p.n_chunks = c->d_n_chunks;
   p.xs = c->xs; p.q = c->q; p.knew = c->knew; p.vnew = c->vnew; p.apart = c->apart; p.attn_o = c->attn_o;
-  p.attn_out = c->attn_out; p.rlogits = c->rlogits; p.h = c->h; p.moe_out = c->moe_out; p.route = c->route;
+  p.attn_out = c->attn_out; p.rlogits = c->rlogits; p.h = c->h; p.attn_hl = c->attn_hl; p.moe_out = c->moe_out; p.route = c->route;
   p.lm_best_v = c->lm_best_v; p.lm_best_i = c->lm_best_i; p.counters = c->counters; p.status = c->status;
   p.status_host = c->status_host_dev; p.topk_ids = c->topk_ids; p.topk_w = c->topk_w;
   p.trace = c->trace; p.trace_count = c->trace_count; p.trace_cap = c->trace_cap;

@@ -14,12 +14,13 @@ constexpr int kConsumerWarps = 8;
 // Two consumer warpgroups and one producer warpgroup (one thread of it issues the copies).
 // Whole warpgroups let the producer hand its registers to the consumers (setmaxnreg).
 constexpr int kThreads = (kConsumerWarps + 4) * 32;
-constexpr int kProducerRegs = 88;
-constexpr int kConsumerRegs = 208;
+constexpr int kProducerRegs = 56;
+constexpr int kConsumerRegs = 224;
 static_assert(kConsumerWarps == 8, "two consumer warpgroups");
 static_assert(kProducerRegs * 128 + kConsumerRegs * 256 <= (65536 / kThreads) / 8 * 8 * kThreads,
               "register split exceeds the launch's allotment");
-constexpr int kStageBytes = 32768;
+constexpr int kStagePayload = 32768;                 // data bytes of a ring stage
+constexpr int kStageBytes = kStagePayload + 64 * 16;  // slot: GEMV rows (at most 64) are padded by 16 bytes
 constexpr int kStages = 6;
 constexpr int kMaxB = 8;
 constexpr int kMaxK = 8;
@@ -104,7 +105,11 @@ struct Params {
   const int32_t* chunk_pages;  // [B] pages per attention chunk
   const int32_t* n_chunks;     // [B]
   // workspace
-  float *xs, *q, *knew, *vnew, *apart, *attn_o, *attn_out, *rlogits, *h, *moe_out;
+  float *xs, *q, *knew, *vnew, *apart, *attn_o, *attn_out, *rlogits, *moe_out;
+  // activations stored as bf16 hi/lo planes (hi = bf16(v), lo = bf16(v - hi)), the form the
+  // tensor-core GEMV consumes: attention output [L][2][B][n_q d]; expert activations
+  // SiLU(gate) * up * routing weight [L][max active][2][max batch][I]
+  uint16_t *attn_hl, *h;
   Route* route;
   float* lm_best_v;
   int32_t* lm_best_i;
@@ -126,6 +131,7 @@ struct Plan {
   std::vector<int32_t> chunk_pages, n_chunks;
   std::vector<long long> load;    // planned bytes per SM (megakernel lists)
   int max_chunks = 1, n_lm_sm = 0, n_tasks = 0, n_op_launches = 0;
+  int n_attn_sm = 0;               // SMs [0, n_attn_sm) take the attention branch, the rest the experts
 };
 mk_status plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_t* seq_lens, Plan& P);
 

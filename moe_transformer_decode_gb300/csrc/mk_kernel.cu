@@ -221,10 +221,11 @@ __device__ bool mbar_wait_cta(const Params& p, uint32_t bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ geometry
 
-// A GEMV stage is RS rows x KS columns (row-major bf16 in shared memory). Each consumer warp
-// owns 8 rows ("row group") and a 256-column slice; a lane owns 8 consecutive columns.
+// A GEMV stage is RS rows x KS columns: bf16 rows in shared memory RST bytes apart (16 bytes of
+// padding per row, so the 8 row addresses of an ldmatrix fall in distinct banks). Each consumer
+// warp owns 8 rows ("row group") and a 256-column slice (16 mma k-steps).
 struct Geo {
-  int KS, KW, RG, RS, NCS;
+  int KS, KW, RG, RS, NCS, RST;
 };
 __device__ __forceinline__ Geo geo_of(int K) {
   Geo g;
@@ -233,6 +234,7 @@ __device__ __forceinline__ Geo geo_of(int K) {
   g.RG = kConsumerWarps / g.KW;
   g.RS = 8 * g.RG;
   g.NCS = K / g.KS;
+  g.RST = g.KS * 2 + 16;
   return g;
 }
 
@@ -272,21 +274,32 @@ __device__ __forceinline__ AttnRange attn_range(int pos, int cpp, int nch, int c
   r.pos_end = pos;
   return r;
 }
-__device__ __forceinline__ int attn_pps(const Params& p) { return kStageBytes / (4096 * (p.d / 64)); }
+__device__ __forceinline__ int attn_pps(const Params& p) { return kStagePayload / (4096 * (p.d / 64)); }
 
 __device__ __forceinline__ int max_active(const Params& p) { return min(p.B * p.topk, p.E); }
 
 // ------------------------------------------------------------------ shared memory
 
+constexpr int kRedBufs = 4;    // GEMV partial-sum buffers in flight
+constexpr int kIdCache = 256;  // page ids the producer keeps (the same pages serve every layer)
+
 struct Misc {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t cbar;                     // consumer-warps barrier (8 arrivals per phase)
-  alignas(16) float red[2][kConsumerWarps][64];  // cross-warp partial sums, double-buffered by stage
-  alignas(16) float res[64 * kMaxB];             // reduced stage results [RS][B]
+  uint64_t gpart[kRedBufs];          // GEMV pass buffers: every consumer warp's partials are in
+  uint64_t gfree[kRedBufs];          // ... and: the pass's epilogue warp has read them
+  union {
+    // GEMV partial sums [buffer][warp][row * 8 + token]; also scratch of the attention combine
+    alignas(16) float red[kRedBufs][kConsumerWarps][64];
+    // per-warp exchange area (256 floats each) for building the norm input's mma fragments; used
+    // only between the norm load's block barriers, when no GEMV pass is in flight
+    alignas(16) float nsm[kConsumerWarps * 256];
+  };
   float norm[kConsumerWarps][kMaxB]; // sum of squares partials
   int flag;
   // routing scratch of the warp that computes a layer's routing
+  uint32_t em[kMaxExperts];  // bit b: token b picked the expert
   int ids[kMaxB][kMaxK];
   float wk[kMaxB][kMaxK];
   // per step (consumers): new token's position, page of its KV slot (-1 if invalid), RoPE at it,
@@ -301,17 +314,17 @@ struct Misc {
   int rc_expert[kMaxActive];
   uint32_t rc_mask[kMaxActive];
   float rc_w[kMaxActive][kMaxB];
-  // producer-private: routed experts of layer pr_layer
+  // producer-private: routed experts of layer pr_layer, and a window of one sequence's page ids
   int pr_n;
   int pr_expert[kMaxActive];
-  // batch 1: the normalized input of the current layer, and per-warp LM argmax candidates
-  alignas(16) float nsm[2048];
-  float lmw_v[kConsumerWarps];
-  int lmw_i[kConsumerWarps];
+  int pr_ids[kIdCache];
+  // per-warp LM argmax candidates per token
+  float lmw_v[kConsumerWarps][kMaxB];
+  int lmw_i[kConsumerWarps][kMaxB];
 };
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + ((int)sizeof(Misc) + 127) / 128 * 128;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds the sm_103a opt-in limit");
-static_assert(offsetof(Misc, red) % 16 == 0 && offsetof(Misc, res) % 16 == 0 && offsetof(Misc, st_rope) % 16 == 0 &&
+static_assert(offsetof(Misc, red) % 16 == 0 && offsetof(Misc, st_rope) % 16 == 0 &&
                   offsetof(Misc, nsm) % 16 == 0,
               "vector-accessed shared arrays must be 16-byte aligned");
 
@@ -329,15 +342,18 @@ struct Producer {
   const TensorMaps& tm;
   Misc& m;
   Ring r;
-  bool ok;
+  int lane;
   uint32_t bar, dst;
   int pos[kMaxB], cpp[kMaxB], nch[kMaxB];  // per step
   int route_layer;
-  uint64_t pol;  // L2 policy of every copy
+  int id_b, id_p0, id_n;  // m.pr_ids holds the page ids of sequence id_b, pages [id_p0, id_p0 + id_n)
+  uint64_t pol;           // L2 policy of every copy
 
   __device__ Producer(const Params& p_, const TensorMaps& tm_, Misc& m_, Ring r_)
-      : p(p_), tm(tm_), m(m_), r(r_), ok(true), route_layer(-1) {
+      : p(p_), tm(tm_), m(m_), r(r_), route_layer(-1), id_b(-1), id_p0(0), id_n(0) {
+    lane = threadIdx.x & 31;
     pol = policy_evict_first();
+#pragma unroll 1
     for (int b = 0; b < kMaxB; ++b) {
       pos[b] = b < p.B ? pos_of(p, b) : 0;
       cpp[b] = b < p.B ? p.chunk_pages[b] : 1;
@@ -345,37 +361,73 @@ struct Producer {
     }
   }
 
-  // the routed experts of layer l, loaded once per layer
+  // the routed experts of layer l, loaded once per layer (lane 0 waits, the warp loads)
   __device__ bool route(int l) {
     if (route_layer == l) return true;
-    if (!wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l))) return false;
+    int fine = 1;
     const Route* rt = p.route + l;
-    const int na = __ldcg(&rt->n_active);
-    for (int a = 0; a < na; ++a) m.pr_expert[a] = __ldcg(&rt->expert[a]);
-    m.pr_n = na;
+    if (lane == 0) {
+      fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l));
+      if (fine) m.pr_n = __ldcg(&rt->n_active);
+    }
+    if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
+    __syncwarp();
+    const int na = m.pr_n;
+#pragma unroll 1
+    for (int a = lane; a < na; a += 32) m.pr_expert[a] = __ldcg(&rt->expert[a]);
+    __syncwarp();
     route_layer = l;
     return true;
   }
 
+  // the next ring slot: lane 0 waits until it is free and arms its barrier with `bytes`
   __device__ bool begin(uint32_t bytes) {
     const uint32_t s = r.it % kStages;
     const uint32_t parity = ((r.it / kStages) & 1u) ^ 1u;
-    if (!mbar_wait(p, r.empty + 8 * s, parity)) return false;
     bar = r.full + 8 * s;
     dst = r.data + s * kStageBytes;
-    mbar_expect_tx(bar, bytes);
-    return true;
+    int fine = 1;
+    if (lane == 0) {
+      fine = mbar_wait(p, r.empty + 8 * s, parity);
+      if (fine) mbar_expect_tx(bar, bytes);
+    }
+    fine = __shfl_sync(0xffffffffu, fine, 0);
+    __syncwarp();
+    return fine != 0;
   }
   __device__ void end() { ++r.it; }
 
-  __device__ bool gemv_rows(const uint16_t* base, int rows, int row_bytes) {
-    const uint32_t bytes = (uint32_t)rows * row_bytes;
-    if (!begin(bytes)) return false;
-    bulk_g2s(dst, base, bytes, bar, pol);
+  // `rows` rows of row_bytes each, src_stride elements apart in global memory, into one stage
+  // with the padded row stride rst (one copy per row, spread over the lanes)
+  __device__ bool gemv_rows(const uint16_t* base, int rows, size_t src_stride, int row_bytes, int rst) {
+    if (!begin((uint32_t)rows * row_bytes)) return false;
+#pragma unroll 1
+    for (int rr = lane; rr < rows; rr += 32)
+      bulk_g2s(dst + (uint32_t)(rr * rst), base + (size_t)rr * src_stride, row_bytes, bar, pol);
     end();
     return true;
   }
 
+  // page ids of sequence b, pages [p0, p0 + n) (n <= kIdCache), into m.pr_ids, one per lane;
+  // invalid ids are reported and kept as -1 (their pages are skipped)
+  __device__ void fill_ids(int b, int p0, int n) {
+    id_b = b;
+    id_p0 = p0;
+    id_n = n;
+#pragma unroll 1
+    for (int i = lane; i < n; i += 32) {
+      const int pg = p0 + i;
+      int v = pg < p.max_pages ? __ldg(&p.block_table[b * p.max_pages + pg]) : -1;
+      if (v < 0 || v >= p.num_pages) {
+        report(p, MK_ERR_BAD_PAGE, b, pg);
+        v = -1;
+      }
+      m.pr_ids[i] = v;
+    }
+    __syncwarp();
+  }
+
+  // Issues every copy of task t into the ring, in order. Warp-uniform; false once a wait gave up.
   __device__ bool run_task(const Task& t) {
     const int l = t.layer;
     switch (t.op) {
@@ -383,26 +435,25 @@ struct Producer {
       case OP_LM: {
         const Geo g = geo_of(p.H);
         const uint16_t* W = t.op == OP_ROUTER ? p.w_router + (size_t)l * p.E * p.H : p.lm_head;
+#pragma unroll 1
         for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS)
-          if (!gemv_rows(W + (size_t)r0 * p.H, min(g.RS, t.a + t.b - r0), p.H * 2)) return false;
+          if (!gemv_rows(W + (size_t)r0 * p.H, min(g.RS, t.a + t.b - r0), p.H, p.H * 2, g.RST)) return false;
         return true;
       }
       case OP_QKV: {
         const Geo g = geo_of(p.H);
         const int us = g.RG;  // units per stage
         const uint16_t* W = p.w_qkv + (size_t)l * p.qkv_rows * p.H;
+#pragma unroll 1
         for (int u0 = t.a; u0 < t.a + t.b; u0 += us) {
           const int nu = min(us, t.a + t.b - u0);
           if (!begin((uint32_t)nu * 8 * p.H * 2)) return false;
-          for (int i = 0; i < nu; ++i) {
-            const QkvUnit q = qkv_unit(p, u0 + i);
-            const uint32_t d0 = dst + (uint32_t)i * 8 * p.H * 2;
-            if (q.kind == 2) {
-              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 8 * p.H * 2, bar, pol);
-            } else {
-              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 4 * p.H * 2, bar, pol);
-              bulk_g2s(d0 + 4 * p.H * 2, W + (size_t)(q.row0 + p.d / 2) * p.H, 4 * p.H * 2, bar, pol);
-            }
+#pragma unroll 1
+          for (int j = lane; j < nu * 8; j += 32) {  // unit j / 8, row j % 8
+            const QkvUnit q = qkv_unit(p, u0 + j / 8);
+            const int tt = j % 8;  // k/q: rows tt < 4 from row0, tt >= 4 from row0 + d/2
+            const int row = q.kind == 2 ? q.row0 + tt : q.row0 + (tt & 3) + (tt >= 4 ? p.d / 2 : 0);
+            bulk_g2s(dst + (uint32_t)(j * g.RST), W + (size_t)row * p.H, p.H * 2, bar, pol);
           }
           end();
         }
@@ -412,42 +463,25 @@ struct Producer {
         const int b = t.a, g = t.b;
         const AttnRange ar = attn_range(pos[b], cpp[b], nch[b], t.c);
         const int pps = attn_pps(p), halves = p.d / 64;
-        int ids[64];  // page ids of up to 64 pages, loaded together (one round trip per 64 pages)
-        for (int base = ar.cp0; base < ar.cp1; base += 64) {
-          const int nb = min(64, ar.cp1 - base);
-          for (int i0 = 0; i0 < nb; i0 += 8) {
-            int v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int pg = base + i0 + j;
-              v[j] = (i0 + j < nb && pg < p.max_pages) ? __ldg(&p.block_table[b * p.max_pages + pg]) : -1;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (i0 + j < nb) ids[i0 + j] = v[j];
-          }
-          for (int i = 0; i < nb; ++i)
-            if (ids[i] < 0 || ids[i] >= p.num_pages) {
-              report(p, MK_ERR_BAD_PAGE, b, base + i);
-              ids[i] = -1;
-            }
-          for (int s0 = 0; s0 < nb; s0 += pps) {
-            const int np = min(pps, nb - s0);
-            int good = 0;
-            for (int i = 0; i < np; ++i) good += ids[s0 + i] >= 0;
-            if (!begin((uint32_t)good * 2 * halves * 2048)) return false;
-            for (int i = 0; i < np; ++i) {
-              const int id = ids[s0 + i];
-              if (id < 0) continue;
+#pragma unroll 1
+        for (int s0 = ar.cp0; s0 < ar.cp1; s0 += pps) {
+          const int np = min(pps, ar.cp1 - s0);
+          if (!(id_b == b && s0 >= id_p0 && s0 + np <= id_p0 + id_n)) fill_ids(b, s0, min(kIdCache, ar.cp1 - s0));
+          const int* ids = m.pr_ids + (s0 - id_p0);
+          const int good = __popc(__ballot_sync(0xffffffffu, lane < np && ids[lane < np ? lane : 0] >= 0));
+          if (!begin((uint32_t)good * 2 * halves * 2048)) return false;
+          // copy j: page j / (2 halves), K (0) or V (1), half h
+          const int per = 2 * halves;
+          if (lane < np * per) {
+            const int i = lane / per, kv = (lane / halves) & 1, h = lane % halves;
+            const int id = ids[i];
+            if (id >= 0) {
               const int row = ((l * p.num_pages + id) * p.nkv + g) * kPage;
-              const uint32_t pb = dst + (uint32_t)i * 4096 * halves;
-              for (int h = 0; h < halves; ++h) {
-                tma_2d_g2s(pb + h * 2048, &tm.k, h * 64, row, bar, pol);
-                tma_2d_g2s(pb + (halves + h) * 2048, &tm.v, h * 64, row, bar, pol);
-              }
+              const uint32_t pb = dst + (uint32_t)i * 4096 * halves + (uint32_t)(kv * halves + h) * 2048;
+              tma_2d_g2s(pb, kv ? &tm.v : &tm.k, h * 64, row, bar, pol);
             }
-            end();
           }
+          end();
         }
         return true;
       }
@@ -455,13 +489,20 @@ struct Producer {
         if (!route(l)) return false;
         const int na = m.pr_n, maxa = max_active(p);
         const Geo g = geo_of(p.H);
+        const int half = g.RS / 2;
+#pragma unroll 1
         for (int u = t.a; u < t.a + t.b; ++u) {
           const int a = u % maxa, tile = u / maxa;
           if (a >= na) continue;
           const int e = m.pr_expert[a];
+          // tile: gate rows [tile RS/2, +RS/2) then the matching up rows (I rows further on)
           const uint16_t* W = p.w_gate_up + ((size_t)l * p.E + e) * 2 * p.I * p.H;
           if (!begin((uint32_t)g.RS * p.H * 2)) return false;
-          bulk_g2s(dst, W + (size_t)tile * g.RS * p.H, (uint32_t)g.RS * p.H * 2, bar, pol);
+#pragma unroll 1
+          for (int rr = lane; rr < g.RS; rr += 32) {
+            const int row = (rr < half ? 0 : p.I) + tile * half + (rr % half);
+            bulk_g2s(dst + (uint32_t)(rr * g.RST), W + (size_t)row * p.H, p.H * 2, bar, pol);
+          }
           end();
         }
         return true;
@@ -469,25 +510,20 @@ struct Producer {
       case OP_O: {
         const Geo g = geo_of(p.od);
         const uint16_t* W = p.w_o + ((size_t)l * p.H + t.a) * p.od;
-        for (int cs = 0; cs < g.NCS; ++cs) {
-          if (g.NCS == 1) {
-            if (!gemv_rows(W, t.b, p.od * 2)) return false;
-          } else {
-            if (!begin((uint32_t)t.b * g.KS * 2)) return false;
-            for (int r = 0; r < t.b; ++r)
-              bulk_g2s(dst + (uint32_t)r * g.KS * 2, W + (size_t)r * p.od + cs * g.KS, g.KS * 2, bar, pol);
-            end();
-          }
-        }
+#pragma unroll 1
+        for (int cs = 0; cs < g.NCS; ++cs)
+          if (!gemv_rows(W + cs * g.KS, t.b, p.od, g.KS * 2, g.RST)) return false;
         return true;
       }
       case OP_DOWN: {
         if (!route(l)) return false;
         const int na = m.pr_n;
+        const Geo g = geo_of(p.I);
+#pragma unroll 1
         for (int a = 0; a < na; ++a) {
           const int e = m.pr_expert[a];
           const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + t.a) * p.I;
-          if (!gemv_rows(W, t.b, p.I * 2)) return false;
+          if (!gemv_rows(W, t.b, p.I, p.I * 2, g.RST)) return false;
         }
         return true;
       }
@@ -511,102 +547,13 @@ struct Producer {
 
 // ------------------------------------------------------------------ consumer building blocks
 
-// Halving butterfly: sums v[N] over the 32 lanes. For N <= 32 the lane ends with the total
-// of index lane >> (5 - log2 N) in v[0]; for N = 64 with indices 2*lane and 2*lane+1.
-template <int C, int O>
-struct LaneReduce {
-  static __device__ __forceinline__ void run(float* v, int lane) {
-    if constexpr (O > 0) {
-      if constexpr (C > 1) {
-        const bool up = (lane & O) != 0;
-#pragma unroll
-        for (int i = 0; i < C / 2; ++i) {
-          const float send = up ? v[i] : v[i + C / 2];
-          const float keep = up ? v[i + C / 2] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-        }
-        LaneReduce<C / 2, O / 2>::run(v, lane);
-      } else {
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-        LaneReduce<1, O / 2>::run(v, lane);
-      }
-    }
-  }
-};
-
-template <int NB>
-__device__ __forceinline__ void warp_partials_to_smem(float (&acc)[8][NB], float* red_w, int lane) {
-  constexpr int N = 8 * NB;
-  float v[N];
-#pragma unroll
-  for (int r = 0; r < 8; ++r)
-#pragma unroll
-    for (int b = 0; b < NB; ++b) v[r * NB + b] = acc[r][b];
-  LaneReduce<N, 16>::run(v, lane);
-  if constexpr (N <= 32) {
-    constexpr int rep = 32 / N;
-    if ((lane & (rep - 1)) == 0) red_w[lane / rep] = v[0];
-  } else {
-    red_w[2 * lane] = v[0];
-    red_w[2 * lane + 1] = v[1];
-  }
-}
-
-// Sum the row groups' k-slices of red into res[row * NB + b] for rows < rows, using threads
-// [t0, t0 + nthreads). Caller syncs around.
-template <int NB>
-__device__ __forceinline__ void cross_warp_reduce(const float (*red)[64], float* res, const Geo& g, int rows, int t,
-                                                  int nthreads) {
-  for (int e = t; e < rows * NB; e += nthreads) {
-    const int r = e / NB, b = e % NB, rg = r / 8;
-    float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (k < g.KW) s += red[rg * g.KW + k][(r % 8) * NB + b];
-    res[e] = s;
-  }
-}
-
-// Accumulate one stage's rows for this warp: acc[r][b] += W[row][cols] . act[b][cols]
-template <int NB>
-__device__ __forceinline__ void gemv_stage(const uint8_t* stage, const Geo& g, int rg, int ks, int lane, int rows_valid,
-                                           const float (&act)[NB][8], float (&acc)[8][NB], uint32_t bmask) {
-  const uint8_t* base = stage + (size_t)(rg * 8) * g.KS * 2 + (size_t)(ks * 256 + lane * 8) * 2;
-  constexpr int RB = NB <= 2 ? 8 : (NB == 4 ? 4 : 2);  // rows whose loads are in flight together
-#pragma unroll
-  for (int r0 = 0; r0 < 8; r0 += RB) {
-    uint4 w[RB];
-#pragma unroll
-    for (int j = 0; j < RB; ++j)
-      w[j] = r0 + j < rows_valid ? *reinterpret_cast<const uint4*>(base + (size_t)(r0 + j) * g.KS * 2)
-                                 : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int j = 0; j < RB; ++j) {
-      const int r = r0 + j;
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if (bmask & (1u << b)) {  // two accumulation chains per row
-          float s0 = fmaf(bf_lo(w[j].x), act[b][0], acc[r][b]);
-          float s1 = bf_hi(w[j].x) * act[b][1];
-          s0 = fmaf(bf_lo(w[j].y), act[b][2], s0);
-          s1 = fmaf(bf_hi(w[j].y), act[b][3], s1);
-          s0 = fmaf(bf_lo(w[j].z), act[b][4], s0);
-          s1 = fmaf(bf_hi(w[j].z), act[b][5], s1);
-          s0 = fmaf(bf_lo(w[j].w), act[b][6], s0);
-          s1 = fmaf(bf_hi(w[j].w), act[b][7], s1);
-          acc[r][b] = s0 + s1;
-        }
-      }
-    }
-  }
-}
-
-template <int NB>
-__device__ __forceinline__ void zero_acc(float (&acc)[8][NB]) {
-#pragma unroll
-  for (int r = 0; r < 8; ++r)
-#pragma unroll
-    for (int b = 0; b < NB; ++b) acc[r][b] = 0.f;
+// bf16 pair (lower column in the low half) of the high or the low part of two fp32 values:
+// hi = bf16(x), lo = bf16(x - hi), so hi + lo carries about 16 significant bits of x
+__device__ __forceinline__ uint32_t pack_part(float x0, float x1, int lo) {
+  const uint16_t h0 = f2bf(x0), h1 = f2bf(x1);
+  const uint16_t v0 = lo ? f2bf(x0 - bf2f(h0)) : h0;
+  const uint16_t v1 = lo ? f2bf(x1 - bf2f(h1)) : h1;
+  return (uint32_t)v0 | ((uint32_t)v1 << 16);
 }
 
 __device__ __forceinline__ void load8(const float* src, float (&dst)[8]) {
@@ -645,14 +592,18 @@ struct Consumer {
   int warp, lane;
   bool ok;
   uint32_t cbar, cphase;
-  int rpar;             // which half of m.red the next reduction uses
-  int n_layer;          // layer whose normalized input is held in `nact` (-1 none)
+  static constexpr int AR = NB > 4 ? 4 : 2;  // mma A-fragment registers per k-step
+  uint32_t gv;          // GEMV passes done (every consumer warp counts the same sequence)
+  int n_layer;          // layer whose normalized input is held in `nf` (-1 none)
   int route_layer;      // layer whose routing is cached in m.rc_*
   int gu_layer;         // layer whose expert gate/up work is known complete
   int attn_layer;       // layer of attn_ok
   uint32_t attn_ok;     // KV groups whose attention is known complete in attn_layer
-  float nact[NB][8];    // this lane's 8 columns of the normalized input, per token
-  float lm_best[NB];    // running LM-head argmax (threads < B)
+  // the normalized input of layer n_layer, this warp's 256-column slice as mma A fragments:
+  // lane (g, t) holds the hi (g even) or lo (g odd) part of token g/2 (registers 0, 1) and of
+  // token g/2 + 4 (registers 2, 3) at columns 16 s + 2 t + {0, 1} and + {8, 9}
+  uint32_t nf[16][AR];
+  float lm_best[NB];    // running LM-head argmax of the stages whose epilogue this lane ran
   int lm_idx[NB];
   uint64_t t_start, t_ready;
 
@@ -663,7 +614,7 @@ struct Consumer {
     lane = threadIdx.x % 32;
     cbar = smem_addr(&m_.cbar);
     cphase = 0;
-    rpar = 0;
+    gv = 0;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       lm_best[b] = -INFINITY;
@@ -685,18 +636,6 @@ struct Consumer {
     ++r.it;
   }
   __device__ uint32_t bmask_all() const { return (1u << p.B) - 1u; }
-  // h holds, per (layer, active expert, token), the raw gate then up projections [2I]
-  __device__ __forceinline__ size_t h_index(int l, int a, int b) const {
-    return (((size_t)l * kMaxActive + a) * kMaxB + b) * 2 * (size_t)p.I;
-  }
-  // SiLU(gate) * up * routing weight for 8 consecutive intermediate columns
-  __device__ __forceinline__ void load_h8(int l, int a, int b, int col, float wgt, float (&dst)[8]) const {
-    float gt[8], up[8];
-    load8(p.h + h_index(l, a, b) + col, gt);
-    load8(p.h + h_index(l, a, b) + p.I + col, up);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = gt[i] / (1.0f + expf(-gt[i])) * up[i] * wgt;
-  }
 
   // Barrier of the 8 consumer warps on an mbarrier, with the same time limit as every other
   // wait: a warp that gives up (timeout or abort) leaves the kernel and the rest follow.
@@ -762,21 +701,48 @@ struct Consumer {
     const uint4 gw = *reinterpret_cast<const uint4*>(gain + col);
     const float gf[8] = {bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y),
                          bf_lo(gw.z), bf_hi(gw.z), bf_lo(gw.w), bf_hi(gw.w)};
+    // normalized input into mma fragments, one token at a time through this warp's exchange area
+    float* xw = m.nsm + warp * 256;
+    const int g8 = lane >> 2, t4 = lane & 3, hl = g8 & 1, tb = g8 >> 1;
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+#pragma unroll
+      for (int r = 0; r < AR; ++r) nf[s][r] = 0u;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       float tot = 0.f;
       for (int k = 0; k < g.KW; ++k) tot += m.norm[k][b];
       const float rinv = 1.0f / sqrtf(tot / (float)p.H + p.eps);
+      float xn[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) nact[b][i] = x[b][i] * rinv * gf[i];
-    }
-    if constexpr (NB == 1) {
-      if (warp < g.KW) {
-        float4* dn = reinterpret_cast<float4*>(&m.nsm[col]);
-        dn[0] = make_float4(nact[0][0], nact[0][1], nact[0][2], nact[0][3]);
-        dn[1] = make_float4(nact[0][4], nact[0][5], nact[0][6], nact[0][7]);
+      for (int i = 0; i < 8; ++i) xn[i] = x[b][i] * rinv * gf[i];
+      __syncwarp();
+      float4* d4 = reinterpret_cast<float4*>(xw + lane * 8);
+      d4[0] = make_float4(xn[0], xn[1], xn[2], xn[3]);
+      d4[1] = make_float4(xn[4], xn[5], xn[6], xn[7]);
+      __syncwarp();
+      if (tb == b) {
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+          const float2 v0 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4);
+          const float2 v1 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4 + 8);
+          nf[s][0] = pack_part(v0.x, v0.y, hl);
+          nf[s][1] = pack_part(v1.x, v1.y, hl);
+        }
+      }
+      if constexpr (AR == 4) {
+        if (tb + 4 == b) {
+#pragma unroll
+          for (int s = 0; s < 16; ++s) {
+            const float2 v0 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4);
+            const float2 v1 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4 + 8);
+            nf[s][2] = pack_part(v0.x, v0.y, hl);
+            nf[s][3] = pack_part(v1.x, v1.y, hl);
+          }
+        }
       }
     }
+    __syncwarp();
     if (write_x && warp < g.KW) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
@@ -794,27 +760,103 @@ struct Consumer {
     if (n_layer != l) load_norm(l, write_x);
   }
 
-  // One GEMV stage against the held normalized input. All warps add their partials to one
-  // half of m.red and meet once; warp 0 then reduces them into m.res [rows][NB] and runs
-  // `epi` (its lanes), while the other warps go on to the next stage.
-  template <typename Epi>
-  __device__ bool norm_gemv_stage(const Geo& g, int rows, uint32_t bmask, Epi&& epi) {
-    const int rg = warp / g.KW, ks = warp % g.KW;
-    float acc[8][NB];
-    zero_acc(acc);
-    const uint8_t* st = acquire();
-    if (!st) return false;
-    if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, rows - rg * 8), nact, acc, bmask);
-    release();
-    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[rpar][warp], lane);
-    if (!csync()) return false;
-    if (warp == 0) {
-      cross_warp_reduce<NB>(m.red[rpar], m.res, g, rows, lane, 32);
-      __syncwarp();
-      epi();
+  // ---------------------------------------------------------------- tensor-core GEMV
+  // A GEMV pass accumulates one or more stages into per-warp mma accumulators: warp (rg, ks)
+  // multiplies rows [8 rg, 8 rg + 8) x columns [256 ks, 256 ks + 256) of each stage (the B
+  // operand, 8 rows = n8) by activation fragments (the A operand: up to 8 tokens x hi/lo = m16),
+  // in four accumulation chains. post_pass / run_epi then add the warps' k-slices.
+
+  __device__ __forceinline__ void afrag(const uint32_t (&f)[AR], uint32_t (&a)[4]) const {
+    a[0] = f[0];
+    a[2] = f[1];
+    if constexpr (AR == 4) {
+      a[1] = f[2];
+      a[3] = f[3];
+    } else {
+      a[1] = 0u;
+      a[3] = 0u;
     }
-    rpar ^= 1;
-    return true;
+  }
+  __device__ __forceinline__ void mma_rows(uint32_t st, const Geo& g, int rg, int ks, const uint32_t (&af)[16][AR],
+                                           float (&c)[4][4]) const {
+    // ldmatrix.x4: lanes 8q..8q+7 address rows 0..7 at columns 8q..8q+7 of a 32-column block,
+    // giving the B fragments of two k-steps
+    const uint32_t base = st + (uint32_t)((rg * 8 + (lane & 7)) * g.RST) + (uint32_t)((ks * 256 + (lane >> 3) * 8) * 2);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t bw[4], a[4];
+      ldsm_x4(base + j * 64, bw);
+      afrag(af[2 * j], a);
+      mma_bf16(c[(2 * j) & 3], a, bw[0], bw[1]);
+      afrag(af[2 * j + 1], a);
+      mma_bf16(c[(2 * j + 1) & 3], a, bw[2], bw[3]);
+    }
+  }
+  // End of a GEMV pass: each warp leaves its partial sums (rows [8 rg, 8 rg + 8) x tokens) in
+  // buffer pid % kRedBufs and goes on; returns the pass id. The buffers are handed over by
+  // mbarriers: gpart (all 8 warps posted) and gfree (the pass's epilogue warp has read them).
+  __device__ uint32_t post_pass(bool active, const float (&c)[4][4]) {
+    const uint32_t pid = gv++;
+    const int buf = pid % kRedBufs;
+    const uint32_t ph = (pid / kRedBufs) & 1u;
+    float s[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s[i] = (c[0][i] + c[1][i]) + (c[2][i] + c[3][i]);
+      s[i] += __shfl_xor_sync(0xffffffffu, s[i], 4);  // hi part (even g) + lo part (odd g)
+    }
+    if (!mbar_wait_cta(p, smem_addr(&m.gfree[buf]), ph ^ 1u)) {
+      ok = false;
+      return pid;
+    }
+    const int g8 = lane >> 2, t4 = lane & 3;
+    if (active && !(g8 & 1)) {  // rows 2 t4, 2 t4 + 1 of token g8/2 (and g8/2 + 4)
+      float* rw = m.red[buf][warp];
+      rw[(2 * t4) * 8 + (g8 >> 1)] = s[0];
+      rw[(2 * t4 + 1) * 8 + (g8 >> 1)] = s[1];
+      if constexpr (NB > 4) {
+        rw[(2 * t4) * 8 + (g8 >> 1) + 4] = s[2];
+        rw[(2 * t4 + 1) * 8 + (g8 >> 1) + 4] = s[3];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&m.gpart[buf]));
+    return pid;
+  }
+  // The epilogue of pass pid, in its epilogue warp (pid % 8: the duty rotates): epi(R) with
+  // R(row, token) the pass's result, summed over the k-slices from the partials. Callers run it
+  // one pass late (after posting the next pass), so it neither waits for the other warps nor
+  // holds up the next stage.
+  template <typename Epi>
+  __device__ void run_epi(uint32_t pid, const Geo& g, Epi&& epi) {
+    if (warp != (int)(pid % kConsumerWarps) || !ok) return;
+    const int buf = pid % kRedBufs;
+    if (!mbar_wait_cta(p, smem_addr(&m.gpart[buf]), (pid / kRedBufs) & 1u)) {
+      ok = false;
+      return;
+    }
+    const float(*rb)[64] = m.red[buf];
+    const int kw = g.KW;
+    auto R = [&](int rr, int b) -> float {
+      const int rg = rr >> 3;
+      float v = 0.f;
+      for (int q = 0; q < kw; ++q) v += rb[rg * kw + q][(rr & 7) * 8 + b];
+      return v;
+    };
+    epi(R);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&m.gfree[buf]));
+  }
+  // One stage against the normalized input (nf), as one pass; returns its id.
+  __device__ uint32_t norm_pass(const Geo& g) {
+    const int rg = warp / g.KW, ks = warp % g.KW;
+    const bool active = rg < g.RG;
+    float c[4][4] = {};
+    const uint8_t* st = acquire();
+    if (!st) return gv;
+    if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, nf, c);
+    release();
+    return post_pass(active, c);
   }
 
   __device__ void release_counter(int idx) {
@@ -888,27 +930,72 @@ struct Consumer {
     return true;
   }
 
+  // hi/lo bf16 planes of an activation value (hi = bf16(v), lo = bf16(v - hi))
+  __device__ __forceinline__ void store_hl(uint16_t* hi, size_t plane, float v) const {
+    const uint16_t h = f2bf(v);
+    hi[0] = h;
+    hi[plane] = f2bf(v - bf2f(h));
+  }
+  // attention output of token b, column col of layer l: fp32 and the GEMV's hi/lo planes
+  __device__ __forceinline__ void store_attn(int l, int b, int col, float v) const {
+    __stcg(&p.attn_o[((size_t)l * p.B + b) * p.od + col], v);
+    store_hl(p.attn_hl + ((size_t)l * 2 * p.B + b) * p.od + col, (size_t)p.B * p.od, v);
+  }
+  // h planes: [layer][active expert][hi, lo][token][I]
+  __device__ __forceinline__ size_t h_plane(int l, int a) const {
+    return ((size_t)l * kMaxActive + a) * 2 * kMaxB * (size_t)p.I;
+  }
+  // A fragments from hi/lo bf16 planes (no conversion): token b's row of this warp's slice in
+  // plane hl starts at element base + hl * plane + b * row; tokens outside bmask are zero
+  __device__ __forceinline__ void ld_frags_hl(const uint16_t* base, size_t plane, size_t row, uint32_t bmask,
+                                              uint32_t (&af)[16][AR]) const {
+    const int g8 = lane >> 2, t4 = lane & 3, hl = g8 & 1, b0 = g8 >> 1;
+    const bool v0 = (bmask >> b0) & 1u;
+    const uint32_t* s0 = reinterpret_cast<const uint32_t*>(base + hl * plane + (size_t)b0 * row) + t4;
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      af[s][0] = v0 ? __ldcg(s0 + 8 * s) : 0u;
+      af[s][1] = v0 ? __ldcg(s0 + 8 * s + 4) : 0u;
+    }
+    if constexpr (AR == 4) {
+      const bool v1 = (bmask >> (b0 + 4)) & 1u;
+      const uint32_t* s1 = reinterpret_cast<const uint32_t*>(base + hl * plane + (size_t)(b0 + 4) * row) + t4;
+#pragma unroll
+      for (int s = 0; s < 16; ++s) {
+        af[s][2] = v1 ? __ldcg(s1 + 8 * s) : 0u;
+        af[s][3] = v1 ? __ldcg(s1 + 8 * s + 4) : 0u;
+      }
+    }
+  }
+
   // ---------------------------------------------------------------- opcodes
 
   __device__ void op_router(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     const Geo g = geo_of(p.H);
-    for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
-      const int rows = min(g.RS, t.a + t.b - r0);
-      const bool st_ok = norm_gemv_stage(g, rows, bmask_all(), [&] {
+    auto epi = [&](uint32_t pid, int r0, int rows) {
+      run_epi(pid, g, [&](auto&& R) {
         for (int i = lane; i < rows * NB; i += 32) {
           const int rr = i / NB, b = i % NB;
           if (b >= p.B) continue;
           const int e = r0 + rr;
           const float bias = p.router_bias ? p.router_bias[(size_t)l * p.E + e] : 0.f;
-          __stcg(&p.rlogits[((size_t)l * p.B + b) * p.E + e], m.res[i] + bias);
+          __stcg(&p.rlogits[((size_t)l * p.B + b) * p.E + e], R(rr, b) + bias);
         }
       });
-      if (!st_ok) return;
+    };
+    uint32_t prev = 0;
+    int pr0 = -1, prows = 0;
+    for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
+      const int rows = min(g.RS, t.a + t.b - r0);
+      const uint32_t pid = norm_pass(g);
+      if (!ok) return;
+      if (pr0 >= 0) epi(prev, pr0, prows);
+      prev = pid, pr0 = r0, prows = rows;
     }
+    if (pr0 >= 0) epi(prev, pr0, prows);
+    if (!ok) return;
     if (arrive_last_w0(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) publish_routing(l);
   }
 
@@ -970,20 +1057,31 @@ struct Consumer {
       if (lane < K) m.wk[b][lane] /= z;
     }
     __syncwarp();
+    // token masks per expert, then the distinct experts in ascending id (32 per round)
+#pragma unroll 1
+    for (int e = lane; e < E; e += 32) m.em[e] = 0u;
+    __syncwarp();
+#pragma unroll 1
+    for (int i = lane; i < B * K; i += 32) atomicOr(&m.em[m.ids[i / K][i % K]], 1u << (i / K));
+    __syncwarp();
     Route* rt = p.route + l;
     int na = 0;
-#pragma unroll
-    for (int i = 0; i < NE; ++i) {
-      const uint32_t act = __ballot_sync(0xffffffffu, emask[i] != 0u);
-      if (emask[i] != 0u) {
-        const int e = lane + 32 * i;
+#pragma unroll 1
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const uint32_t mask = e < E ? m.em[e] : 0u;
+      const uint32_t act = __ballot_sync(0xffffffffu, mask != 0u);
+      if (mask != 0u) {
         const int r = na + __popc(act & ((1u << lane) - 1u));
         __stcg(&rt->expert[r], e);
-        __stcg(&rt->mask[r], emask[i]);
+        __stcg(&rt->mask[r], mask);
+#pragma unroll 1
         for (int b = 0; b < kMaxB; ++b) {
           float w = 0.f;
-          if (emask[i] & (1u << b))
+          if (mask & (1u << b)) {
+#pragma unroll 1
             for (int j = 0; j < K; ++j) w = m.ids[b][j] == e ? m.wk[b][j] : w;
+          }
           __stcg(&rt->w[r][b], w);
         }
       }
@@ -1003,15 +1101,12 @@ struct Consumer {
 
   __device__ void op_qkv(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     const Geo g = geo_of(p.H);
     const int hd = p.d / 2;
-    for (int u0 = t.a; u0 < t.a + t.b && ok; u0 += g.RG) {
-      const int nu = min(g.RG, t.a + t.b - u0);
-      const bool st_ok = norm_gemv_stage(g, nu * 8, bmask_all(), [&] {
-      // epilogue: RoPE on q/k pairs, bf16 K/V append
+    // epilogue: RoPE on k pairs, bf16 K/V append, q stored before RoPE
+    auto epi = [&](uint32_t pid, int u0, int nu) {
+      run_epi(pid, g, [&](auto&& R) {
       for (int i = lane; i < nu * 8 * NB; i += 32) {
         const int unit = i / (8 * NB), rem = i % (8 * NB), tt = rem / NB, b = rem % NB;
         if (b >= p.B) continue;
@@ -1019,10 +1114,9 @@ struct Consumer {
         const int pos = m.st_pos[b];
         const int page = q.kind != 0 ? m.st_page[b] : -1;
         if (q.kind != 0 && page < 0 && tt == 0 && unit == 0) report(p, MK_ERR_BAD_PAGE, b, pos);
-        const float* res = m.res + unit * 8 * NB;
         if (q.kind == 2) {  // v: 8 consecutive elements
           const int e = 8 * q.j + tt;
-          const uint16_t vb = f2bf(res[tt * NB + b]);
+          const uint16_t vb = f2bf(R(unit * 8 + tt, b));
           __stcg(&p.vnew[(((size_t)l * p.B + b) * p.nkv + q.head) * p.d + e], bf2f(vb));
           if (page >= 0)
             p.vpool[((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d + e] = vb;
@@ -1030,12 +1124,12 @@ struct Consumer {
         }
         if (q.kind == 0) {  // q is stored before RoPE; attention rotates it when it loads it
           const int e = 4 * q.j + (tt & 3) + (tt >= 4 ? hd : 0);
-          __stcg(&p.q[(((size_t)l * p.B + b) * p.nq + q.head) * p.d + e], res[tt * NB + b]);
+          __stcg(&p.q[(((size_t)l * p.B + b) * p.nq + q.head) * p.d + e], R(unit * 8 + tt, b));
           continue;
         }
         if (tt >= 4) continue;  // k pair (tt, tt + 4) handled by the lower row
         const int pi2 = 4 * q.j + tt;  // pair index in [0, d/2)
-        const float a = res[tt * NB + b], c = res[(tt + 4) * NB + b];
+        const float a = R(unit * 8 + tt, b), c = R(unit * 8 + tt + 4, b);
         const float2 cs = m.st_rope[b][pi2];
         const float lo = a * cs.x - c * cs.y;
         const float hi = a * cs.y + c * cs.x;
@@ -1052,31 +1146,52 @@ struct Consumer {
         }
       }
       });
-      if (!st_ok) return;
+    };
+    uint32_t prev = 0;
+    int pu0 = -1, pnu = 0;
+    for (int u0 = t.a; u0 < t.a + t.b && ok; u0 += g.RG) {
+      const int nu = min(g.RG, t.a + t.b - u0);
+      const uint32_t pid = norm_pass(g);
+      if (!ok) return;
+      if (pu0 >= 0) epi(prev, pu0, pnu);
+      prev = pid, pu0 = u0, pnu = nu;
     }
+    if (pu0 >= 0) epi(prev, pu0, pnu);
     if (ok) release_counter(cm.qkv(l, t.c));
   }
 
   __device__ void op_gu(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     if (!load_route(l)) return;
     t_ready = gtimer();
     const int na = m.rc_n, maxa = max_active(p);
     const Geo g = geo_of(p.H);
+    // a stage holds gate rows [tile RS/2, +RS/2) of active expert a, then the matching up rows;
+    // the epilogue stores SiLU(gate) * up * routing weight
+    auto epi = [&](uint32_t pid, int a, int tile) {
+      const uint32_t bm = m.rc_mask[a];
+      run_epi(pid, g, [&](auto&& R) {
+        const int half = g.RS / 2;
+        for (int i = lane; i < half * NB; i += 32) {
+          const int j = i / NB, b = i % NB;
+          if (!(bm & (1u << b))) continue;
+          const float gt = R(j, b), up = R(half + j, b);
+          store_hl(p.h + h_plane(l, a) + (size_t)b * p.I + tile * half + j, (size_t)kMaxB * p.I,
+                   gt / (1.0f + expf(-gt)) * up * m.rc_w[a][b]);
+        }
+      });
+    };
+    uint32_t prev = 0;
+    int pa = -1, ptile = 0;
     for (int u = t.a; u < t.a + t.b && ok; ++u) {
       const int a = u % maxa, tile = u / maxa;
       if (a >= na) continue;
-      const uint32_t bm = m.rc_mask[a];
-      const bool st_ok = norm_gemv_stage(g, g.RS, bm, [&] {
-        for (int i = lane; i < g.RS * NB; i += 32) {
-          const int rr = i / NB, b = i % NB;
-          if (bm & (1u << b)) __stcg(&p.h[h_index(l, a, b) + tile * g.RS + rr], m.res[i]);
-        }
-      });
-      if (!st_ok) return;
+      const uint32_t pid = norm_pass(g);
+      if (!ok) return;
+      if (pa >= 0) epi(prev, pa, ptile);
+      prev = pid, pa = a, ptile = tile;
     }
+    if (pa >= 0) epi(prev, pa, ptile);
     if (ok) release_counter(cm.gu(l));
   }
 
@@ -1084,40 +1199,31 @@ struct Consumer {
     const int l = t.layer;
     const Geo g = geo_of(p.od);
     const int rg = warp / g.KW, ks = warp % g.KW;
+    const bool active = rg < g.RG;
     const int gw = p.group * p.d;  // columns per KV group
-    float acc[8][NB];
-    zero_acc(acc);
+    float c[4][4] = {};
     t_ready = 0;
     for (int cs = 0; cs < g.NCS; ++cs) {
       const int c0 = cs * g.KS + ks * 256;
-      float act[NB][8];
-      if (rg < g.RG) {
+      uint32_t af[16][AR];
+      if (active) {
         for (int gg = c0 / gw; gg <= (c0 + 255) / gw; ++gg)
           if (!wait_attn_group(l, gg)) return;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          if (b < p.B) load8(p.attn_o + ((size_t)l * p.B + b) * p.od + c0 + lane * 8, act[b]);
-          else
-#pragma unroll
-            for (int i = 0; i < 8; ++i) act[b][i] = 0.f;
-        }
+        ld_frags_hl(p.attn_hl + (size_t)l * 2 * p.B * p.od + c0, (size_t)p.B * p.od, p.od, bmask_all(), af);
       }
       if (!t_ready) t_ready = gtimer();
       const uint8_t* st = acquire();
       if (!st) return;
-      if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, t.b - rg * 8), act, acc, bmask_all());
+      if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, af, c);
       release();
     }
-    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[rpar][warp], lane);
-    if (!csync()) return;
-    cross_warp_reduce<NB>(m.red[rpar], m.res, g, t.b, threadIdx.x, 256);
-    rpar ^= 1;
-    if (!csync()) return;
-    for (int i = threadIdx.x; i < t.b * NB; i += 256) {
-      const int rr = i / NB, b = i % NB;
-      if (b < p.B) __stcg(&p.attn_out[((size_t)l * p.B + b) * p.H + t.a + rr], m.res[i]);
-    }
-    release_counter(cm.layer(l));
+    run_epi(post_pass(active, c), g, [&](auto&& R) {
+      for (int i = lane; i < t.b * NB; i += 32) {
+        const int rr = i / NB, b = i % NB;
+        if (b < p.B) __stcg(&p.attn_out[((size_t)l * p.B + b) * p.H + t.a + rr], R(rr, b));
+      }
+    });
+    if (ok) release_counter(cm.layer(l));
   }
 
   __device__ void op_down(const Task& t) {
@@ -1126,53 +1232,45 @@ struct Consumer {
     t_ready = gtimer();
     const Geo g = geo_of(p.I);
     const int rg = warp / g.KW, ks = warp % g.KW;
+    const bool active = rg < g.RG;
     const int na = m.rc_n;
-    float acc[8][NB];
-    zero_acc(acc);
+    float c[4][4] = {};
+    uint32_t af[16][AR], an[16][AR];
+    const size_t hpl = (size_t)kMaxB * p.I;
+    // the activations of expert a + 1 are loaded while expert a's stage is multiplied
+    if (active && na > 0) ld_frags_hl(p.h + h_plane(l, 0) + ks * 256, hpl, p.I, m.rc_mask[0], an);
     for (int a = 0; a < na; ++a) {
-      const uint32_t bm = m.rc_mask[a];
-      float act[NB][8];
-      if (rg < g.RG) {
+      if (active) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          if (bm & (1u << b)) {
-            load_h8(l, a, b, ks * 256 + lane * 8, m.rc_w[a][b], act[b]);
-          } else {
+        for (int s = 0; s < 16; ++s)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) act[b][i] = 0.f;
-          }
-        }
+          for (int r = 0; r < AR; ++r) af[s][r] = an[s][r];
+        if (a + 1 < na) ld_frags_hl(p.h + h_plane(l, a + 1) + ks * 256, hpl, p.I, m.rc_mask[a + 1], an);
       }
       const uint8_t* st = acquire();
       if (!st) return;
-      if (rg < g.RG) gemv_stage<NB>(st, g, rg, ks, lane, min(8, t.b - rg * 8), act, acc, bm);
+      if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, af, c);
       release();
     }
-    if (rg < g.RG) warp_partials_to_smem<NB>(acc, m.red[rpar][warp], lane);
-    if (!csync()) return;
-    cross_warp_reduce<NB>(m.red[rpar], m.res, g, t.b, threadIdx.x, 256);
-    rpar ^= 1;
-    if (!csync()) return;
-    for (int i = threadIdx.x; i < t.b * NB; i += 256) {
-      const int rr = i / NB, b = i % NB;
-      if (b < p.B) __stcg(&p.moe_out[((size_t)l * p.B + b) * p.H + t.a + rr], m.res[i]);
-    }
-    release_counter(cm.layer(l));
+    run_epi(post_pass(active, c), g, [&](auto&& R) {
+      for (int i = lane; i < t.b * NB; i += 32) {
+        const int rr = i / NB, b = i % NB;
+        if (b < p.B) __stcg(&p.moe_out[((size_t)l * p.B + b) * p.H + t.a + rr], R(rr, b));
+      }
+    });
+    if (ok) release_counter(cm.layer(l));
   }
 
   __device__ void op_lm(const Task& t) {
-    ensure_norm(p.L, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     const Geo g = geo_of(p.H);
-    for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
-      const int rows = min(g.RS, t.a + t.b - r0);
-      const bool st_ok = norm_gemv_stage(g, rows, bmask_all(), [&] {
+    auto epi = [&](uint32_t pid, int r0, int rows) {
+      run_epi(pid, g, [&](auto&& R) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
         for (int e = lane; e < rows * NB; e += 32) {  // e % NB == lane % NB since 32 % NB == 0
           const int rr = e / NB, b = e % NB;
-          const float v = m.res[e];
+          const float v = R(rr, b);
           if (b < p.B && p.logits) __stcg(&p.logits[(size_t)b * p.V + r0 + rr], v);
           if (v > bv || (v == bv && r0 + rr < bi)) { bv = v; bi = r0 + rr; }
         }
@@ -1184,12 +1282,32 @@ struct Consumer {
         }
         if (bv > lm_best[0] || (bv == lm_best[0] && bi < lm_idx[0])) { lm_best[0] = bv; lm_idx[0] = bi; }
       });
-      if (!st_ok) return;
+    };
+    uint32_t prev = 0;
+    int pr0 = -1, prows = 0;
+    for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
+      const int rows = min(g.RS, t.a + t.b - r0);
+      const uint32_t pid = norm_pass(g);
+      if (!ok) return;
+      if (pr0 >= 0) epi(prev, pr0, prows);
+      prev = pid, pr0 = r0, prows = rows;
     }
+    if (pr0 >= 0) epi(prev, pr0, prows);
     if (!(t.flags & TF_LAST_LM) || !ok) return;
-    if (threadIdx.x < NB && threadIdx.x < p.B) {  // warp 0, lane b: token b
-      __stcg(&p.lm_best_v[t.c * kMaxB + threadIdx.x], lm_best[0]);
-      __stcg(&p.lm_best_i[t.c * kMaxB + threadIdx.x], lm_idx[0]);
+    // lanes < NB of every warp hold that warp's candidate for token lane; combine over warps
+    if (lane < NB) {
+      m.lmw_v[warp][lane] = lm_best[0];
+      m.lmw_i[warp][lane] = lm_idx[0];
+    }
+    if (!csync()) return;
+    if (threadIdx.x < p.B) {  // warp 0, lane b: token b
+      const int b = threadIdx.x;
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int w = 0; w < kConsumerWarps; ++w)
+        if (m.lmw_v[w][b] > bv || (m.lmw_v[w][b] == bv && m.lmw_i[w][b] < bi)) { bv = m.lmw_v[w][b]; bi = m.lmw_i[w][b]; }
+      __stcg(&p.lm_best_v[t.c * kMaxB + b], bv);
+      __stcg(&p.lm_best_i[t.c * kMaxB + b], bi);
     }
     if (!arrive_last(cm.lm_arrive(), p.n_lm_sm)) return;
     if (threadIdx.x < p.B) {
@@ -1202,215 +1320,6 @@ struct Consumer {
         if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
       }
       if (p.argmax_out) p.argmax_out[b] = bi;
-    }
-  }
-
-
-  // ---------------------------------------------------------------- batch-1 row-per-warp opcodes
-  // With one token, a warp owns whole rows of a stage (all H columns, the normalized input in
-  // registers), so each row needs only a warp reduction and its epilogue runs in that warp: no
-  // block-wide barrier per stage.
-
-  // this lane's columns pp*256 + lane*8 + i of the normalized input held in m.nsm
-  __device__ __forceinline__ void rows_act(float (&a)[64]) const {
-    const int np = p.H / 256;
-#pragma unroll
-    for (int pp = 0; pp < 8; ++pp) {
-      if (pp < np) {
-        const float4 x = *reinterpret_cast<const float4*>(&m.nsm[pp * 256 + lane * 8]);
-        const float4 y = *reinterpret_cast<const float4*>(&m.nsm[pp * 256 + lane * 8 + 4]);
-        a[pp * 8 + 0] = x.x; a[pp * 8 + 1] = x.y; a[pp * 8 + 2] = x.z; a[pp * 8 + 3] = x.w;
-        a[pp * 8 + 4] = y.x; a[pp * 8 + 5] = y.y; a[pp * 8 + 6] = y.z; a[pp * 8 + 7] = y.w;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[pp * 8 + i] = 0.f;
-      }
-    }
-  }
-  // full-warp dot of one shared-memory row (np * 256 bf16 columns) with a
-  __device__ __forceinline__ float rdot(const uint8_t* row, int np, const float (&a)[64]) const {
-    uint4 w[8];
-#pragma unroll
-    for (int pp = 0; pp < 8; ++pp)
-      w[pp] = pp < np ? *reinterpret_cast<const uint4*>(row + (size_t)(pp * 256 + lane * 8) * 2) : make_uint4(0, 0, 0, 0);
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int pp = 0; pp < 8; ++pp) {
-      s0 = fmaf(bf_lo(w[pp].x), a[pp * 8 + 0], s0);
-      s1 = fmaf(bf_hi(w[pp].x), a[pp * 8 + 1], s1);
-      s0 = fmaf(bf_lo(w[pp].y), a[pp * 8 + 2], s0);
-      s1 = fmaf(bf_hi(w[pp].y), a[pp * 8 + 3], s1);
-      s0 = fmaf(bf_lo(w[pp].z), a[pp * 8 + 4], s0);
-      s1 = fmaf(bf_hi(w[pp].z), a[pp * 8 + 5], s1);
-      s0 = fmaf(bf_lo(w[pp].w), a[pp * 8 + 6], s0);
-      s1 = fmaf(bf_hi(w[pp].w), a[pp * 8 + 7], s1);
-    }
-    float s = s0 + s1;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    return s;
-  }
-
-  __device__ void op_router_r(const Task& t) {
-    const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
-    t_ready = gtimer();
-    float a[64];
-    rows_act(a);
-    const int np = p.H / 256;
-    const Geo g = geo_of(p.H);
-    for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS) {
-      const int rows = min(g.RS, t.a + t.b - r0);
-      const uint8_t* st = acquire();
-      if (!st) return;
-      for (int r = warp; r < rows; r += kConsumerWarps) {
-        const float s = rdot(st + (size_t)r * p.H * 2, np, a);
-        if (lane == 0) {
-          const int e = r0 + r;
-          const float bias = p.router_bias ? p.router_bias[(size_t)l * p.E + e] : 0.f;
-          __stcg(&p.rlogits[(size_t)l * p.E + e], s + bias);
-        }
-      }
-      release();
-    }
-    if (arrive_last_w0(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) publish_routing(l);
-  }
-
-  __device__ void op_qkv_r(const Task& t) {
-    const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
-    t_ready = gtimer();
-    float a[64];
-    rows_act(a);
-    const Geo g = geo_of(p.H);
-    const int np = p.H / 256, hd = p.d / 2;
-    const int pos = m.st_pos[0], page = m.st_page[0];
-    for (int u0 = t.a; u0 < t.a + t.b; u0 += g.RG) {
-      const int nu = min(g.RG, t.a + t.b - u0);
-      const uint8_t* st = acquire();
-      if (!st) return;
-      int item = 0;
-      for (int i = 0; i < nu; ++i) {
-        const QkvUnit q = qkv_unit(p, u0 + i);
-        const uint8_t* ub = st + (size_t)i * 8 * p.H * 2;
-        if (q.kind == 0) {  // q: 8 rows, stored before RoPE (attention rotates q when it loads it)
-          for (int tt = 0; tt < 8; ++tt, ++item) {
-            if (item % kConsumerWarps != warp) continue;
-            const float s = rdot(ub + (size_t)tt * p.H * 2, np, a);
-            if (lane == 0) __stcg(&p.q[((size_t)l * p.nq + q.head) * p.d + 4 * q.j + (tt & 3) + (tt >= 4 ? hd : 0)], s);
-          }
-        } else if (q.kind == 2) {  // v: 8 rows = 8 consecutive elements of v head q.head
-          for (int tt = 0; tt < 8; ++tt, ++item) {
-            if (item % kConsumerWarps != warp) continue;
-            const float s = rdot(ub + (size_t)tt * p.H * 2, np, a);
-            if (lane == 0) {
-              const int e = 8 * q.j + tt;
-              const uint16_t vb = f2bf(s);
-              __stcg(&p.vnew[((size_t)l * p.nkv + q.head) * p.d + e], bf2f(vb));
-              if (page >= 0)
-                p.vpool[((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d + e] = vb;
-            }
-          }
-        } else {  // k: RoPE pair (4 j + tt, 4 j + tt + d/2) from rows tt and tt + 4, for the cache
-          for (int tt = 0; tt < 4; ++tt, ++item) {
-            if (item % kConsumerWarps != warp) continue;
-            const float x0 = rdot(ub + (size_t)tt * p.H * 2, np, a);
-            const float x1 = rdot(ub + (size_t)(tt + 4) * p.H * 2, np, a);
-            if (lane == 0) {
-              const int pi2 = 4 * q.j + tt;
-              const float2 cs = m.st_rope[0][pi2];
-              const float lo = x0 * cs.x - x1 * cs.y;
-              const float hi = x0 * cs.y + x1 * cs.x;
-              {
-                const uint16_t kl = f2bf(lo), kh = f2bf(hi);
-                float* dst = p.knew + ((size_t)l * p.nkv + q.head) * p.d;
-                __stcg(dst + pi2, bf2f(kl));
-                __stcg(dst + pi2 + hd, bf2f(kh));
-                if (page >= 0) {
-                  uint16_t* kp = p.kpool + ((((size_t)l * p.num_pages + page) * p.nkv + q.head) * kPage + pos % kPage) * p.d;
-                  kp[pi2] = kl;
-                  kp[pi2 + hd] = kh;
-                }
-              }
-            }
-          }
-        }
-      }
-      release();
-    }
-    if (page < 0 && threadIdx.x == 0) report(p, MK_ERR_BAD_PAGE, 0, pos);
-    release_counter(cm.qkv(l, t.c));
-  }
-
-  __device__ void op_gu_r(const Task& t) {
-    const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok || !load_route(l)) return;
-    t_ready = gtimer();
-    float a[64];
-    rows_act(a);
-    const int na = m.rc_n, maxa = max_active(p);
-    const Geo g = geo_of(p.H);
-    const int np = p.H / 256;
-    for (int u = t.a; u < t.a + t.b; ++u) {
-      const int ar = u % maxa, tile = u / maxa;
-      if (ar >= na) continue;
-      const uint8_t* st = acquire();
-      if (!st) return;
-      for (int rr = warp; rr < g.RS; rr += kConsumerWarps) {
-        const float s = rdot(st + (size_t)rr * p.H * 2, np, a);
-        if (lane == 0) __stcg(&p.h[h_index(l, ar, 0) + tile * g.RS + rr], s);
-      }
-      release();
-    }
-    release_counter(cm.gu(l));
-  }
-
-  __device__ void op_lm_r(const Task& t) {
-    ensure_norm(p.L, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
-    t_ready = gtimer();
-    float a[64];
-    rows_act(a);
-    const int np = p.H / 256;
-    const Geo g = geo_of(p.H);
-    for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS) {
-      const int rows = min(g.RS, t.a + t.b - r0);
-      const uint8_t* st = acquire();
-      if (!st) return;
-      for (int r = warp; r < rows; r += kConsumerWarps) {  // ascending rows per warp
-        const float s = rdot(st + (size_t)r * p.H * 2, np, a);
-        if (lane == 0) {
-          const int v = r0 + r;
-          if (p.logits) __stcg(&p.logits[v], s);
-          if (s > lm_best[0] || (s == lm_best[0] && v < lm_idx[0])) { lm_best[0] = s; lm_idx[0] = v; }
-        }
-      }
-      release();
-    }
-    if (!(t.flags & TF_LAST_LM)) return;
-    if (lane == 0) { m.lmw_v[warp] = lm_best[0]; m.lmw_i[warp] = lm_idx[0]; }
-    if (!csync()) return;
-    if (threadIdx.x == 0) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int w = 0; w < kConsumerWarps; ++w)
-        if (m.lmw_v[w] > bv || (m.lmw_v[w] == bv && m.lmw_i[w] < bi)) { bv = m.lmw_v[w]; bi = m.lmw_i[w]; }
-      __stcg(&p.lm_best_v[t.c * kMaxB], bv);
-      __stcg(&p.lm_best_i[t.c * kMaxB], bi);
-    }
-    if (!arrive_last(cm.lm_arrive(), p.n_lm_sm)) return;
-    if (threadIdx.x == 0) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int s = 0; s < p.n_lm_sm; ++s) {
-        const float v = __ldcg(&p.lm_best_v[s * kMaxB]);
-        const int i = __ldcg(&p.lm_best_i[s * kMaxB]);
-        if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
-      }
-      if (p.argmax_out) p.argmax_out[0] = bi;
     }
   }
 
@@ -1603,7 +1512,7 @@ struct Consumer {
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) m.res[warp] = s * qscale;
+      if (lane == 0) m.red[2][0][warp] = s * qscale;
     }
     if (!csync()) return;
     const float* vn = p.vnew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
@@ -1621,7 +1530,7 @@ struct Consumer {
       if (!csync()) return;
       if (threadIdx.x < p.group) {
         const int h = threadIdx.x;
-        const float sn = m.res[h];
+        const float sn = m.red[2][0][h];
         float M = sn;
         for (int c = 0; c < nch; ++c) M = fmaxf(M, sm_m[c * 8 + h]);
         const float fn = exp2f(sn - M);
@@ -1632,14 +1541,14 @@ struct Consumer {
           L += sm_l[c * 8 + h] * f;
           sm_m[c * 8 + h] = f;
         }
-        m.res[8 + h] = fn;
-        m.res[16 + h] = 1.0f / L;
+        m.red[2][0][8 + h] = fn;
+        m.red[2][0][16 + h] = 1.0f / L;
       }
       if (!csync()) return;
       for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
         const int h = i / p.d, dd = i % p.d;
         const float* src = pbase + 16 + h * p.d + dd;
-        float O = m.res[8 + h] * __ldcg(vn + dd);
+        float O = m.red[2][0][8 + h] * __ldcg(vn + dd);
         int c = 0;
         for (; c + 8 <= nch; c += 8) {
           float v[8];
@@ -1649,12 +1558,12 @@ struct Consumer {
           for (int j = 0; j < 8; ++j) O = fmaf(v[j], sm_m[(c + j) * 8 + h], O);
         }
         for (; c < nch; ++c) O = fmaf(__ldcg(src + (size_t)c * cstride), sm_m[c * 8 + h], O);
-        __stcg(&p.attn_o[((size_t)l * p.B + b) * p.od + (g * p.group + h) * p.d + dd], O * m.res[16 + h]);
+        store_attn(l, b, (g * p.group + h) * p.d + dd, O * m.red[2][0][16 + h]);
       }
     } else {
       for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
         const int h = i / p.d, dd = i % p.d;
-        const float sn = m.res[h];
+        const float sn = m.red[2][0][h];
         float M = sn;
         for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(pbase + (size_t)c * cstride + h));
         float fn = exp2f(sn - M);
@@ -1667,7 +1576,7 @@ struct Consumer {
           L += __ldcg(src + 8 + h) * f;
           O += __ldcg(src + 16 + h * p.d + dd) * f;
         }
-        __stcg(&p.attn_o[((size_t)l * p.B + b) * p.od + (g * p.group + h) * p.d + dd], O / L);
+        store_attn(l, b, (g * p.group + h) * p.d + dd, O / L);
       }
     }
     release_counter(cm.attn(l, g));
@@ -1676,26 +1585,20 @@ struct Consumer {
   __device__ void run_task(const Task& t) {
     t_start = gtimer();
     t_ready = t_start;
-    if constexpr (NB == 1) {
-      switch (t.op) {
-        case OP_ROUTER: op_router_r(t); break;
-        case OP_QKV: op_qkv_r(t); break;
-        case OP_ATTN: op_attn(t); break;
-        case OP_GU: op_gu_r(t); break;
-        case OP_O: op_o(t); break;
-        case OP_DOWN: op_down(t); break;
-        case OP_LM: op_lm_r(t); break;
-      }
-    } else {
-      switch (t.op) {
-        case OP_ROUTER: op_router(t); break;
-        case OP_QKV: op_qkv(t); break;
-        case OP_ATTN: op_attn(t); break;
-        case OP_GU: op_gu(t); break;
-        case OP_O: op_o(t); break;
-        case OP_DOWN: op_down(t); break;
-        case OP_LM: op_lm(t); break;
-      }
+    // ops that read the normalized input of their layer (the final norm for the LM head) get it
+    // here, at one call site
+    if (t.op == OP_ROUTER || t.op == OP_QKV || t.op == OP_GU || t.op == OP_LM) {
+      ensure_norm(t.op == OP_LM ? p.L : (int)t.layer, (t.flags & TF_WRITE_X) != 0);
+      if (!ok) return;
+    }
+    switch (t.op) {
+      case OP_ROUTER: op_router(t); break;
+      case OP_QKV: op_qkv(t); break;
+      case OP_ATTN: op_attn(t); break;
+      case OP_GU: op_gu(t); break;
+      case OP_O: op_o(t); break;
+      case OP_DOWN: op_down(t); break;
+      case OP_LM: op_lm(t); break;
     }
     if (ok) trace_task(p, t, t_start, t_ready ? t_ready : t_start);
   }
@@ -1715,6 +1618,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
       mbar_init(smem_addr(&misc.empty[s]), kConsumerWarps);
     }
     mbar_init(smem_addr(&misc.cbar), kConsumerWarps);
+    for (int i = 0; i < kRedBufs; ++i) {
+      mbar_init(smem_addr(&misc.gpart[i]), kConsumerWarps);
+      mbar_init(smem_addr(&misc.gfree[i]), 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -1728,7 +1635,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
 
   if (threadIdx.x / 32 >= kConsumerWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    if (threadIdx.x != kConsumerWarps * 32) return;
+    if (threadIdx.x / 32 != kConsumerWarps) return;
     Producer pr(p, tm, misc, ring);
     // descriptors in a 4-deep register queue, refilled as tasks are taken (one call site, so
     // the task code is inlined once)
@@ -1745,7 +1652,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
       q2 = q3;
       q3 = nx;
     }
-    pr.drain();  // never leave while a copy into this CTA's shared memory is in flight
+    if ((threadIdx.x & 31) == 0) pr.drain();  // never leave while a copy into shared memory is in flight
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
