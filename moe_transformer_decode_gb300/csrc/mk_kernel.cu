@@ -287,6 +287,7 @@ struct Misc {
   float norm[kConsumerWarps][kMaxB]; // sum of squares partials
   int flag;
   // routing scratch of the warp that computes a layer's routing
+  uint32_t em[kMaxExperts];  // bit b: token b picked the expert
   int ids[kMaxB][kMaxK];
   float wk[kMaxB][kMaxK];
   // per step (consumers): new token's position, page of its KV slot (-1 if invalid), RoPE at it,
@@ -338,6 +339,7 @@ struct Producer {
   __device__ Producer(const Params& p_, const TensorMaps& tm_, Misc& m_, Ring r_)
       : p(p_), tm(tm_), m(m_), r(r_), ok(true), route_layer(-1) {
     pol = policy_evict_first();
+#pragma unroll 1
     for (int b = 0; b < kMaxB; ++b) {
       pos[b] = b < p.B ? pos_of(p, b) : 0;
       cpp[b] = b < p.B ? p.chunk_pages[b] : 1;
@@ -351,6 +353,7 @@ struct Producer {
     if (!wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l))) return false;
     const Route* rt = p.route + l;
     const int na = __ldcg(&rt->n_active);
+#pragma unroll 1
     for (int a = 0; a < na; ++a) m.pr_expert[a] = __ldcg(&rt->expert[a]);
     m.pr_n = na;
     route_layer = l;
@@ -383,6 +386,7 @@ struct Producer {
       case OP_LM: {
         const Geo g = geo_of(p.H);
         const uint16_t* W = t.op == OP_ROUTER ? p.w_router + (size_t)l * p.E * p.H : p.lm_head;
+#pragma unroll 1
         for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS)
           if (!gemv_rows(W + (size_t)r0 * p.H, min(g.RS, t.a + t.b - r0), p.H * 2)) return false;
         return true;
@@ -391,9 +395,11 @@ struct Producer {
         const Geo g = geo_of(p.H);
         const int us = g.RG;  // units per stage
         const uint16_t* W = p.w_qkv + (size_t)l * p.qkv_rows * p.H;
+#pragma unroll 1
         for (int u0 = t.a; u0 < t.a + t.b; u0 += us) {
           const int nu = min(us, t.a + t.b - u0);
           if (!begin((uint32_t)nu * 8 * p.H * 2)) return false;
+#pragma unroll 1
           for (int i = 0; i < nu; ++i) {
             const QkvUnit q = qkv_unit(p, u0 + i);
             const uint32_t d0 = dst + (uint32_t)i * 8 * p.H * 2;
@@ -413,8 +419,10 @@ struct Producer {
         const AttnRange ar = attn_range(pos[b], cpp[b], nch[b], t.c);
         const int pps = attn_pps(p), halves = p.d / 64;
         int ids[64];  // page ids of up to 64 pages, loaded together (one round trip per 64 pages)
+#pragma unroll 1
         for (int base = ar.cp0; base < ar.cp1; base += 64) {
           const int nb = min(64, ar.cp1 - base);
+#pragma unroll 1
           for (int i0 = 0; i0 < nb; i0 += 8) {
             int v[8];
 #pragma unroll
@@ -426,21 +434,26 @@ struct Producer {
             for (int j = 0; j < 8; ++j)
               if (i0 + j < nb) ids[i0 + j] = v[j];
           }
+#pragma unroll 1
           for (int i = 0; i < nb; ++i)
             if (ids[i] < 0 || ids[i] >= p.num_pages) {
               report(p, MK_ERR_BAD_PAGE, b, base + i);
               ids[i] = -1;
             }
+#pragma unroll 1
           for (int s0 = 0; s0 < nb; s0 += pps) {
             const int np = min(pps, nb - s0);
             int good = 0;
+#pragma unroll 1
             for (int i = 0; i < np; ++i) good += ids[s0 + i] >= 0;
             if (!begin((uint32_t)good * 2 * halves * 2048)) return false;
+#pragma unroll 1
             for (int i = 0; i < np; ++i) {
               const int id = ids[s0 + i];
               if (id < 0) continue;
               const int row = ((l * p.num_pages + id) * p.nkv + g) * kPage;
               const uint32_t pb = dst + (uint32_t)i * 4096 * halves;
+#pragma unroll 1
               for (int h = 0; h < halves; ++h) {
                 tma_2d_g2s(pb + h * 2048, &tm.k, h * 64, row, bar, pol);
                 tma_2d_g2s(pb + (halves + h) * 2048, &tm.v, h * 64, row, bar, pol);
@@ -455,6 +468,7 @@ struct Producer {
         if (!route(l)) return false;
         const int na = m.pr_n, maxa = max_active(p);
         const Geo g = geo_of(p.H);
+#pragma unroll 1
         for (int u = t.a; u < t.a + t.b; ++u) {
           const int a = u % maxa, tile = u / maxa;
           if (a >= na) continue;
@@ -469,11 +483,13 @@ struct Producer {
       case OP_O: {
         const Geo g = geo_of(p.od);
         const uint16_t* W = p.w_o + ((size_t)l * p.H + t.a) * p.od;
+#pragma unroll 1
         for (int cs = 0; cs < g.NCS; ++cs) {
           if (g.NCS == 1) {
             if (!gemv_rows(W, t.b, p.od * 2)) return false;
           } else {
             if (!begin((uint32_t)t.b * g.KS * 2)) return false;
+#pragma unroll 1
             for (int r = 0; r < t.b; ++r)
               bulk_g2s(dst + (uint32_t)r * g.KS * 2, W + (size_t)r * p.od + cs * g.KS, g.KS * 2, bar, pol);
             end();
@@ -484,6 +500,7 @@ struct Producer {
       case OP_DOWN: {
         if (!route(l)) return false;
         const int na = m.pr_n;
+#pragma unroll 1
         for (int a = 0; a < na; ++a) {
           const int e = m.pr_expert[a];
           const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + t.a) * p.I;
@@ -892,8 +909,6 @@ struct Consumer {
 
   __device__ void op_router(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     const Geo g = geo_of(p.H);
     for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
@@ -970,20 +985,31 @@ struct Consumer {
       if (lane < K) m.wk[b][lane] /= z;
     }
     __syncwarp();
+    // token masks per expert, then the distinct experts in ascending id (32 per round)
+#pragma unroll 1
+    for (int e = lane; e < E; e += 32) m.em[e] = 0u;
+    __syncwarp();
+#pragma unroll 1
+    for (int i = lane; i < B * K; i += 32) atomicOr(&m.em[m.ids[i / K][i % K]], 1u << (i / K));
+    __syncwarp();
     Route* rt = p.route + l;
     int na = 0;
-#pragma unroll
-    for (int i = 0; i < NE; ++i) {
-      const uint32_t act = __ballot_sync(0xffffffffu, emask[i] != 0u);
-      if (emask[i] != 0u) {
-        const int e = lane + 32 * i;
+#pragma unroll 1
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const uint32_t mask = e < E ? m.em[e] : 0u;
+      const uint32_t act = __ballot_sync(0xffffffffu, mask != 0u);
+      if (mask != 0u) {
         const int r = na + __popc(act & ((1u << lane) - 1u));
         __stcg(&rt->expert[r], e);
-        __stcg(&rt->mask[r], emask[i]);
+        __stcg(&rt->mask[r], mask);
+#pragma unroll 1
         for (int b = 0; b < kMaxB; ++b) {
           float w = 0.f;
-          if (emask[i] & (1u << b))
+          if (mask & (1u << b)) {
+#pragma unroll 1
             for (int j = 0; j < K; ++j) w = m.ids[b][j] == e ? m.wk[b][j] : w;
+          }
           __stcg(&rt->w[r][b], w);
         }
       }
@@ -1003,8 +1029,6 @@ struct Consumer {
 
   __device__ void op_qkv(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     const Geo g = geo_of(p.H);
     const int hd = p.d / 2;
@@ -1059,8 +1083,6 @@ struct Consumer {
 
   __device__ void op_gu(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     if (!load_route(l)) return;
     t_ready = gtimer();
     const int na = m.rc_n, maxa = max_active(p);
@@ -1161,8 +1183,6 @@ struct Consumer {
   }
 
   __device__ void op_lm(const Task& t) {
-    ensure_norm(p.L, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     const Geo g = geo_of(p.H);
     for (int r0 = t.a; r0 < t.a + t.b && ok; r0 += g.RS) {
@@ -1253,8 +1273,6 @@ struct Consumer {
 
   __device__ void op_router_r(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     float a[64];
     rows_act(a);
@@ -1279,8 +1297,6 @@ struct Consumer {
 
   __device__ void op_qkv_r(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     float a[64];
     rows_act(a);
@@ -1346,8 +1362,7 @@ struct Consumer {
 
   __device__ void op_gu_r(const Task& t) {
     const int l = t.layer;
-    ensure_norm(l, (t.flags & TF_WRITE_X) != 0);
-    if (!ok || !load_route(l)) return;
+    if (!load_route(l)) return;
     t_ready = gtimer();
     float a[64];
     rows_act(a);
@@ -1369,8 +1384,6 @@ struct Consumer {
   }
 
   __device__ void op_lm_r(const Task& t) {
-    ensure_norm(p.L, (t.flags & TF_WRITE_X) != 0);
-    if (!ok) return;
     t_ready = gtimer();
     float a[64];
     rows_act(a);
@@ -1676,6 +1689,12 @@ struct Consumer {
   __device__ void run_task(const Task& t) {
     t_start = gtimer();
     t_ready = t_start;
+    // ops that read the normalized input of their layer (the final norm for the LM head) get it
+    // here, at one call site
+    if (t.op == OP_ROUTER || t.op == OP_QKV || t.op == OP_GU || t.op == OP_LM) {
+      ensure_norm(t.op == OP_LM ? p.L : (int)t.layer, (t.flags & TF_WRITE_X) != 0);
+      if (!ok) return;
+    }
     if constexpr (NB == 1) {
       switch (t.op) {
         case OP_ROUTER: op_router_r(t); break;
