@@ -164,14 +164,13 @@ struct WaitClock {
       t0 = gtimer();
       return true;
     }
-    if (now < next_poll) return true;
-    next_poll = now + kAbortPollCycles;
-    if (aborted(p)) return false;
     if ((long long)(gtimer() - t0) > p.timeout_ns) {
       report(p, MK_ERR_DEVICE_TIMEOUT, idx, aux);
       return false;
     }
-    return true;
+    if (now < next_poll) return true;
+    next_poll = now + kAbortPollCycles;
+    return !aborted(p);
   }
 };
 
@@ -443,15 +442,13 @@ struct Producer {
 #pragma unroll 1
           for (int s0 = 0; s0 < nb; s0 += pps) {
             const int np = min(pps, nb - s0);
-            int good = 0;
-#pragma unroll 1
-            for (int i = 0; i < np; ++i) good += ids[s0 + i] >= 0;
-            if (!begin((uint32_t)good * 2 * halves * 2048)) return false;
+            if (!begin((uint32_t)np * 2 * halves * 2048)) return false;
 #pragma unroll 1
             for (int i = 0; i < np; ++i) {
+              // an invalid page (reported above) is loaded as zeros: a tile load at an
+              // out-of-range row fills the box, so the stage never holds stale bytes
               const int id = ids[s0 + i];
-              if (id < 0) continue;
-              const int row = ((l * p.num_pages + id) * p.nkv + g) * kPage;
+              const int row = id >= 0 ? ((l * p.num_pages + id) * p.nkv + g) * kPage : -kPage;
               const uint32_t pb = dst + (uint32_t)i * 4096 * halves;
 #pragma unroll 1
               for (int h = 0; h < halves; ++h) {
@@ -512,7 +509,9 @@ struct Producer {
     return true;
   }
 
-  // Abort path: wait (bounded) until every copy this warp issued has landed.
+  // Abort path: wait until every copy this warp issued has landed. Bounded, but by its own
+  // limit (1 s), not the caller's wait limit: a copy in flight completes in microseconds, and
+  // the block must not leave while one still writes its shared memory.
   __device__ void drain() {
     const uint32_t n = r.it < (uint32_t)kStages ? r.it : (uint32_t)kStages;
     for (uint32_t k = 0; k < n; ++k) {
@@ -520,7 +519,7 @@ struct Producer {
       const uint32_t s = it % kStages, parity = (it / kStages) & 1u;
       const uint64_t t0 = gtimer();
       while (!mbar_try_wait(r.full + 8 * s, parity)) {
-        if ((long long)(gtimer() - t0) > p.timeout_ns) break;
+        if (gtimer() - t0 > 1000000000ull) break;
       }
     }
   }
@@ -950,7 +949,8 @@ struct Consumer {
 #pragma unroll
       for (int i = 0; i < NE; ++i) {
         const int e = lane + 32 * i;
-        v[b][i] = (b < B && e < E) ? __ldcg(&p.rlogits[((size_t)l * B + b) * E + e]) : -INFINITY;
+        const float x = (b < B && e < E) ? __ldcg(&p.rlogits[((size_t)l * B + b) * E + e]) : -INFINITY;
+        v[b][i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
       }
     uint32_t emask[NE];
 #pragma unroll
@@ -959,13 +959,15 @@ struct Consumer {
     for (int b = 0; b < NB; ++b) {
       if (b >= B) break;
       float top0 = 0.f, z = 0.f;
+      uint32_t taken = 0u;  // bit i: expert lane + 32 i already picked for token b
       for (int j = 0; j < K; ++j) {
+        // every pick is a valid, distinct expert: -inf ties go to the lowest free id
         float bv = -INFINITY;
         int be = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < NE; ++i) {
           const int e = lane + 32 * i;
-          if (e < E && (v[b][i] > bv || (v[b][i] == bv && e < be))) { bv = v[b][i]; be = e; }
+          if (e < E && !((taken >> i) & 1u) && (v[b][i] > bv || (v[b][i] == bv && e < be))) { bv = v[b][i]; be = e; }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -975,7 +977,7 @@ struct Consumer {
         }
 #pragma unroll
         for (int i = 0; i < NE; ++i)
-          if (lane + 32 * i == be) { v[b][i] = -INFINITY; emask[i] |= 1u << b; }
+          if (lane + 32 * i == be) { taken |= 1u << i; emask[i] |= 1u << b; }
         if (j == 0) top0 = bv;
         const float w = expf(bv - top0);
         z += w;
