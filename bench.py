@@ -162,7 +162,8 @@ def run_reference(args, w, rank):
     if timed > 1:
         per_step = oracle_sample(w, tokens, ctx, timed)
     value = w.B / per_step
-    cores = os.cpu_count()
+    import oracle
+    cores = oracle.threads()
     sample = (f"{timed} oracle decode step(s) of {w.name} (batch {w.B}) at the prefill position after one warm-up "
               f"step that synthesises and caches the weights it touches; KV values synthesised on read")
     line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "tok/s", "n_gpus": args.gpus,
@@ -319,7 +320,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tokens = W.first_tokens(w)
         sec = oracle_sample(w, tokens, np.asarray(ctx, np.int32), 1)
-        line["cpu_baseline"] = {"value": w.B / sec, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+        import oracle
+        line["cpu_baseline"] = {"value": w.B / sec, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
                                 "sample": f"1 oracle decode step of {w.name} after one warm-up step that "
                                           f"synthesises and caches the weights it touches"}
     if rank == 0:
