@@ -15,6 +15,7 @@ speed-of-light, the CPU oracle's throughput on a bounded sample, and the clocks 
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -91,6 +92,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) per launch of the decode kernel from the committed ncu capture,
+    if it was taken on this workload and on the kernel source as it stands; else None."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    try:
+        rec = json.load(open(os.path.join(here, "profiles", "mk_decode_kernel_traffic.json")))
+        h = hashlib.sha256()
+        for f in ("mk_kernel.cu", "mk_internal.h"):
+            h.update(open(os.path.join(here, "moe_transformer_decode_gb300", "csrc", f), "rb").read())
+    except (OSError, ValueError):
+        return None
+    if rec.get("workload") != workload or rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+
+
 def setup_gpu(w, capacity, device):
     import torch
 
@@ -145,7 +162,8 @@ def run_reference(args, w, rank):
     if timed > 1:
         per_step = oracle_sample(w, tokens, ctx, timed)
     value = w.B / per_step
-    cores = os.cpu_count()
+    import oracle
+    cores = oracle.threads()
     sample = (f"{timed} oracle decode step(s) of {w.name} (batch {w.B}) at the prefill position after one warm-up "
               f"step that synthesises and caches the weights it touches; KV values synthesised on read")
     line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "tok/s", "n_gpus": args.gpus,
@@ -289,7 +307,7 @@ def main():
                    "l2": "inputs larger than L2: each step streams its weights and KV once (GBs vs 129 MB of L2)"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / hbm_gbs, "traffic": measured_traffic(w.name), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": bytes_per_step / launches_per_step,
                      "distinct_experts_per_layer": float(np.mean(de))},
         "sol": {"bytes_per_step": bytes_per_step, "frac_of_nominal_8tbs": bytes_per_step / (ms_step * 1e-3) / 8.0e12,
@@ -302,7 +320,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tokens = W.first_tokens(w)
         sec = oracle_sample(w, tokens, np.asarray(ctx, np.int32), 1)
-        line["cpu_baseline"] = {"value": w.B / sec, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+        import oracle
+        line["cpu_baseline"] = {"value": w.B / sec, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
                                 "sample": f"1 oracle decode step of {w.name} after one warm-up step that "
                                           f"synthesises and caches the weights it touches"}
     if rank == 0:

@@ -134,6 +134,13 @@ const char* mk_last_error(const mk_ctx* ctx);
 #define MK_MODE_PER_OP 1
 mk_status mk_set_mode(mk_ctx* ctx, int mode);
 
+/* Time limit of every device-side wait of a step (a dependency counter, a ring slot, the
+ * blocks' own barrier), in nanoseconds; default 2e9 (2 s), accepted range [1e3, 6e10]. A
+ * wait that runs out latches MK_ERR_DEVICE_TIMEOUT and every block of the step leaves
+ * early, its copies in flight drained (the error is returned by mk_status_sync, which
+ * also resets the counters so the context stays usable). Errors: MK_ERR_INVALID_ARG. */
+mk_status mk_set_wait_limit(mk_ctx* ctx, int64_t ns);
+
 /* Per-task trace: when dev_buf is non-NULL, each step records one 32-byte entry per task
  * (mk_trace_entry) into dev_buf (device memory, caller-owned, `bytes` long; entries past
  * the end are dropped). The first 16 bytes of dev_buf hold the entry count (uint64) and

@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_UNSUPPORTED", 3:
 MK_MODE_MEGAKERNEL, MK_MODE_PER_OP = 0, 1
 
 EXPORTS = ["mk_create", "mk_plan_schedule", "mk_build_schedule", "mk_decode_step", "mk_decode_greedy", "mk_status_sync", "mk_last_error",
-           "mk_set_mode", "mk_enable_trace", "mk_get_activations", "mk_get_launch_info", "mk_decode_step_noalloc", "mk_destroy"]
+           "mk_set_mode", "mk_set_wait_limit", "mk_enable_trace", "mk_get_activations", "mk_get_launch_info", "mk_decode_step_noalloc", "mk_destroy"]
 
 
 class mk_model_cfg(ctypes.Structure):
@@ -89,6 +89,8 @@ def lib():
         L.mk_last_error.argtypes = [vp]
         L.mk_set_mode.restype = ctypes.c_int
         L.mk_set_mode.argtypes = [vp, ctypes.c_int]
+        L.mk_set_wait_limit.restype = ctypes.c_int
+        L.mk_set_wait_limit.argtypes = [vp, ctypes.c_int64]
         L.mk_enable_trace.restype = ctypes.c_int
         L.mk_enable_trace.argtypes = [vp, vp, ctypes.c_size_t]
         L.mk_get_activations.restype = ctypes.c_int
@@ -168,6 +170,10 @@ def mk_last_error(ctx) -> str:
 
 def mk_set_mode(ctx, mode: int) -> None:
     _check(ctx, lib().mk_set_mode(ctx, mode))
+
+
+def mk_set_wait_limit(ctx, ns: int) -> None:
+    _check(ctx, lib().mk_set_wait_limit(ctx, ns))
 
 
 def mk_enable_trace(ctx, buf) -> None:

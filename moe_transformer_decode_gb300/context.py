@@ -85,6 +85,9 @@ class DecodeContext:
     def set_mode(self, mode):
         B.mk_set_mode(self.ctx, mode)
 
+    def set_wait_limit(self, ns: int):
+        B.mk_set_wait_limit(self.ctx, int(ns))
+
     def launch_info(self):
         return B.mk_get_launch_info(self.ctx)
 

@@ -40,6 +40,7 @@ struct mk_ctx {
   mk_weight_ptrs w;
   int device, n_sm;
   int mode;
+  long long wait_ns = 2000000000LL;  // device-side wait limit
   std::string err;
   // workspace (device)
   float *xs, *q, *knew, *vnew, *attn_o, *attn_out, *rlogits, *moe_out, *apart, *lm_best_v;
@@ -599,7 +600,7 @@ static Params make_params(mk_ctx* c, const int32_t* tokens, const int32_t* posit
   p.group = m.n_q_heads / m.n_kv_heads; p.max_chunks = c->max_chunks; p.n_lm_sm = c->n_lm_sm; p.max_pos = c->max_pos;
   p.eps = m.rms_eps;
   p.pos_offset = pos_offset;
-  p.timeout_ns = 2000000000LL;
+  p.timeout_ns = c->wait_ns;
   p.embed = (const uint16_t*)c->w.embed; p.norm_gain = (const uint16_t*)c->w.norm_gain;
   p.w_qkv = (const uint16_t*)c->w.w_qkv; p.w_o = (const uint16_t*)c->w.w_o; p.w_router = (const uint16_t*)c->w.w_router;
   p.w_gate_up = (const uint16_t*)c->w.w_gate_up; p.w_down = (const uint16_t*)c->w.w_down;
@@ -684,8 +685,12 @@ extern "C" mk_status mk_status_sync(mk_ctx* c) {
   e = cudaMemcpy(st, c->status, sizeof(st), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(c, e, "status copy");
   if (st[ST_CODE] == 0) return MK_OK;
-  char buf[160];
-  snprintf(buf, sizeof(buf), "device error %d (aux %d, %d)", st[ST_CODE], st[ST_AUX0], st[ST_AUX1]);
+  char buf[200];
+  const char* what = st[ST_CODE] == MK_ERR_BAD_PAGE        ? "page id out of range (sequence, page index)"
+                     : st[ST_CODE] == MK_ERR_DEVICE_TIMEOUT ? "a device-side wait ran out of time (wait, progress)"
+                     : st[ST_CODE] == MK_ERR_BAD_TOKEN      ? "token id out of range (sequence, token)"
+                                                            : "device error";
+  snprintf(buf, sizeof(buf), "device error %d: %s = (%d, %d)", st[ST_CODE], what, st[ST_AUX0], st[ST_AUX1]);
   c->err = buf;
   cudaMemset(c->status, 0, ST_WORDS * sizeof(int32_t));
   *(volatile int32_t*)c->status_host = 0;
@@ -700,6 +705,12 @@ extern "C" const char* mk_last_error(const mk_ctx* c) { return c ? c->err.c_str(
 extern "C" mk_status mk_set_mode(mk_ctx* c, int mode) {
   if (!c || (mode != MK_MODE_MEGAKERNEL && mode != MK_MODE_PER_OP)) return MK_ERR_INVALID_ARG;
   c->mode = mode;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_set_wait_limit(mk_ctx* c, int64_t ns) {
+  if (!c || ns < 1000 || ns > 60000000000LL) return MK_ERR_INVALID_ARG;
+  c->wait_ns = ns;
   return MK_OK;
 }
 

@@ -164,14 +164,13 @@ struct WaitClock {
       t0 = gtimer();
       return true;
     }
-    if (now < next_poll) return true;
-    next_poll = now + kAbortPollCycles;
-    if (aborted(p)) return false;
     if ((long long)(gtimer() - t0) > p.timeout_ns) {
       report(p, MK_ERR_DEVICE_TIMEOUT, idx, aux);
       return false;
     }
-    return true;
+    if (now < next_poll) return true;
+    next_poll = now + kAbortPollCycles;
+    return !aborted(p);
   }
 };
 
@@ -468,18 +467,17 @@ struct Producer {
           const int np = min(pps, ar.cp1 - s0);
           if (!(id_b == b && s0 >= id_p0 && s0 + np <= id_p0 + id_n)) fill_ids(b, s0, min(kIdCache, ar.cp1 - s0));
           const int* ids = m.pr_ids + (s0 - id_p0);
-          const int good = __popc(__ballot_sync(0xffffffffu, lane < np && ids[lane < np ? lane : 0] >= 0));
-          if (!begin((uint32_t)good * 2 * halves * 2048)) return false;
-          // copy j: page j / (2 halves), K (0) or V (1), half h
+          if (!begin((uint32_t)np * 2 * halves * 2048)) return false;
+          // copy j: page j / (2 halves), K (0) or V (1), half h. An invalid page (reported when
+          // its id was read) loads as zeros: a tile load at an out-of-range row fills the box,
+          // so the stage never holds stale bytes.
           const int per = 2 * halves;
           if (lane < np * per) {
             const int i = lane / per, kv = (lane / halves) & 1, h = lane % halves;
             const int id = ids[i];
-            if (id >= 0) {
-              const int row = ((l * p.num_pages + id) * p.nkv + g) * kPage;
-              const uint32_t pb = dst + (uint32_t)i * 4096 * halves + (uint32_t)(kv * halves + h) * 2048;
-              tma_2d_g2s(pb, kv ? &tm.v : &tm.k, h * 64, row, bar, pol);
-            }
+            const int row = id >= 0 ? ((l * p.num_pages + id) * p.nkv + g) * kPage : -kPage;
+            const uint32_t pb = dst + (uint32_t)i * 4096 * halves + (uint32_t)(kv * halves + h) * 2048;
+            tma_2d_g2s(pb, kv ? &tm.v : &tm.k, h * 64, row, bar, pol);
           }
           end();
         }
@@ -531,7 +529,9 @@ struct Producer {
     return true;
   }
 
-  // Abort path: wait (bounded) until every copy this warp issued has landed.
+  // Abort path: wait until every copy this warp issued has landed. Bounded, but by its own
+  // limit (1 s), not the caller's wait limit: a copy in flight completes in microseconds, and
+  // the block must not leave while one still writes its shared memory.
   __device__ void drain() {
     const uint32_t n = r.it < (uint32_t)kStages ? r.it : (uint32_t)kStages;
     for (uint32_t k = 0; k < n; ++k) {
@@ -539,7 +539,7 @@ struct Producer {
       const uint32_t s = it % kStages, parity = (it / kStages) & 1u;
       const uint64_t t0 = gtimer();
       while (!mbar_try_wait(r.full + 8 * s, parity)) {
-        if ((long long)(gtimer() - t0) > p.timeout_ns) break;
+        if (gtimer() - t0 > 1000000000ull) break;
       }
     }
   }
@@ -1022,7 +1022,8 @@ struct Consumer {
 #pragma unroll
       for (int i = 0; i < NE; ++i) {
         const int e = lane + 32 * i;
-        v[b][i] = (b < B && e < E) ? __ldcg(&p.rlogits[((size_t)l * B + b) * E + e]) : -INFINITY;
+        const float x = (b < B && e < E) ? __ldcg(&p.rlogits[((size_t)l * B + b) * E + e]) : -INFINITY;
+        v[b][i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
       }
     uint32_t emask[NE];
 #pragma unroll
@@ -1031,13 +1032,15 @@ struct Consumer {
     for (int b = 0; b < NB; ++b) {
       if (b >= B) break;
       float top0 = 0.f, z = 0.f;
+      uint32_t taken = 0u;  // bit i: expert lane + 32 i already picked for token b
       for (int j = 0; j < K; ++j) {
+        // every pick is a valid, distinct expert: -inf ties go to the lowest free id
         float bv = -INFINITY;
         int be = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < NE; ++i) {
           const int e = lane + 32 * i;
-          if (e < E && (v[b][i] > bv || (v[b][i] == bv && e < be))) { bv = v[b][i]; be = e; }
+          if (e < E && !((taken >> i) & 1u) && (v[b][i] > bv || (v[b][i] == bv && e < be))) { bv = v[b][i]; be = e; }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -1047,7 +1050,7 @@ struct Consumer {
         }
 #pragma unroll
         for (int i = 0; i < NE; ++i)
-          if (lane + 32 * i == be) { v[b][i] = -INFINITY; emask[i] |= 1u << b; }
+          if (lane + 32 * i == be) { taken |= 1u << i; emask[i] |= 1u << b; }
         if (j == 0) top0 = bv;
         const float w = expf(bv - top0);
         z += w;

@@ -46,6 +46,8 @@ def lib():
     if _lib is None:
         L = ctypes.CDLL(_build.build())
         vp, i32, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_double
+        L.orc_threads.restype = ctypes.c_int
+        L.orc_threads.argtypes = []
         L.orc_decode_step.restype = ctypes.c_int
         L.orc_decode_step.argtypes = [ctypes.POINTER(OrcCfg), ctypes.POINTER(OrcSource), ctypes.c_int, vp, vp, vp, vp,
                                       ctypes.POINTER(OrcTrace)]
@@ -138,6 +140,11 @@ class SynthSource:
         if getattr(self, "h", None):
             lib().orc_synth_source_destroy(self.h)
             self.h = None
+
+
+def threads() -> int:
+    """Host threads the oracle's parallel loops use."""
+    return int(lib().orc_threads())
 
 
 def decode_step(w, source, tokens, positions, trace: bool = False):

@@ -14,6 +14,7 @@
 #include "oracle.h"
 
 #include <math.h>
+#include <omp.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -326,3 +327,6 @@ done:
   free(x); free(n); free(qkv); free(o); free(attn); free(moe); free(rl); free(wk); free(ids); free(kb); free(vb);
   return status;
 }
+
+/* Host threads the oracle's parallel loops use (reported next to its timings). */
+int orc_threads(void) { return omp_get_max_threads(); }

@@ -80,6 +80,9 @@ typedef struct {
 /* One decode step for B sequences: token_ids[b] at position positions[b] (= tokens
  * already cached). Appends each layer's k,v (bf16) through kv_write, writes fp32 logits
  * [B][V] and the greedy next token [B] (lowest index on ties). */
+/* Host threads the oracle's parallel loops use. */
+int orc_threads(void);
+
 int orc_decode_step(const orc_cfg* cfg, const orc_source* src, int B, const int32_t* token_ids,
                     const int32_t* positions, float* logits, int32_t* next_token, orc_trace* trace);
 
