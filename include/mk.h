@@ -50,8 +50,10 @@ typedef enum {
 
 /* Model shape. Supported by this build: hidden in {256, 512, 1024, 2048}; head_dim in
  * {64, 128}; n_q_heads / n_kv_heads <= 8 and n_kv_heads divides n_q_heads; n_q_heads *
- * head_dim a multiple of 256 (and of 2048 when above 2048); expert_inter a multiple of 256;
- * top_k <= 8; max_batch <= 8; page_size == 16. */
+ * head_dim a multiple of 256 (and of 2048 when above 2048); expert_inter a multiple of 256,
+ * at most 2048, with 2 * max_batch * (2 * expert_inter + 16) <= 33792 (one expert's hi/lo
+ * activations for the batch fit a ring stage: any max_batch up to expert_inter 1024, max_batch
+ * <= 4 at 2048); top_k <= 8; max_batch <= 8; page_size == 16. */
 typedef struct {
   int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim;
   int32_t n_experts, top_k, expert_inter, vocab;
@@ -176,10 +178,11 @@ mk_status mk_get_activations(const mk_ctx* ctx, mk_activations* out);
  * grouped by SM) when tasks_cap >= info->n_tasks, else returns MK_ERR_INVALID_ARG; if
  * sm_begin is non-NULL, writes the n_sm + 1 list offsets; if sm_bytes is non-NULL, the
  * planned bytes per SM. Opcodes: 1 router, 2 QKV, 3 attention, 4 expert gate/up, 5 O-proj,
- * 6 expert down, 7 LM head. The two branches of each layer run on disjoint SM partitions:
- * SMs [0, n_attn_sm) take QKV, attention and O-proj, the others router, gate/up and down
- * (n_attn_sm == n_sm: every SM takes both, as for very small n_sm). The LM head spreads over
- * all SMs. Errors: MK_ERR_INVALID_ARG. */
+ * 6 expert down, 7 LM head. At batch 1 (n_sm >= 8), when the attention branch streams at most
+ * 1.5x the expert branch's bytes, the two branches of each layer run on disjoint SM partitions:
+ * SMs [0, n_attn_sm) take QKV, attention and O-proj, the others router, gate/up and down;
+ * otherwise n_attn_sm == n_sm and every SM takes both. The LM head spreads over all SMs.
+ * Errors: MK_ERR_INVALID_ARG. */
 typedef struct {
   int32_t n_tasks, n_counters, max_chunks, n_lm_sm, n_op_launches, n_attn_sm;
 } mk_plan_info;

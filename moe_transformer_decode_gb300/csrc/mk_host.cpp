@@ -147,7 +147,9 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
                         od % 256 == 0 && (od <= 2048 || od % 2048 == 0) && m.expert_inter % 256 == 0 &&
                         m.expert_inter <= 2048 && m.top_k <= kMaxK && m.max_batch <= kMaxB &&
                         m.page_size == kPage && m.n_experts <= kMaxExperts && m.n_experts % 8 == 0 &&
-                        m.vocab % 64 == 0;
+                        m.vocab % 64 == 0 &&
+                        // an expert's activations for the whole batch fit one ring stage
+                        2 * m.max_batch * (2 * m.expert_inter + 16) <= kStageBytes;
   if (!shape_ok) return MK_ERR_UNSUPPORTED;
 
   mk_ctx* c = new mk_ctx();  // value-initialized: every pointer starts null
@@ -342,14 +344,15 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   // expected live fraction of the planned expert slots (1 at batch 1)
   const double live = maxa == m.top_k ? 1.0 : std::min(1.0, (double)E * (1.0 - std::pow(1.0 - (double)m.top_k / E, B)) / maxa);
 
-  // The two branches of a layer (attention: QKV, attention, O-proj; experts: router, gate/up,
-  // down) only meet at the residual, so they run on disjoint SM partitions sized by their bytes
-  // per layer: neither branch's tasks queue behind the other's on an SM.
+  // At batch 1, when the two branches of a layer (attention: QKV, attention, O-proj; experts:
+  // router, gate/up, down) stream comparable bytes, they run on disjoint SM partitions sized by
+  // those bytes, so neither branch's tasks queue behind the other's on an SM. At larger batches,
+  // or when one branch dominates (the KV of a long context), every SM takes both: measured faster.
   const double attn_bytes = (double)(m.n_q_heads + 2 * nkv) * d * H * 2 + (double)H * od * 2 +
                             (double)group_pages * 2 * kPage * d * 2;
   const double moe_bytes = (double)E * H * 2 + live * maxa * 3.0 * I * H * 2;
-  int n_attn = n_sm;  // too few SMs to split: every SM takes both branches
-  if (n_sm >= 8) {
+  int n_attn = n_sm;  // every SM takes both branches
+  if (n_sm >= 8 && B == 1 && attn_bytes <= 1.5 * moe_bytes) {
     n_attn = (int)std::lround(n_sm * attn_bytes / (attn_bytes + moe_bytes));
     n_attn = std::min(std::max(n_attn, 1), n_sm - 1);
   }

@@ -317,6 +317,9 @@ struct Misc {
   int pr_n;
   int pr_expert[kMaxActive];
   int pr_ids[kIdCache];
+  // batch 1: the normalized input's mma fragments (only lanes 0-7 hold data: hi and lo of
+  // token 0), per warp and k-step
+  alignas(16) uint2 nf1[kConsumerWarps][16][8];
   // per-warp LM argmax candidates per token
   float lmw_v[kConsumerWarps][kMaxB];
   int lmw_i[kConsumerWarps][kMaxB];
@@ -517,11 +520,28 @@ struct Producer {
         if (!route(l)) return false;
         const int na = m.pr_n;
         const Geo g = geo_of(p.I);
+        const int hrst = p.I * 2 + 16;  // padded row stride of the activation stage
 #pragma unroll 1
         for (int a = 0; a < na; ++a) {
           const int e = m.pr_expert[a];
           const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + t.a) * p.I;
           if (!gemv_rows(W, t.b, p.I, p.I * 2, g.RST)) return false;
+          // then the expert's activations: row hl * B + b holds plane hl (hi, lo) of token b.
+          // They exist once every gate/up task of the layer is done (the first weight stage
+          // above is already on its way).
+          if (a == 0) {
+            int fine = 1;
+            if (lane == 0) fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.gu(l));
+            if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
+          }
+          if (!begin((uint32_t)2 * p.B * p.I * 2)) return false;
+          const uint16_t* hp = p.h + (((size_t)l * kMaxActive + a) * 2 * kMaxB) * p.I;
+#pragma unroll 1
+          for (int rr = lane; rr < 2 * p.B; rr += 32) {
+            const int hl = rr / p.B, b = rr % p.B;
+            bulk_g2s(dst + (uint32_t)(rr * hrst), hp + ((size_t)hl * kMaxB + b) * p.I, p.I * 2, bar, pol);
+          }
+          end();
         }
         return true;
       }
@@ -602,7 +622,7 @@ struct Consumer {
   // the normalized input of layer n_layer, this warp's 256-column slice as mma A fragments:
   // lane (g, t) holds the hi (g even) or lo (g odd) part of token g/2 (registers 0, 1) and of
   // token g/2 + 4 (registers 2, 3) at columns 16 s + 2 t + {0, 1} and + {8, 9}
-  uint32_t nf[16][AR];
+  uint32_t nf[NB > 1 ? 16 : 1][AR];  // batch 1 keeps them in m.nf1 instead
   float lm_best[NB];    // running LM-head argmax of the stages whose epilogue this lane ran
   int lm_idx[NB];
   uint64_t t_start, t_ready;
@@ -624,6 +644,16 @@ struct Consumer {
 
   __device__ const uint8_t* acquire() {
     const uint32_t s = r.it % kStages, parity = (r.it / kStages) & 1u;
+    if (!mbar_wait(p, r.full + 8 * s, parity)) {
+      ok = false;
+      return nullptr;
+    }
+    return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(r.data + s * kStageBytes));
+  }
+  // the ring slot k stages after the next one (held together with it)
+  __device__ const uint8_t* acquire_at(uint32_t k) {
+    const uint32_t it = r.it + k;
+    const uint32_t s = it % kStages, parity = (it / kStages) & 1u;
     if (!mbar_wait(p, r.full + 8 * s, parity)) {
       ok = false;
       return nullptr;
@@ -704,10 +734,12 @@ struct Consumer {
     // normalized input into mma fragments, one token at a time through this warp's exchange area
     float* xw = m.nsm + warp * 256;
     const int g8 = lane >> 2, t4 = lane & 3, hl = g8 & 1, tb = g8 >> 1;
+    if constexpr (NB > 1) {
 #pragma unroll
-    for (int s = 0; s < 16; ++s)
+      for (int s = 0; s < 16; ++s)
 #pragma unroll
-      for (int r = 0; r < AR; ++r) nf[s][r] = 0u;
+        for (int r = 0; r < AR; ++r) nf[s][r] = 0u;
+    }
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       float tot = 0.f;
@@ -726,8 +758,12 @@ struct Consumer {
         for (int s = 0; s < 16; ++s) {
           const float2 v0 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4);
           const float2 v1 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4 + 8);
-          nf[s][0] = pack_part(v0.x, v0.y, hl);
-          nf[s][1] = pack_part(v1.x, v1.y, hl);
+          if constexpr (NB == 1) {
+            m.nf1[warp][s][lane] = make_uint2(pack_part(v0.x, v0.y, hl), pack_part(v1.x, v1.y, hl));
+          } else {
+            nf[s][0] = pack_part(v0.x, v0.y, hl);
+            nf[s][1] = pack_part(v1.x, v1.y, hl);
+          }
         }
       }
       if constexpr (AR == 4) {
@@ -847,14 +883,36 @@ struct Consumer {
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&m.gfree[buf]));
   }
-  // One stage against the normalized input (nf), as one pass; returns its id.
+  // batch 1: as mma_rows, A fragments of the normalized input from m.nf1 (lanes 0-7 hold the
+  // hi and lo parts of token 0; every other lane's are zero)
+  __device__ __forceinline__ void mma_rows_nf1(uint32_t st, const Geo& g, int rg, int ks, float (&c)[4][4]) const {
+    const uint32_t base = st + (uint32_t)((rg * 8 + (lane & 7)) * g.RST) + (uint32_t)((ks * 256 + (lane >> 3) * 8) * 2);
+    const uint2* fr = &m.nf1[warp][0][lane & 7];
+    const bool has = lane < 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t bw[4];
+      ldsm_x4(base + j * 64, bw);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint2 f = has ? fr[(2 * j + h) * 8] : make_uint2(0u, 0u);
+        const uint32_t a[4] = {f.x, 0u, f.y, 0u};
+        mma_bf16(c[(2 * j + h) & 3], a, bw[2 * h], bw[2 * h + 1]);
+      }
+    }
+  }
+  // One stage against the normalized input, as one pass; returns its id.
   __device__ uint32_t norm_pass(const Geo& g) {
     const int rg = warp / g.KW, ks = warp % g.KW;
     const bool active = rg < g.RG;
     float c[4][4] = {};
     const uint8_t* st = acquire();
     if (!st) return gv;
-    if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, nf, c);
+    if constexpr (NB == 1) {
+      if (active) mma_rows_nf1((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, c);
+    } else {
+      if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, nf, c);
+    }
     release();
     return post_pass(active, c);
   }
@@ -945,6 +1003,34 @@ struct Consumer {
   __device__ __forceinline__ size_t h_plane(int l, int a) const {
     return ((size_t)l * kMaxActive + a) * 2 * kMaxB * (size_t)p.I;
   }
+  // As mma_rows, with the A fragments read from an activation stage in shared memory: row
+  // hl * B + b holds plane hl of token b (I bf16, rows hrst bytes apart). A row m = 2 b + hl;
+  // tokens outside bmask (or >= B) are zeroed after the load.
+  __device__ __forceinline__ void mma_rows_sa(uint32_t st, const Geo& g, int rg, int ks, uint32_t act, int hrst,
+                                              uint32_t bmask, float (&c)[4][4]) const {
+    const uint32_t base = st + (uint32_t)((rg * 8 + (lane & 7)) * g.RST) + (uint32_t)((ks * 256 + (lane >> 3) * 8) * 2);
+    // ldmatrix.x4 for A: lane supplies row (lane & 7) + 8 (q & 1) of k-half q >> 1, q = lane >> 3
+    const int q = lane >> 3, mrow = (lane & 7) + 8 * (q & 1), mb = mrow >> 1;
+    const int arow = mb < p.B ? (mrow & 1) * p.B + mb : 0;
+    const uint32_t abase = act + (uint32_t)(arow * hrst) + (uint32_t)((ks * 256 + 8 * (q >> 1)) * 2);
+    const int tb = (lane >> 2) >> 1;  // token of this lane's rows g (regs 0, 2); + 4 for regs 1, 3
+    const bool ok0 = tb < p.B && ((bmask >> tb) & 1u);
+    const bool ok1 = NB > 4 && tb + 4 < p.B && ((bmask >> (tb + 4)) & 1u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t bw[4];
+      ldsm_x4(base + j * 64, bw);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t a[4];
+        ldsm_x4(abase + (2 * j + h) * 32, a);
+        if (!ok0) a[0] = a[2] = 0u;
+        if (!ok1) a[1] = a[3] = 0u;
+        mma_bf16(c[(2 * j + h) & 3], a, bw[2 * h], bw[2 * h + 1]);
+      }
+    }
+  }
+
   // A fragments from hi/lo bf16 planes (no conversion): token b's row of this warp's slice in
   // plane hl starts at element base + hl * plane + b * row; tokens outside bmask are zero
   __device__ __forceinline__ void ld_frags_hl(const uint16_t* base, size_t plane, size_t row, uint32_t bmask,
@@ -1236,23 +1322,17 @@ struct Consumer {
     const Geo g = geo_of(p.I);
     const int rg = warp / g.KW, ks = warp % g.KW;
     const bool active = rg < g.RG;
-    const int na = m.rc_n;
+    const int na = m.rc_n, hrst = p.I * 2 + 16;
     float c[4][4] = {};
-    uint32_t af[16][AR], an[16][AR];
-    const size_t hpl = (size_t)kMaxB * p.I;
-    // the activations of expert a + 1 are loaded while expert a's stage is multiplied
-    if (active && na > 0) ld_frags_hl(p.h + h_plane(l, 0) + ks * 256, hpl, p.I, m.rc_mask[0], an);
+    // per routed expert: its weight stage, then its activation stage (both held at once)
     for (int a = 0; a < na; ++a) {
-      if (active) {
-#pragma unroll
-        for (int s = 0; s < 16; ++s)
-#pragma unroll
-          for (int r = 0; r < AR; ++r) af[s][r] = an[s][r];
-        if (a + 1 < na) ld_frags_hl(p.h + h_plane(l, a + 1) + ks * 256, hpl, p.I, m.rc_mask[a + 1], an);
-      }
-      const uint8_t* st = acquire();
-      if (!st) return;
-      if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, af, c);
+      const uint8_t* sw = acquire();
+      const uint8_t* sa = sw ? acquire_at(1) : nullptr;
+      if (!sa) return;
+      if (active)
+        mma_rows_sa((uint32_t)__cvta_generic_to_shared(sw), g, rg, ks, (uint32_t)__cvta_generic_to_shared(sa), hrst,
+                    m.rc_mask[a], c);
+      release();
       release();
     }
     run_epi(post_pass(active, c), g, [&](auto&& R) {

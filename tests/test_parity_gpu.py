@@ -52,14 +52,19 @@ def _run(w, steps, per_layer=False, mode=0):
                         if s.bt[b, pos[b] // w.page] == pg:
                             keep[:, :, pos[b] % w.page] = False
                     assert np.array_equal(after[keep], before[pg][keep]), "KV bytes outside the new slots changed"
+            # values: one bf16 rounding apart, plus the error the step's input carries at depth.
+            # The GPU carries every GEMV input as a bf16 hi + lo pair (>= 16 significant bits),
+            # so each layer adds up to ~2^-16 relative error to the residual stream: over L layers
+            # at most L * 2^-16 (7.3e-4 at 48 layers) of the head's rms, bounded here by 1e-3.
+            kv_abs = max(1e-4, w.L * 2.0 ** -16)
             for b in range(w.B):
                 pg, sl = s.bt[b, pos[b] // w.page], pos[b] % w.page
                 for got, ref in ((_bits(s.K[:, pg, :, sl]), tr["k_new"][:, b]), (_bits(s.V[:, pg, :, sl]), tr["v_new"][:, b])):
                     g32 = synth.bf16_bits_to_f32(got).astype(np.float64)
                     r32 = synth.bf16_bits_to_f32(ref).astype(np.float64)
                     scale = np.sqrt(np.mean(r32 ** 2, axis=-1, keepdims=True))
-                    assert np.all(np.abs(g32 - r32) <= 2.0 ** -7 * np.abs(r32) + 1e-4 * scale), \
-                        "appended K/V differ from the oracle beyond bf16 rounding"
+                    assert np.all(np.abs(g32 - r32) <= 2.0 ** -7 * np.abs(r32) + kv_abs * scale), \
+                        "appended K/V differ from the oracle beyond bf16 rounding and the input's error"
             tokens = ref_next  # teacher forcing
     finally:
         s.close()
