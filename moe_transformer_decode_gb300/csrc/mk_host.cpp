@@ -260,10 +260,10 @@ Geo geo_of(int K) {
   return g;
 }
 
-// Least-loaded assignment within a partition of the SMs. Loads are counted per layer
-// (new_layer() restarts them), so each layer's work, phase by phase, is spread evenly over the
-// partition; ties go to the SM with the least bytes over the whole step (`total`), so no SM
-// takes the extra task in every layer.
+// Least-loaded assignment within a partition of the SMs. Loads are counted per phase
+// (new_layer() restarts them), so each phase's work is spread evenly over the partition; ties
+// go to the SM with the least bytes over the whole step (`total`), so no SM takes the extra
+// task in every phase.
 struct Assigner {
   int n_sm;
   std::vector<int> part;  // partition of each SM
@@ -378,14 +378,19 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   // about two QKV tasks per attention SM and two expert gate/up tasks per expert SM, per layer
   // (whole stages each)
   const int upg_ = (G + 2) * (d / 8);
-  int qkv_per_task = std::max(1, (int)std::lround((double)nkv * upg_ / (2.0 * n_attn)));
+  // (rounded up, so no SM of a partition gets a third)
+  int qkv_per_task = std::max(1, (nkv * upg_ + 2 * n_attn - 1) / (2 * n_attn));
   qkv_per_task = std::max(gh.RG, (qkv_per_task + gh.RG - 1) / gh.RG * gh.RG);
-  const int gu_per_task = std::max(1, (int)std::lround((double)maxa * tiles / (2.0 * n_moe)));
+  const int gu_per_task = std::max(1, (maxa * tiles + 2 * n_moe - 1) / (2 * n_moe));
   const long long row_h = 2LL * H;
 
   Assigner as(n_sm, part, PM + 1);
   std::vector<std::vector<std::vector<Task>>> per_op;  // [launch][sm] tasks for the per-op mode
+  // Each phase (the tasks of one op kind in a layer) becomes ready at once, after a dependency
+  // every SM shares, so it is balanced on its own: loads restart at every phase (ties still go
+  // to the SM with the fewest bytes over the step).
   auto emit = [&](std::vector<std::pair<Task, long long>>& ts, int pt) {
+    as.new_layer();
     for (auto& x : ts) as.put(x.first, x.second, pt);
     std::vector<std::vector<Task>> lists(n_sm);
     for (size_t i = 0; i < ts.size(); ++i) lists[i % n_sm].push_back(ts[i].first);
