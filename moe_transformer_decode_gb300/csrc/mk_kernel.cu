@@ -1421,16 +1421,28 @@ struct Consumer {
     const float qscale = rsqrtf((float)p.d) * 1.4426950408889634f;  // scores in log2 units
     uint32_t qa[8][4];
     {
+      // the group's q (group x d floats, contiguous) into shared memory once per block, one
+      // float4 per thread, rows padded by 4 floats; the partial-sum buffers are free here (the
+      // barrier waits for the previous task's last epilogue)
+      float* qs = &m.red[1][0][0];
+      const int qst = p.d + 4;
+      if (!csync()) return;
+      const float4* qg = reinterpret_cast<const float4*>(p.q + (((size_t)l * p.B + b) * p.nq + g * p.group) * p.d);
+      for (int i = threadIdx.x; i < p.group * p.d / 4; i += 256) {
+        const int hh = 4 * i / p.d, dd = 4 * i % p.d;
+        *reinterpret_cast<float4*>(qs + hh * qst + dd) = __ldcg(qg + i);
+      }
+      if (!csync()) return;
       // q arrives before RoPE: element d pairs with d + d/2, which this lane also holds (k-step
       // kk + ksteps/2), so the rotation happens here in registers
-      const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + head) * p.d;
+      const float* qh = qs + head * qst;
       const bool hv = head < p.group;
       float x[8][4];
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const int d0 = kk * 16 + tig * 2;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[kk][e] = (kk < ksteps && hv) ? __ldcg(qh + d0 + (e & 1) + (e >> 1) * 8) : 0.f;
+        for (int e = 0; e < 4; ++e) x[kk][e] = (kk < ksteps && hv) ? qh[d0 + (e & 1) + (e >> 1) * 8] : 0.f;
       }
       const int half = ksteps / 2, hd = p.d / 2;
 #pragma unroll
@@ -1578,11 +1590,24 @@ struct Consumer {
     const int arr = cm.attn_arrive(l, b, g);
     if (!arrive_last(arr, m.st_nch[b])) return;
 
-    // combine the chunks of (b, g) with the new token (position pos, read from knew / vnew)
+    // combine the chunks of (b, g) with the new token (position pos, read from knew / vnew):
+    // the chunk maxima and sums and the new token's scores in one round of loads, then the chunk
+    // outputs in one round (a float4 of one head per thread)
     const int nch = m.st_nch[b];
     const float* pbase = p.apart + (((size_t)l * p.B + b) * p.nkv + g) * p.max_chunks * (16 + 8 * (size_t)p.d);
-    // s_new per head: warp h < group
-    if (warp < p.group) {
+    const size_t cstride = 16 + 8 * (size_t)p.d;
+    const float* vn = p.vnew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
+    float* sc = &m.red[2][0][0];  // [0, 8): new token's scores, [8, 16): its factor, [16, 24): 1 / sum
+    float* sm_m = &m.red[0][0][0];  // [nch][8]: chunk max, then its scale factor
+    float* sm_l = &m.red[1][0][0];  // [nch][8]: chunk sum
+    const bool few = nch <= 64;
+    if (few)
+      for (int i = threadIdx.x; i < nch * 8; i += 256) {
+        const float* src = pbase + (size_t)(i / 8) * cstride;
+        sm_m[i] = __ldcg(src + (i % 8));
+        sm_l[i] = __ldcg(src + 8 + (i % 8));
+      }
+    if (warp < p.group) {  // s_new of head `warp`
       const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + warp) * p.d;
       const float* kn = p.knew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
       float s = 0.f;
@@ -1595,25 +1620,13 @@ struct Consumer {
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) m.red[2][0][warp] = s * qscale;
+      if (lane == 0) sc[warp] = s * qscale;
     }
     if (!csync()) return;
-    const float* vn = p.vnew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
-    const size_t cstride = 16 + 8 * (size_t)p.d;
-    if (nch <= 64) {
-      // chunk maxima and sums in one parallel load round, scale factors in shared memory, then
-      // independent loads of the chunk outputs
-      float* sm_m = &m.red[0][0][0];  // [nch][8]: chunk max, then its scale factor
-      float* sm_l = &m.red[1][0][0];  // [nch][8]: chunk sum
-      for (int i = threadIdx.x; i < nch * 8; i += 256) {
-        const float* src = pbase + (size_t)(i / 8) * cstride;
-        sm_m[i] = __ldcg(src + (i % 8));
-        sm_l[i] = __ldcg(src + 8 + (i % 8));
-      }
-      if (!csync()) return;
+    if (few) {
       if (threadIdx.x < p.group) {
         const int h = threadIdx.x;
-        const float sn = m.red[2][0][h];
+        const float sn = sc[h];
         float M = sn;
         for (int c = 0; c < nch; ++c) M = fmaxf(M, sm_m[c * 8 + h]);
         const float fn = exp2f(sn - M);
@@ -1624,29 +1637,42 @@ struct Consumer {
           L += sm_l[c * 8 + h] * f;
           sm_m[c * 8 + h] = f;
         }
-        m.red[2][0][8 + h] = fn;
-        m.red[2][0][16 + h] = 1.0f / L;
+        sc[8 + h] = fn;
+        sc[16 + h] = 1.0f / L;
       }
       if (!csync()) return;
-      for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
-        const int h = i / p.d, dd = i % p.d;
+      for (int i = threadIdx.x; i < p.group * p.d / 4; i += 256) {
+        const int h = 4 * i / p.d, dd = 4 * i % p.d;
         const float* src = pbase + 16 + h * p.d + dd;
-        float O = m.red[2][0][8 + h] * __ldcg(vn + dd);
-        int c = 0;
-        for (; c + 8 <= nch; c += 8) {
-          float v[8];
+        const float fn = sc[8 + h];
+        const float4 vv = __ldcg(reinterpret_cast<const float4*>(vn + dd));
+        float4 O = make_float4(fn * vv.x, fn * vv.y, fn * vv.z, fn * vv.w);
+        for (int c0 = 0; c0 < nch; c0 += 16) {
+          float4 v[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (size_t)(c + j) * cstride);
+          for (int j = 0; j < 16; ++j)
+            v[j] = c0 + j < nch ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)(c0 + j) * cstride))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) O = fmaf(v[j], sm_m[(c + j) * 8 + h], O);
+          for (int j = 0; j < 16; ++j) {
+            const float f = c0 + j < nch ? sm_m[(c0 + j) * 8 + h] : 0.f;
+            O.x = fmaf(v[j].x, f, O.x);
+            O.y = fmaf(v[j].y, f, O.y);
+            O.z = fmaf(v[j].z, f, O.z);
+            O.w = fmaf(v[j].w, f, O.w);
+          }
         }
-        for (; c < nch; ++c) O = fmaf(__ldcg(src + (size_t)c * cstride), sm_m[c * 8 + h], O);
-        store_attn(l, b, (g * p.group + h) * p.d + dd, O * m.red[2][0][16 + h]);
+        const float inv = sc[16 + h];
+        const int col = (g * p.group + h) * p.d + dd;
+        store_attn(l, b, col, O.x * inv);
+        store_attn(l, b, col + 1, O.y * inv);
+        store_attn(l, b, col + 2, O.z * inv);
+        store_attn(l, b, col + 3, O.w * inv);
       }
     } else {
       for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
         const int h = i / p.d, dd = i % p.d;
-        const float sn = m.red[2][0][h];
+        const float sn = sc[h];
         float M = sn;
         for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(pbase + (size_t)c * cstride + h));
         float fn = exp2f(sn - M);
