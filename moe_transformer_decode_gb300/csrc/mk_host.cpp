@@ -454,10 +454,13 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
       ts.push_back({mkt(OP_DOWN, l, r0, std::min(gi.RS, H - r0), 0),
                     (long long)(std::min(gi.RS, H - r0) * 2.0 * I * maxa * live)});
     emit(ts, PM);
-    // O-proj rows
+    // O-proj: blocks of RS rows; at batch <= 4 (and at most two 2048-column chunks) a task takes
+    // several blocks, reusing one load of the attention output, about one task per SM
+    const int o_blocks = (H + go.RS - 1) / go.RS;
+    const int o_per = (B <= 4 && go.NCS <= 2) ? (o_blocks + n_attn - 1) / n_attn : 1;
     int n_o = 0;
-    for (int r0 = 0; r0 < H; r0 += go.RS, ++n_o)
-      ts.push_back({mkt(OP_O, l, r0, std::min(go.RS, H - r0), 0), std::min(go.RS, H - r0) * 2LL * od});
+    for (int r0 = 0; r0 < H; r0 += o_per * go.RS, ++n_o)
+      ts.push_back({mkt(OP_O, l, r0, std::min(o_per * go.RS, H - r0), 0), std::min(o_per * go.RS, H - r0) * 2LL * od});
     emit(ts, PA);
     cnt[cmap.layer(l)] = n_o + n_down;
   }

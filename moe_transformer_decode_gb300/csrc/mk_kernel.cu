@@ -512,8 +512,10 @@ struct Producer {
         const Geo g = geo_of(p.od);
         const uint16_t* W = p.w_o + ((size_t)l * p.H + t.a) * p.od;
 #pragma unroll 1
-        for (int cs = 0; cs < g.NCS; ++cs)
-          if (!gemv_rows(W + cs * g.KS, t.b, p.od, g.KS * 2, g.RST)) return false;
+        for (int r0 = 0; r0 < t.b; r0 += g.RS)  // row blocks, each over the column chunks
+#pragma unroll 1
+          for (int cs = 0; cs < g.NCS; ++cs)
+            if (!gemv_rows(W + (size_t)r0 * p.od + cs * g.KS, min(g.RS, t.b - r0), p.od, g.KS * 2, g.RST)) return false;
         return true;
       }
       case OP_DOWN: {
@@ -1290,28 +1292,56 @@ struct Consumer {
     const int rg = warp / g.KW, ks = warp % g.KW;
     const bool active = rg < g.RG;
     const int gw = p.group * p.d;  // columns per KV group
-    float c[4][4] = {};
-    t_ready = 0;
-    for (int cs = 0; cs < g.NCS; ++cs) {
+    const uint16_t* base = p.attn_hl + (size_t)l * 2 * p.B * p.od + ks * 256;
+    const size_t plane = (size_t)p.B * p.od;
+    // waits for the KV groups behind chunk cs's columns of this warp's slice
+    auto wait_chunk = [&](int cs) -> bool {
       const int c0 = cs * g.KS + ks * 256;
-      uint32_t af[16][AR];
-      if (active) {
-        for (int gg = c0 / gw; gg <= (c0 + 255) / gw; ++gg)
-          if (!wait_attn_group(l, gg)) return;
-        ld_frags_hl(p.attn_hl + (size_t)l * 2 * p.B * p.od + c0, (size_t)p.B * p.od, p.od, bmask_all(), af);
-      }
-      if (!t_ready) t_ready = gtimer();
-      const uint8_t* st = acquire();
-      if (!st) return;
-      if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, af, c);
-      release();
+      for (int gg = c0 / gw; gg <= (c0 + 255) / gw; ++gg)
+        if (!wait_attn_group(l, gg)) return false;
+      return true;
+    };
+    auto epi = [&](uint32_t pid, int r0, int rows) {
+      run_epi(pid, g, [&](auto&& R) {
+        for (int i = lane; i < rows * NB; i += 32) {
+          const int rr = i / NB, b = i % NB;
+          if (b < p.B) __stcg(&p.attn_out[((size_t)l * p.B + b) * p.H + t.a + r0 + rr], R(rr, b));
+        }
+      });
+    };
+    t_ready = 0;
+    // At batch <= 4 with at most two column chunks, both chunks' fragments are loaded once and
+    // reused by every row block of the task; otherwise (one block per task) chunk by chunk.
+    constexpr bool kHold = AR == 2;
+    const bool hold = kHold && g.NCS <= 2;
+    uint32_t af[kHold ? 2 : 1][16][AR];
+    if (hold && active) {
+      for (int cs = 0; cs < g.NCS; ++cs)
+        if (!wait_chunk(cs)) return;
+      ld_frags_hl(base, plane, p.od, bmask_all(), af[0]);
+      if (g.NCS > 1) ld_frags_hl(base + g.KS, plane, p.od, bmask_all(), af[kHold ? 1 : 0]);
     }
-    run_epi(post_pass(active, c), g, [&](auto&& R) {
-      for (int i = lane; i < t.b * NB; i += 32) {
-        const int rr = i / NB, b = i % NB;
-        if (b < p.B) __stcg(&p.attn_out[((size_t)l * p.B + b) * p.H + t.a + rr], R(rr, b));
+    uint32_t prev = 0;
+    int pr0 = -1, prows = 0;
+    for (int r0 = 0; r0 < t.b && ok; r0 += g.RS) {
+      float c[4][4] = {};
+      for (int cs = 0; cs < g.NCS; ++cs) {
+        if (!hold && active) {
+          if (!wait_chunk(cs)) return;
+          ld_frags_hl(base + cs * g.KS, plane, p.od, bmask_all(), af[0]);
+        }
+        if (!t_ready) t_ready = gtimer();
+        const uint8_t* st = acquire();
+        if (!st) return;
+        if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, af[hold ? (cs & 1) : 0], c);
+        release();
       }
-    });
+      const uint32_t pid = post_pass(active, c);
+      if (!ok) return;
+      if (pr0 >= 0) epi(prev, pr0, prows);
+      prev = pid, pr0 = r0, prows = min(g.RS, t.b - r0);
+    }
+    if (pr0 >= 0) epi(prev, pr0, prows);
     if (ok) release_counter(cm.layer(l));
   }
 

@@ -59,7 +59,9 @@ def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
         g = t[t["op"] == OP_GU]
         assert sorted(_ranges(g).tolist()) == list(range(maxa * (w.I // (rows_per_stage(w.H) // 2))))
         o = t[t["op"] == OP_O]
-        assert sorted(_ranges(o).tolist()) == list(range(w.H)) and np.all(o["b"] <= rows_per_stage(w.nq * w.d))
+        rs_o = rows_per_stage(w.nq * w.d)  # O tasks: whole row blocks (the last may be short)
+        assert sorted(_ranges(o).tolist()) == list(range(w.H))
+        assert np.all((o["b"] % rs_o == 0) | (o["a"] + o["b"] == w.H))
         dn = t[t["op"] == OP_DOWN]
         assert sorted(_ranges(dn).tolist()) == list(range(w.H)) and np.all(dn["b"] <= rows_per_stage(w.I))
     lm = tasks[tasks["op"] == OP_LM]
