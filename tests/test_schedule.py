@@ -71,10 +71,14 @@ def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
     assert len(set(owners.tolist())) == len(lm), "two LM tasks on one SM"
 
 
-def test_plan_balances_bytes_over_sms():
-    w = W.M30B_BS1
-    info, tasks, begin, load = B.mk_plan_schedule(cfg_of(w, 600), 148, W.context_lengths(w))
-    assert load.max() / load.mean() < 1.02
+@pytest.mark.parametrize("w,n_sm", [(W.M30B_BS1, 148), (W.M30B_BS1, 152), (W.M30B_BS8, 152)])
+def test_plan_balances_bytes_over_sms(w, n_sm):
+    """Planned bytes are even over the SMs of each partition (the partitions themselves are
+    sized by the branches' critical paths, not their bytes)."""
+    info, tasks, begin, load = B.mk_plan_schedule(cfg_of(w, 600), n_sm, W.context_lengths(w))
+    na = info.n_attn_sm
+    for part in ((load[:na], load[na:]) if na < n_sm else (load,)):
+        assert part.max() / part.mean() < 1.03
 
 
 def test_plan_rejects_bad_arguments():
