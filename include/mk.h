@@ -51,9 +51,9 @@ typedef enum {
 /* Model shape. Supported by this build: hidden in {256, 512, 1024, 2048}; head_dim in
  * {64, 128}; n_q_heads / n_kv_heads <= 8 and n_kv_heads divides n_q_heads; n_q_heads *
  * head_dim a multiple of 256 (and of 2048 when above 2048); expert_inter a multiple of 256,
- * at most 2048, with 2 * max_batch * (2 * expert_inter + 16) <= 33792 (one expert's hi/lo
- * activations for the batch fit a ring stage: any max_batch up to expert_inter 1024, max_batch
- * <= 4 at 2048); top_k <= 8; max_batch <= 8; page_size == 16. */
+ * at most 2048, with 4 * max_batch * expert_inter <= 32768 (one expert's hi/lo activations
+ * for the batch fit a ring stage: any max_batch up to expert_inter 1024, max_batch <= 4 at
+ * 2048); top_k <= 8; max_batch <= 8; page_size == 16. */
 typedef struct {
   int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim;
   int32_t n_experts, top_k, expert_inter, vocab;

@@ -149,7 +149,7 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
                         m.page_size == kPage && m.n_experts <= kMaxExperts && m.n_experts % 8 == 0 &&
                         m.vocab % 64 == 0 &&
                         // an expert's activations for the whole batch fit one ring stage
-                        2 * m.max_batch * (2 * m.expert_inter + 16) <= kStageBytes;
+                        2 * m.max_batch * 2 * m.expert_inter <= kStagePayload;
   if (!shape_ok) return MK_ERR_UNSUPPORTED;
 
   mk_ctx* c = new mk_ctx();  // value-initialized: every pointer starts null

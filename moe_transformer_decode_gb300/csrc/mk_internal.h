@@ -20,7 +20,7 @@ static_assert(kConsumerWarps == 8, "two consumer warpgroups");
 static_assert(kProducerRegs * 128 + kConsumerRegs * 256 <= (65536 / kThreads) / 8 * 8 * kThreads,
               "register split exceeds the launch's allotment");
 constexpr int kStagePayload = 32768;                 // data bytes of a ring stage
-constexpr int kStageBytes = kStagePayload + 64 * 16;  // slot: GEMV rows (at most 64) are padded by 16 bytes
+constexpr int kStageBytes = kStagePayload;           // ring slot
 constexpr int kStages = 6;
 constexpr int kMaxB = 8;
 constexpr int kMaxK = 8;

@@ -220,8 +220,8 @@ __device__ bool mbar_wait_cta(const Params& p, uint32_t bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ geometry
 
-// A GEMV stage is RS rows x KS columns: bf16 rows in shared memory RST bytes apart (16 bytes of
-// padding per row, so the 8 row addresses of an ldmatrix fall in distinct banks). Each consumer
+// A GEMV stage is RS rows x KS columns of bf16, row-major in shared memory (RST = 2 KS bytes
+// apart, as in global memory, so a stage of consecutive rows is one bulk copy). Each consumer
 // warp owns 8 rows ("row group") and a 256-column slice (16 mma k-steps).
 struct Geo {
   int KS, KW, RG, RS, NCS, RST;
@@ -233,7 +233,7 @@ __device__ __forceinline__ Geo geo_of(int K) {
   g.RG = kConsumerWarps / g.KW;
   g.RS = 8 * g.RG;
   g.NCS = K / g.KS;
-  g.RST = g.KS * 2 + 16;
+  g.RST = g.KS * 2;
   return g;
 }
 
@@ -400,12 +400,17 @@ struct Producer {
   __device__ void end() { ++r.it; }
 
   // `rows` rows of row_bytes each, src_stride elements apart in global memory, into one stage
-  // with the padded row stride rst (one copy per row, spread over the lanes)
-  __device__ bool gemv_rows(const uint16_t* base, int rows, size_t src_stride, int row_bytes, int rst) {
+  // (rows row_bytes apart): one copy when the rows are contiguous, else one per row, spread over
+  // the lanes (a bulk copy costs about the same to issue whatever its size)
+  __device__ bool gemv_rows(const uint16_t* base, int rows, size_t src_stride, int row_bytes) {
     if (!begin((uint32_t)rows * row_bytes)) return false;
+    if (src_stride * 2 == (size_t)row_bytes) {
+      if (lane == 0) bulk_g2s(dst, base, (uint32_t)rows * row_bytes, bar, pol);
+    } else {
 #pragma unroll 1
-    for (int rr = lane; rr < rows; rr += 32)
-      bulk_g2s(dst + (uint32_t)(rr * rst), base + (size_t)rr * src_stride, row_bytes, bar, pol);
+      for (int rr = lane; rr < rows; rr += 32)
+        bulk_g2s(dst + (uint32_t)(rr * row_bytes), base + (size_t)rr * src_stride, row_bytes, bar, pol);
+    }
     end();
     return true;
   }
@@ -439,7 +444,7 @@ struct Producer {
         const uint16_t* W = t.op == OP_ROUTER ? p.w_router + (size_t)l * p.E * p.H : p.lm_head;
 #pragma unroll 1
         for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS)
-          if (!gemv_rows(W + (size_t)r0 * p.H, min(g.RS, t.a + t.b - r0), p.H, p.H * 2, g.RST)) return false;
+          if (!gemv_rows(W + (size_t)r0 * p.H, min(g.RS, t.a + t.b - r0), p.H, p.H * 2)) return false;
         return true;
       }
       case OP_QKV: {
@@ -451,11 +456,15 @@ struct Producer {
           const int nu = min(us, t.a + t.b - u0);
           if (!begin((uint32_t)nu * 8 * p.H * 2)) return false;
 #pragma unroll 1
-          for (int j = lane; j < nu * 8; j += 32) {  // unit j / 8, row j % 8
-            const QkvUnit q = qkv_unit(p, u0 + j / 8);
-            const int tt = j % 8;  // k/q: rows tt < 4 from row0, tt >= 4 from row0 + d/2
-            const int row = q.kind == 2 ? q.row0 + tt : q.row0 + (tt & 3) + (tt >= 4 ? p.d / 2 : 0);
-            bulk_g2s(dst + (uint32_t)(j * g.RST), W + (size_t)row * p.H, p.H * 2, bar, pol);
+          for (int i = lane; i < nu; i += 32) {  // unit i: v rows are consecutive; q/k rows are
+            const QkvUnit q = qkv_unit(p, u0 + i);  // 4 at row0 and 4 at row0 + d/2 (RoPE pairs)
+            const uint32_t d0 = dst + (uint32_t)(i * 8 * g.RST);
+            if (q.kind == 2) {
+              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 8 * p.H * 2, bar, pol);
+            } else {
+              bulk_g2s(d0, W + (size_t)q.row0 * p.H, 4 * p.H * 2, bar, pol);
+              bulk_g2s(d0 + 4 * g.RST, W + (size_t)(q.row0 + p.d / 2) * p.H, 4 * p.H * 2, bar, pol);
+            }
           }
           end();
         }
@@ -499,11 +508,9 @@ struct Producer {
           // tile: gate rows [tile RS/2, +RS/2) then the matching up rows (I rows further on)
           const uint16_t* W = p.w_gate_up + ((size_t)l * p.E + e) * 2 * p.I * p.H;
           if (!begin((uint32_t)g.RS * p.H * 2)) return false;
-#pragma unroll 1
-          for (int rr = lane; rr < g.RS; rr += 32) {
-            const int row = (rr < half ? 0 : p.I) + tile * half + (rr % half);
-            bulk_g2s(dst + (uint32_t)(rr * g.RST), W + (size_t)row * p.H, p.H * 2, bar, pol);
-          }
+          if (lane < 2)  // lane 0: the gate rows, lane 1: the matching up rows
+            bulk_g2s(dst + (uint32_t)(lane * half * g.RST), W + ((size_t)lane * p.I + tile * half) * p.H,
+                     (uint32_t)half * p.H * 2, bar, pol);
           end();
         }
         return true;
@@ -515,19 +522,18 @@ struct Producer {
         for (int r0 = 0; r0 < t.b; r0 += g.RS)  // row blocks, each over the column chunks
 #pragma unroll 1
           for (int cs = 0; cs < g.NCS; ++cs)
-            if (!gemv_rows(W + (size_t)r0 * p.od + cs * g.KS, min(g.RS, t.b - r0), p.od, g.KS * 2, g.RST)) return false;
+            if (!gemv_rows(W + (size_t)r0 * p.od + cs * g.KS, min(g.RS, t.b - r0), p.od, g.KS * 2)) return false;
         return true;
       }
       case OP_DOWN: {
         if (!route(l)) return false;
         const int na = m.pr_n;
         const Geo g = geo_of(p.I);
-        const int hrst = p.I * 2 + 16;  // padded row stride of the activation stage
 #pragma unroll 1
         for (int a = 0; a < na; ++a) {
           const int e = m.pr_expert[a];
           const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + t.a) * p.I;
-          if (!gemv_rows(W, t.b, p.I, p.I * 2, g.RST)) return false;
+          if (!gemv_rows(W, t.b, p.I, p.I * 2)) return false;
           // then the expert's activations: row hl * B + b holds plane hl (hi, lo) of token b.
           // They exist once every gate/up task of the layer is done (the first weight stage
           // above is already on its way).
@@ -538,11 +544,9 @@ struct Producer {
           }
           if (!begin((uint32_t)2 * p.B * p.I * 2)) return false;
           const uint16_t* hp = p.h + (((size_t)l * kMaxActive + a) * 2 * kMaxB) * p.I;
-#pragma unroll 1
-          for (int rr = lane; rr < 2 * p.B; rr += 32) {
-            const int hl = rr / p.B, b = rr % p.B;
-            bulk_g2s(dst + (uint32_t)(rr * hrst), hp + ((size_t)hl * kMaxB + b) * p.I, p.I * 2, bar, pol);
-          }
+          if (lane < 2)  // plane `lane` (hi, lo): the batch's rows are consecutive
+            bulk_g2s(dst + (uint32_t)(lane * p.B * p.I * 2), hp + (size_t)lane * kMaxB * p.I, (uint32_t)p.B * p.I * 2,
+                     bar, pol);
           end();
         }
         return true;
@@ -755,16 +759,16 @@ struct Consumer {
       d4[0] = make_float4(xn[0], xn[1], xn[2], xn[3]);
       d4[1] = make_float4(xn[4], xn[5], xn[6], xn[7]);
       __syncwarp();
+      // k-step s = 2 j + h of group j: columns 32 j + 8 t + 4 h + {0, 1} and {2, 3}
       if (tb == b) {
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-          const float2 v0 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4);
-          const float2 v1 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4 + 8);
+          const float4 v = *reinterpret_cast<const float4*>(xw + 32 * (s >> 1) + 8 * t4 + 4 * (s & 1));
           if constexpr (NB == 1) {
-            m.nf1[warp][s][lane] = make_uint2(pack_part(v0.x, v0.y, hl), pack_part(v1.x, v1.y, hl));
+            m.nf1[warp][s][lane] = make_uint2(pack_part(v.x, v.y, hl), pack_part(v.z, v.w, hl));
           } else {
-            nf[s][0] = pack_part(v0.x, v0.y, hl);
-            nf[s][1] = pack_part(v1.x, v1.y, hl);
+            nf[s][0] = pack_part(v.x, v.y, hl);
+            nf[s][1] = pack_part(v.z, v.w, hl);
           }
         }
       }
@@ -772,10 +776,9 @@ struct Consumer {
         if (tb + 4 == b) {
 #pragma unroll
           for (int s = 0; s < 16; ++s) {
-            const float2 v0 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4);
-            const float2 v1 = *reinterpret_cast<const float2*>(xw + 16 * s + 2 * t4 + 8);
-            nf[s][2] = pack_part(v0.x, v0.y, hl);
-            nf[s][3] = pack_part(v1.x, v1.y, hl);
+            const float4 v = *reinterpret_cast<const float4*>(xw + 32 * (s >> 1) + 8 * t4 + 4 * (s & 1));
+            nf[s][2] = pack_part(v.x, v.y, hl);
+            nf[s][3] = pack_part(v.z, v.w, hl);
           }
         }
       }
@@ -803,6 +806,14 @@ struct Consumer {
   // multiplies rows [8 rg, 8 rg + 8) x columns [256 ks, 256 ks + 256) of each stage (the B
   // operand, 8 rows = n8) by activation fragments (the A operand: up to 8 tokens x hi/lo = m16),
   // in four accumulation chains. post_pass / run_epi then add the warps' k-slices.
+  //
+  // Column map: a dot product may sum its columns in any order, so the k order inside the mma
+  // is permuted to suit the loads. In each 32-column group, lane t (= lane & 3) holds columns
+  // [8t, 8t + 8) of its row as one 16-byte word w: k-step 2j of group j takes columns (w.x, w.y)
+  // as its (2t, 2t + 1) and (2t + 8, 2t + 9) pairs, k-step 2j + 1 takes (w.z, w.w). The A
+  // fragments (af[s][0], af[s][1] = a0, a2) follow the same map. Rows are 2 KS bytes apart
+  // (a multiple of 128), so the two rows that share a load phase (g even and odd) read the two
+  // 64-byte halves of a 128-byte block in opposite orders and hit distinct banks.
 
   __device__ __forceinline__ void afrag(const uint32_t (&f)[AR], uint32_t (&a)[4]) const {
     a[0] = f[0];
@@ -815,19 +826,34 @@ struct Consumer {
       a[3] = 0u;
     }
   }
-  __device__ __forceinline__ void mma_rows(uint32_t st, const Geo& g, int rg, int ks, const uint32_t (&af)[16][AR],
+  // this lane's 16-byte words of column groups 2jj and 2jj + 1 from its row (rowp: the row's
+  // slice start + 16 t); odd rows load the two groups in the other order (distinct banks)
+  __device__ __forceinline__ void ld_pair(const uint8_t* rowp, int jj, uint4& w0, uint4& w1) const {
+    const int odd = (lane >> 2) & 1;
+    const uint4 x = *reinterpret_cast<const uint4*>(rowp + (2 * jj + odd) * 64);
+    const uint4 y = *reinterpret_cast<const uint4*>(rowp + (2 * jj + (odd ^ 1)) * 64);
+    w0 = odd ? y : x;
+    w1 = odd ? x : y;
+  }
+  __device__ __forceinline__ const uint8_t* b_row(const uint8_t* st, const Geo& g, int rg, int ks) const {
+    return st + (size_t)(rg * 8 + (lane >> 2)) * g.RST + ks * 512 + (lane & 3) * 16;
+  }
+  __device__ __forceinline__ void mma_rows(const uint8_t* st, const Geo& g, int rg, int ks, const uint32_t (&af)[16][AR],
                                            float (&c)[4][4]) const {
-    // ldmatrix.x4: lanes 8q..8q+7 address rows 0..7 at columns 8q..8q+7 of a 32-column block,
-    // giving the B fragments of two k-steps
-    const uint32_t base = st + (uint32_t)((rg * 8 + (lane & 7)) * g.RST) + (uint32_t)((ks * 256 + (lane >> 3) * 8) * 2);
+    const uint8_t* rowp = b_row(st, g, rg, ks);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t bw[4], a[4];
-      ldsm_x4(base + j * 64, bw);
-      afrag(af[2 * j], a);
-      mma_bf16(c[(2 * j) & 3], a, bw[0], bw[1]);
-      afrag(af[2 * j + 1], a);
-      mma_bf16(c[(2 * j + 1) & 3], a, bw[2], bw[3]);
+    for (int jj = 0; jj < 4; ++jj) {
+      uint4 w0, w1;
+      ld_pair(rowp, jj, w0, w1);
+      uint32_t a[4];
+      afrag(af[4 * jj], a);
+      mma_bf16(c[0], a, w0.x, w0.y);
+      afrag(af[4 * jj + 1], a);
+      mma_bf16(c[1], a, w0.z, w0.w);
+      afrag(af[4 * jj + 2], a);
+      mma_bf16(c[2], a, w1.x, w1.y);
+      afrag(af[4 * jj + 3], a);
+      mma_bf16(c[3], a, w1.z, w1.w);
     }
   }
   // End of a GEMV pass: each warp leaves its partial sums (rows [8 rg, 8 rg + 8) x tokens) in
@@ -887,19 +913,20 @@ struct Consumer {
   }
   // batch 1: as mma_rows, A fragments of the normalized input from m.nf1 (lanes 0-7 hold the
   // hi and lo parts of token 0; every other lane's are zero)
-  __device__ __forceinline__ void mma_rows_nf1(uint32_t st, const Geo& g, int rg, int ks, float (&c)[4][4]) const {
-    const uint32_t base = st + (uint32_t)((rg * 8 + (lane & 7)) * g.RST) + (uint32_t)((ks * 256 + (lane >> 3) * 8) * 2);
+  __device__ __forceinline__ void mma_rows_nf1(const uint8_t* st, const Geo& g, int rg, int ks, float (&c)[4][4]) const {
+    const uint8_t* rowp = b_row(st, g, rg, ks);
     const uint2* fr = &m.nf1[warp][0][lane & 7];
     const bool has = lane < 8;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t bw[4];
-      ldsm_x4(base + j * 64, bw);
+    for (int jj = 0; jj < 4; ++jj) {
+      uint4 w0, w1;
+      ld_pair(rowp, jj, w0, w1);
+      const uint32_t bw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint2 f = has ? fr[(2 * j + h) * 8] : make_uint2(0u, 0u);
+      for (int h = 0; h < 4; ++h) {
+        const uint2 f = has ? fr[(4 * jj + h) * 8] : make_uint2(0u, 0u);
         const uint32_t a[4] = {f.x, 0u, f.y, 0u};
-        mma_bf16(c[(2 * j + h) & 3], a, bw[2 * h], bw[2 * h + 1]);
+        mma_bf16(c[h], a, bw[2 * h], bw[2 * h + 1]);
       }
     }
   }
@@ -911,9 +938,9 @@ struct Consumer {
     const uint8_t* st = acquire();
     if (!st) return gv;
     if constexpr (NB == 1) {
-      if (active) mma_rows_nf1((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, c);
+      if (active) mma_rows_nf1(st, g, rg, ks, c);
     } else {
-      if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, nf, c);
+      if (active) mma_rows(st, g, rg, ks, nf, c);
     }
     release();
     return post_pass(active, c);
@@ -1006,52 +1033,55 @@ struct Consumer {
     return ((size_t)l * kMaxActive + a) * 2 * kMaxB * (size_t)p.I;
   }
   // As mma_rows, with the A fragments read from an activation stage in shared memory: row
-  // hl * B + b holds plane hl of token b (I bf16, rows hrst bytes apart). A row m = 2 b + hl;
-  // tokens outside bmask (or >= B) are zeroed after the load.
-  __device__ __forceinline__ void mma_rows_sa(uint32_t st, const Geo& g, int rg, int ks, uint32_t act, int hrst,
+  // hl * B + b holds plane hl of token b (I bf16, I * 2 bytes apart). A row m = 2 b + hl, so the
+  // lane's rows are plane g & 1 of tokens g / 2 and g / 2 + 4; tokens outside bmask (or >= B)
+  // are zero.
+  __device__ __forceinline__ void mma_rows_sa(const uint8_t* st, const Geo& g, int rg, int ks, const uint8_t* act,
                                               uint32_t bmask, float (&c)[4][4]) const {
-    const uint32_t base = st + (uint32_t)((rg * 8 + (lane & 7)) * g.RST) + (uint32_t)((ks * 256 + (lane >> 3) * 8) * 2);
-    // ldmatrix.x4 for A: lane supplies row (lane & 7) + 8 (q & 1) of k-half q >> 1, q = lane >> 3
-    const int q = lane >> 3, mrow = (lane & 7) + 8 * (q & 1), mb = mrow >> 1;
-    const int arow = mb < p.B ? (mrow & 1) * p.B + mb : 0;
-    const uint32_t abase = act + (uint32_t)(arow * hrst) + (uint32_t)((ks * 256 + 8 * (q >> 1)) * 2);
-    const int tb = (lane >> 2) >> 1;  // token of this lane's rows g (regs 0, 2); + 4 for regs 1, 3
+    const uint8_t* rowp = b_row(st, g, rg, ks);
+    const int g8 = lane >> 2, tb = g8 >> 1, hl = g8 & 1;
     const bool ok0 = tb < p.B && ((bmask >> tb) & 1u);
     const bool ok1 = NB > 4 && tb + 4 < p.B && ((bmask >> (tb + 4)) & 1u);
+    const size_t rb = (size_t)p.I * 2;
+    const uint8_t* a0p = act + (ok0 ? hl * p.B + tb : 0) * rb + ks * 512 + (lane & 3) * 16;
+    const uint8_t* a1p = act + (ok1 ? hl * p.B + tb + 4 : 0) * rb + ks * 512 + (lane & 3) * 16;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t bw[4];
-      ldsm_x4(base + j * 64, bw);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t a[4];
-        ldsm_x4(abase + (2 * j + h) * 32, a);
-        if (!ok0) a[0] = a[2] = 0u;
-        if (!ok1) a[1] = a[3] = 0u;
-        mma_bf16(c[(2 * j + h) & 3], a, bw[2 * h], bw[2 * h + 1]);
+    for (int jj = 0; jj < 4; ++jj) {
+      uint4 w0, w1, u0, u1, v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+      ld_pair(rowp, jj, w0, w1);
+      ld_pair(a0p, jj, u0, u1);
+      if (!ok0) u0 = u1 = v0;
+      if constexpr (NB > 4) {
+        ld_pair(a1p, jj, v0, v1);
+        if (!ok1) v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
       }
+      { const uint32_t a[4] = {u0.x, v0.x, u0.y, v0.y}; mma_bf16(c[0], a, w0.x, w0.y); }
+      { const uint32_t a[4] = {u0.z, v0.z, u0.w, v0.w}; mma_bf16(c[1], a, w0.z, w0.w); }
+      { const uint32_t a[4] = {u1.x, v1.x, u1.y, v1.y}; mma_bf16(c[2], a, w1.x, w1.y); }
+      { const uint32_t a[4] = {u1.z, v1.z, u1.w, v1.w}; mma_bf16(c[3], a, w1.z, w1.w); }
     }
   }
 
   // A fragments from hi/lo bf16 planes (no conversion): token b's row of this warp's slice in
-  // plane hl starts at element base + hl * plane + b * row; tokens outside bmask are zero
+  // plane hl starts at element base + hl * plane + b * row (16-byte aligned); tokens outside
+  // bmask are zero. One 16-byte load per 32-column group (the column map above).
   __device__ __forceinline__ void ld_frags_hl(const uint16_t* base, size_t plane, size_t row, uint32_t bmask,
                                               uint32_t (&af)[16][AR]) const {
     const int g8 = lane >> 2, t4 = lane & 3, hl = g8 & 1, b0 = g8 >> 1;
     const bool v0 = (bmask >> b0) & 1u;
-    const uint32_t* s0 = reinterpret_cast<const uint32_t*>(base + hl * plane + (size_t)b0 * row) + t4;
+    const uint4* s0 = reinterpret_cast<const uint4*>(base + hl * plane + (size_t)b0 * row) + t4;
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      af[s][0] = v0 ? __ldcg(s0 + 8 * s) : 0u;
-      af[s][1] = v0 ? __ldcg(s0 + 8 * s + 4) : 0u;
+    for (int j = 0; j < 8; ++j) {
+      const uint4 w = v0 ? __ldcg(s0 + 4 * j) : make_uint4(0u, 0u, 0u, 0u);
+      af[2 * j][0] = w.x; af[2 * j][1] = w.y; af[2 * j + 1][0] = w.z; af[2 * j + 1][1] = w.w;
     }
     if constexpr (AR == 4) {
       const bool v1 = (bmask >> (b0 + 4)) & 1u;
-      const uint32_t* s1 = reinterpret_cast<const uint32_t*>(base + hl * plane + (size_t)(b0 + 4) * row) + t4;
+      const uint4* s1 = reinterpret_cast<const uint4*>(base + hl * plane + (size_t)(b0 + 4) * row) + t4;
 #pragma unroll
-      for (int s = 0; s < 16; ++s) {
-        af[s][2] = v1 ? __ldcg(s1 + 8 * s) : 0u;
-        af[s][3] = v1 ? __ldcg(s1 + 8 * s + 4) : 0u;
+      for (int j = 0; j < 8; ++j) {
+        const uint4 w = v1 ? __ldcg(s1 + 4 * j) : make_uint4(0u, 0u, 0u, 0u);
+        af[2 * j][2] = w.x; af[2 * j][3] = w.y; af[2 * j + 1][2] = w.z; af[2 * j + 1][3] = w.w;
       }
     }
   }
@@ -1333,7 +1363,7 @@ struct Consumer {
         if (!t_ready) t_ready = gtimer();
         const uint8_t* st = acquire();
         if (!st) return;
-        if (active) mma_rows((uint32_t)__cvta_generic_to_shared(st), g, rg, ks, af[hold ? (cs & 1) : 0], c);
+        if (active) mma_rows(st, g, rg, ks, af[hold ? (cs & 1) : 0], c);
         release();
       }
       const uint32_t pid = post_pass(active, c);
@@ -1352,7 +1382,7 @@ struct Consumer {
     const Geo g = geo_of(p.I);
     const int rg = warp / g.KW, ks = warp % g.KW;
     const bool active = rg < g.RG;
-    const int na = m.rc_n, hrst = p.I * 2 + 16;
+    const int na = m.rc_n;
     float c[4][4] = {};
     // per routed expert: its weight stage, then its activation stage (both held at once)
     for (int a = 0; a < na; ++a) {
@@ -1360,8 +1390,7 @@ struct Consumer {
       const uint8_t* sa = sw ? acquire_at(1) : nullptr;
       if (!sa) return;
       if (active)
-        mma_rows_sa((uint32_t)__cvta_generic_to_shared(sw), g, rg, ks, (uint32_t)__cvta_generic_to_shared(sa), hrst,
-                    m.rc_mask[a], c);
+        mma_rows_sa(sw, g, rg, ks, sa, m.rc_mask[a], c);
       release();
       release();
     }
