@@ -180,8 +180,9 @@ mk_status mk_get_activations(const mk_ctx* ctx, mk_activations* out);
  * planned bytes per SM. Opcodes: 1 router, 2 QKV, 3 attention, 4 expert gate/up, 5 O-proj,
  * 6 expert down, 7 LM head. At batch 1 (n_sm >= 8), when the attention branch streams at most
  * 1.5x the expert branch's bytes, the two branches of each layer run on disjoint SM partitions:
- * SMs [0, n_attn_sm) take QKV, attention and O-proj, the others router, gate/up and down;
- * otherwise n_attn_sm == n_sm and every SM takes both. The LM head spreads over all SMs.
+ * SMs [0, n_attn_sm) take attention and O-proj, the others router, gate/up and down, and QKV
+ * spreads over all SMs; otherwise n_attn_sm == n_sm and every SM takes both branches. The LM
+ * head spreads over all SMs.
  * Errors: MK_ERR_INVALID_ARG. */
 typedef struct {
   int32_t n_tasks, n_counters, max_chunks, n_lm_sm, n_op_launches, n_attn_sm;

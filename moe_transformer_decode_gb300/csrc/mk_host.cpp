@@ -297,6 +297,16 @@ struct Assigner {
     }
     for (auto& k : keep) heap.push(k);
   }
+  // onto the least-loaded SM of any partition, except those marked in `skip`
+  int put_any(const Task& t, long long bytes, const std::vector<char>& skip) {
+    int best = -1;
+    for (int s = 0; s < n_sm; ++s)
+      if (!skip[s] && (best < 0 || std::make_tuple(load[s], total[s], s) < std::make_tuple(load[best], total[best], best)))
+        best = s;
+    if (best < 0) best = 0;
+    put_on(t, bytes, best);
+    return best;
+  }
   int put(const Task& t, long long bytes, int pt) {
     auto& heap = heaps[pt];
     const int s = std::get<2>(heap.top());
@@ -381,8 +391,11 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   // about two QKV tasks per attention SM and two expert gate/up tasks per expert SM, per layer
   // (whole stages each)
   const int upg_ = (G + 2) * (d / 8);
-  // (rounded up, so no SM of a partition gets a third)
-  int qkv_per_task = std::max(1, (nkv * upg_ + 2 * n_attn - 1) / (2 * n_attn));
+  // (rounded up, so no SM of a partition gets a third). When the SMs are partitioned, QKV
+  // runs on every SM, about one task each: it needs only the layer's input, and the expert
+  // SMs would otherwise wait idle for the routing.
+  const int qkv_tasks = n_attn < n_sm ? n_sm - (E + gh.RS - 1) / gh.RS : 2 * n_attn;
+  int qkv_per_task = std::max(1, (nkv * upg_ + qkv_tasks - 1) / qkv_tasks);
   qkv_per_task = std::max(gh.RG, (qkv_per_task + gh.RG - 1) / gh.RG * gh.RG);
   const int gu_per_task = std::max(1, (maxa * tiles + 2 * n_moe - 1) / (2 * n_moe));
   const long long row_h = 2LL * H;
@@ -392,9 +405,19 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   // Each phase (the tasks of one op kind in a layer) becomes ready at once, after a dependency
   // every SM shares, so it is balanced on its own: loads restart at every phase (ties still go
   // to the SM with the fewest bytes over the step).
-  auto emit = [&](std::vector<std::pair<Task, long long>>& ts, int pt) {
+  // SMs holding a router task of the current layer (QKV avoids them: one of them computes the
+  // routing right after its router task)
+  std::vector<char> router_sm(n_sm, 0);
+  auto emit = [&](std::vector<std::pair<Task, long long>>& ts, int pt) {  // pt < 0: any SM
     as.new_layer();
-    for (auto& x : ts) as.put(x.first, x.second, pt);
+    for (auto& x : ts) {
+      if (pt < 0) {
+        as.put_any(x.first, x.second, router_sm);
+      } else {
+        const int s = as.put(x.first, x.second, pt);
+        if (x.first.op == OP_ROUTER) router_sm[s] = 1;
+      }
+    }
     std::vector<std::vector<Task>> lists(n_sm);
     for (size_t i = 0; i < ts.size(); ++i) lists[i % n_sm].push_back(ts[i].first);
     if (!ts.empty()) per_op.push_back(std::move(lists));
@@ -403,6 +426,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
 
   std::vector<std::pair<Task, long long>> ts;
   for (int l = 0; l < L; ++l) {
+    std::fill(router_sm.begin(), router_sm.end(), 0);
     as.new_layer();
     // Per layer, in an order that is a topological order of the dependencies (so no SM can
     // wait on work listed after its own): router, QKV, expert gate/up (needs the routing),
@@ -426,7 +450,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
                       std::min(qkv_per_task, (g + 1) * upg - u) * 8 * row_h});
       cnt[cmap.qkv(l, g)] = n;
     }
-    emit(ts, PA);
+    emit(ts, n_attn < n_sm ? -1 : PA);
     // expert gate/up: units u = tile * maxa + active_rank
     int n_gu = 0;
     for (int u = 0; u < maxa * tiles; u += gu_per_task, ++n_gu) {

@@ -91,20 +91,23 @@ def test_plan_rejects_bad_arguments():
 @pytest.mark.parametrize("w,n_sm", [(W.M30B_BS1, 152), (W.M30B_BS8, 152), (W.SMALL, 152), (W.TINY, 152),
                                     (W.TINY, 7)])
 def test_plan_splits_branches_over_disjoint_sms(w, n_sm):
-    """At batch 1, attention-branch tasks (QKV, attention, O-proj) and expert-branch tasks
-    (router, gate/up, down) sit on disjoint SM partitions sized by their bytes; larger batches
-    and very small grids do not split."""
+    """At batch 1, attention tasks (attention, O-proj) and expert-branch tasks (router, gate/up,
+    down) sit on disjoint SM partitions, and QKV (which needs only the layer's input) spreads
+    over every SM, at most one task each; larger batches and very small grids do not split."""
     ctx = W.context_lengths(w)
     info, tasks, begin, load = B.mk_plan_schedule(cfg_of(w, int(np.max(ctx)) // 16 + 64), n_sm, ctx)
     na = info.n_attn_sm
     owner = np.searchsorted(begin, np.arange(info.n_tasks), side="right") - 1
-    attn = np.isin(tasks["op"], [OP_QKV, OP_ATTN, OP_O])
+    attn = np.isin(tasks["op"], [OP_ATTN, OP_O])
     moe = np.isin(tasks["op"], [OP_ROUTER, OP_GU, OP_DOWN])
     if n_sm < 8 or w.B > 1:
         assert na == n_sm
         return
     assert 0 < na < n_sm
     assert np.all(owner[attn] < na) and np.all(owner[moe] >= na)
+    for l in (0, w.L - 1):
+        q = owner[(tasks["op"] == OP_QKV) & (tasks["layer"] == l)]
+        assert np.bincount(q, minlength=n_sm).max() <= 1
     if w.H < 2048:  # the small models have fewer tasks than SMs
         return
     # every SM of a partition gets work of its branch in every layer
