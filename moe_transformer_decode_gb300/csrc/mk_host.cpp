@@ -364,9 +364,10 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   int n_attn = n_sm;  // every SM takes both branches
   if (n_sm >= 8 && B == 1 && attn_bytes <= 1.5 * moe_bytes) {
     // The expert branch has one more dependent hand-off per layer (router -> routing -> gate/up ->
-    // down) than the attention branch, so it gets more than its byte share: 0.75 x the
-    // attention branch's byte share (measured best among 0.55-1.0 on the 30B-shaped model).
-    n_attn = (int)std::lround(0.75 * n_sm * attn_bytes / (attn_bytes + moe_bytes));
+    // down) than the attention branch, and QKV runs on every SM, so the attention partition is
+    // 0.65 x the attention branch's byte share (measured: flat between 0.55 and 0.7 on the
+    // 30B-shaped model, worse above).
+    n_attn = (int)std::lround(0.65 * n_sm * attn_bytes / (attn_bytes + moe_bytes));
     n_attn = std::min(std::max(n_attn, 1), n_sm - 1);
   }
   std::vector<int> part(n_sm, 0);
@@ -375,10 +376,22 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   const int n_moe = n_attn < n_sm ? n_sm - n_attn : n_sm;
   P.n_attn_sm = n_attn;
 
-  // attention chunks: about one (sequence, group, chunk) task per attention SM, whole stages each
+  // attention chunks: whole stages each, the smallest size for which the (sequence, group,
+  // chunk) tasks number at most one per attention SM (a second task on one SM would double the
+  // attention phase); unless that size is impractically large (more than twice the even share)
   int cp = (int)((group_pages + n_attn - 1) / n_attn);
   cp = std::max(cp, pps);
   cp = (cp + pps - 1) / pps * pps;
+  auto n_attn_tasks = [&](int c) {
+    long long n = 0;
+    for (int b = 0; b < B; ++b) n += (long long)nkv * std::max(1, (npg[b] + c - 1) / c);
+    return n;
+  };
+  for (int c = cp; c <= 2 * cp; c += pps)
+    if (n_attn_tasks(c) <= n_attn) {
+      cp = c;
+      break;
+    }
   P.chunk_pages.assign(B, cp);
   P.n_chunks.assign(B, 1);
   P.max_chunks = 1;
