@@ -488,11 +488,21 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
       per_op.push_back(std::move(lists));
     }
     for (int g = 0; g < nkv; ++g) cnt[cmap.attn(l, g)] = B;
-    // expert down rows over all active experts
+    // expert down rows over all active experts: blocks of RS rows while they number at most one
+    // per expert SM; else one task per expert SM of 8-row blocks (passes of RS rows), so that
+    // no SM takes two tasks while another takes one (the layer ends with its last down task)
     int n_down = 0;
-    for (int r0 = 0; r0 < H; r0 += gi.RS, ++n_down)
-      ts.push_back({mkt(OP_DOWN, l, r0, std::min(gi.RS, H - r0), 0),
-                    (long long)(std::min(gi.RS, H - r0) * 2.0 * I * maxa * live)});
+    {
+      const int nb = (H + gi.RS - 1) / gi.RS, nb8 = (H + 7) / 8;
+      const int n_t = nb <= n_moe ? nb : std::min(n_moe, nb8);
+      int r0 = 0;
+      for (int i = 0; i < n_t; ++i, ++n_down) {
+        const int rows = nb <= n_moe ? gi.RS : 8 * (nb8 / n_t + (i < nb8 % n_t ? 1 : 0));
+        const int n = std::min(rows, H - r0);
+        ts.push_back({mkt(OP_DOWN, l, r0, n, 0), (long long)(n * 2.0 * I * maxa * live)});
+        r0 += n;
+      }
+    }
     emit(ts, PM);
     // O-proj: blocks of RS rows; at batch <= 4 (and at most two 2048-column chunks) a task takes
     // several blocks, reusing one load of the attention output, about one task per SM

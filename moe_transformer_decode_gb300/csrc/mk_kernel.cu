@@ -312,7 +312,7 @@ struct Misc {
   int rc_n;
   int rc_expert[kMaxActive];
   uint32_t rc_mask[kMaxActive];
-  float rc_w[kMaxActive][kMaxB];
+  alignas(16) float rc_w[kMaxActive][kMaxB];
   // producer-private: routed experts of layer pr_layer, and a window of one sequence's page ids
   int pr_n;
   int pr_expert[kMaxActive];
@@ -368,15 +368,14 @@ struct Producer {
     if (route_layer == l) return true;
     int fine = 1;
     const Route* rt = p.route + l;
-    if (lane == 0) {
-      fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l));
-      if (fine) m.pr_n = __ldcg(&rt->n_active);
-    }
+    if (lane == 0) fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.route(l));
     if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
     __syncwarp();
-    const int na = m.pr_n;
-#pragma unroll 1
-    for (int a = lane; a < na; a += 32) m.pr_expert[a] = __ldcg(&rt->expert[a]);
+    // the count and the whole list in one round of loads (entries past the count are unused)
+    const int na = __ldcg(&rt->n_active);
+#pragma unroll
+    for (int a = lane; a < kMaxActive; a += 32) m.pr_expert[a] = __ldcg(&rt->expert[a]);
+    if (lane == 0) m.pr_n = na;
     __syncwarp();
     route_layer = l;
     return true;
@@ -529,25 +528,31 @@ struct Producer {
         if (!route(l)) return false;
         const int na = m.pr_n;
         const Geo g = geo_of(p.I);
+        bool gu_done = false;
 #pragma unroll 1
-        for (int a = 0; a < na; ++a) {
-          const int e = m.pr_expert[a];
-          const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + t.a) * p.I;
-          if (!gemv_rows(W, t.b, p.I, p.I * 2)) return false;
-          // then the expert's activations: row hl * B + b holds plane hl (hi, lo) of token b.
-          // They exist once every gate/up task of the layer is done (the first weight stage
-          // above is already on its way).
-          if (a == 0) {
-            int fine = 1;
-            if (lane == 0) fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.gu(l));
-            if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
+        for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS) {  // passes of RS rows
+          const int rows = min(g.RS, t.a + t.b - r0);
+#pragma unroll 1
+          for (int a = 0; a < na; ++a) {
+            const int e = m.pr_expert[a];
+            const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + r0) * p.I;
+            if (!gemv_rows(W, rows, p.I, p.I * 2)) return false;
+            // then the expert's activations: row hl * B + b holds plane hl (hi, lo) of token b.
+            // They exist once every gate/up task of the layer is done (the first weight stage
+            // above is already on its way).
+            if (!gu_done) {
+              int fine = 1;
+              if (lane == 0) fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.gu(l));
+              if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
+              gu_done = true;
+            }
+            if (!begin((uint32_t)2 * p.B * p.I * 2)) return false;
+            const uint16_t* hp = p.h + (((size_t)l * kMaxActive + a) * 2 * kMaxB) * p.I;
+            if (lane < 2)  // plane `lane` (hi, lo): the batch's rows are consecutive
+              bulk_g2s(dst + (uint32_t)(lane * p.B * p.I * 2), hp + (size_t)lane * kMaxB * p.I, (uint32_t)p.B * p.I * 2,
+                       bar, pol);
+            end();
           }
-          if (!begin((uint32_t)2 * p.B * p.I * 2)) return false;
-          const uint16_t* hp = p.h + (((size_t)l * kMaxActive + a) * 2 * kMaxB) * p.I;
-          if (lane < 2)  // plane `lane` (hi, lo): the batch's rows are consecutive
-            bulk_g2s(dst + (uint32_t)(lane * p.B * p.I * 2), hp + (size_t)lane * kMaxB * p.I, (uint32_t)p.B * p.I * 2,
-                     bar, pol);
-          end();
         }
         return true;
       }
@@ -992,13 +997,14 @@ struct Consumer {
     if (route_layer == l) return true;
     if (!warp_wait(p, cm.route(l))) { ok = false; return false; }
     const Route* rt = p.route + l;
-    const int na = __ldcg(&rt->n_active);
-    for (int i = threadIdx.x; i < na; i += 256) {
+    // the count and the whole tables in one round of loads (rows past the count are unused)
+    if (threadIdx.x == 0) m.rc_n = __ldcg(&rt->n_active);
+    for (int i = threadIdx.x; i < kMaxActive; i += 256) {
       m.rc_expert[i] = __ldcg(&rt->expert[i]);
       m.rc_mask[i] = __ldcg(&rt->mask[i]);
     }
-    for (int i = threadIdx.x; i < na * kMaxB; i += 256) m.rc_w[i / kMaxB][i % kMaxB] = __ldcg(&rt->w[i / kMaxB][i % kMaxB]);
-    if (threadIdx.x == 0) m.rc_n = na;
+    for (int i = threadIdx.x; i < kMaxActive * kMaxB / 4; i += 256)
+      reinterpret_cast<float4*>(&m.rc_w[0][0])[i] = __ldcg(reinterpret_cast<const float4*>(&rt->w[0][0]) + i);
     if (!csync()) return false;
     route_layer = l;
     return true;
@@ -1130,92 +1136,88 @@ struct Consumer {
   // Routing of layer l by warp 0 alone, then published with one release of the route counter.
   // Per token: top-k (value descending, lower expert id first on ties), softmax over the k
   // selected logits. Then the distinct routed experts in ascending id, each with its token
-  // mask and per-token weights. Lane owns experts lane + 32 i.
+  // mask and per-token weights. Lane owns experts lane + 32 i. This runs on the critical path
+  // of every layer, so each pick is two warp reductions (redux.sync) on an order-preserving
+  // integer image of the logit, and the lists are built with ballots, not per-lane loops.
+  __device__ static __forceinline__ uint32_t order_key(float x) {
+    // +0 and -0 compare equal as logits, so both map to the image of +0
+    const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  __device__ static __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+  }
   __device__ void publish_routing(int l) {
     constexpr int NE = kMaxExperts / 32;
     const int E = p.E, K = p.topk, B = p.B;
-    float v[NB][NE];
+    uint32_t key[NB][NE];
 #pragma unroll
     for (int b = 0; b < NB; ++b)
 #pragma unroll
       for (int i = 0; i < NE; ++i) {
         const int e = lane + 32 * i;
         const float x = (b < B && e < E) ? __ldcg(&p.rlogits[((size_t)l * B + b) * E + e]) : -INFINITY;
-        v[b][i] = x == x ? x : -INFINITY;  // a NaN logit ranks last
+        // a NaN logit ranks last (with -inf); 0 marks "no expert" and is never picked
+        key[b][i] = e < E ? order_key(x == x ? x : -INFINITY) : 0u;
       }
-    uint32_t emask[NE];
+    uint32_t emask[NE];  // bit b: token b picked expert lane + 32 i
 #pragma unroll
     for (int i = 0; i < NE; ++i) emask[i] = 0u;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       if (b >= B) break;
-      float top0 = 0.f, z = 0.f;
-      uint32_t taken = 0u;  // bit i: expert lane + 32 i already picked for token b
+      float top0 = 0.f, z = 0.f, my_w = 0.f;
+      int my_id = 0;
       for (int j = 0; j < K; ++j) {
-        // every pick is a valid, distinct expert: -inf ties go to the lowest free id
-        float bv = -INFINITY;
+        uint32_t bk = 0u;
         int be = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < NE; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && !((taken >> i) & 1u) && (v[b][i] > bv || (v[b][i] == bv && e < be))) { bv = v[b][i]; be = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-        }
-#pragma unroll
         for (int i = 0; i < NE; ++i)
-          if (lane + 32 * i == be) { taken |= 1u << i; emask[i] |= 1u << b; }
+          if (key[b][i] > bk) { bk = key[b][i]; be = lane + 32 * i; }  // ascending e: ties keep the lower id
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+        const int pick = (int)__reduce_min_sync(0xffffffffu, bk == kmax ? (uint32_t)be : 0xffffffffu);
+        if ((pick & 31) == lane) {
+#pragma unroll
+          for (int i = 0; i < NE; ++i)
+            if (i == (pick >> 5)) { key[b][i] = 0u; emask[i] |= 1u << b; }
+        }
+        const float bv = key_value(kmax);
         if (j == 0) top0 = bv;
         const float w = expf(bv - top0);
         z += w;
-        if (lane == 0) { m.ids[b][j] = be; m.wk[b][j] = w; }
+        if (lane == j) { my_id = pick; my_w = w; }
       }
-      __syncwarp();
-      if (lane < K) m.wk[b][lane] /= z;
+      if (lane < K) { m.ids[b][lane] = my_id; m.wk[b][lane] = my_w / z; }
     }
-    __syncwarp();
-    // token masks per expert, then the distinct experts in ascending id (32 per round)
-#pragma unroll 1
-    for (int e = lane; e < E; e += 32) m.em[e] = 0u;
-    __syncwarp();
-#pragma unroll 1
-    for (int i = lane; i < B * K; i += 32) atomicOr(&m.em[m.ids[i / K][i % K]], 1u << (i / K));
-    __syncwarp();
+    // the distinct experts in ascending id; m.em[e] holds e's rank for the weight scatter
     Route* rt = p.route + l;
     int na = 0;
-#pragma unroll 1
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const uint32_t mask = e < E ? m.em[e] : 0u;
-      const uint32_t act = __ballot_sync(0xffffffffu, mask != 0u);
-      if (mask != 0u) {
+#pragma unroll
+    for (int i = 0; i < NE; ++i) {
+      const uint32_t act = __ballot_sync(0xffffffffu, emask[i] != 0u);
+      if (emask[i] != 0u) {
         const int r = na + __popc(act & ((1u << lane) - 1u));
-        __stcg(&rt->expert[r], e);
-        __stcg(&rt->mask[r], mask);
-#pragma unroll 1
-        for (int b = 0; b < kMaxB; ++b) {
-          float w = 0.f;
-          if (mask & (1u << b)) {
-#pragma unroll 1
-            for (int j = 0; j < K; ++j) w = m.ids[b][j] == e ? m.wk[b][j] : w;
-          }
-          __stcg(&rt->w[r][b], w);
-        }
+        __stcg(&rt->expert[r], lane + 32 * i);
+        __stcg(&rt->mask[r], emask[i]);
+        m.em[lane + 32 * i] = (uint32_t)r;
       }
       na += __popc(act);
     }
-    if (lane == 0) __stcg(&rt->n_active, na);
+    static_assert(offsetof(Route, w) % 16 == 0 && sizeof(Route) % 16 == 0, "Route rows must be 16-byte aligned");
+    float4* w4 = reinterpret_cast<float4*>(&rt->w[0][0]);
+    for (int i = lane; i < na * (kMaxB / 4); i += 32) __stcg(w4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
+    __syncwarp();
     for (int i = lane; i < B * K; i += 32) {
       const int b = i / K, j = i % K;
-      __stcg(&rt->ids[b][j], m.ids[b][j]);
-      __stcg(&rt->wk[b][j], m.wk[b][j]);
-      __stcg(&p.topk_ids[((size_t)l * B + b) * K + j], m.ids[b][j]);
-      __stcg(&p.topk_w[((size_t)l * B + b) * K + j], m.wk[b][j]);
+      const int e = m.ids[b][j];
+      const float w = m.wk[b][j];
+      __stcg(&rt->w[m.em[e]][b], w);
+      __stcg(&rt->ids[b][j], e);
+      __stcg(&rt->wk[b][j], w);
+      __stcg(&p.topk_ids[((size_t)l * B + b) * K + j], e);
+      __stcg(&p.topk_w[((size_t)l * B + b) * K + j], w);
     }
+    if (lane == 0) __stcg(&rt->n_active, na);
     __syncwarp();
     if (lane == 0) red_release_add(p.counters + cm.route(l), 1u);
   }
@@ -1383,23 +1385,34 @@ struct Consumer {
     const int rg = warp / g.KW, ks = warp % g.KW;
     const bool active = rg < g.RG;
     const int na = m.rc_n;
-    float c[4][4] = {};
-    // per routed expert: its weight stage, then its activation stage (both held at once)
-    for (int a = 0; a < na; ++a) {
-      const uint8_t* sw = acquire();
-      const uint8_t* sa = sw ? acquire_at(1) : nullptr;
-      if (!sa) return;
-      if (active)
-        mma_rows_sa(sw, g, rg, ks, sa, m.rc_mask[a], c);
-      release();
-      release();
-    }
-    run_epi(post_pass(active, c), g, [&](auto&& R) {
-      for (int i = lane; i < t.b * NB; i += 32) {
-        const int rr = i / NB, b = i % NB;
-        if (b < p.B) __stcg(&p.moe_out[((size_t)l * p.B + b) * p.H + t.a + rr], R(rr, b));
+    auto epi = [&](uint32_t pid, int r0, int rows) {
+      run_epi(pid, g, [&](auto&& R) {
+        for (int i = lane; i < rows * NB; i += 32) {
+          const int rr = i / NB, b = i % NB;
+          if (b < p.B) __stcg(&p.moe_out[((size_t)l * p.B + b) * p.H + r0 + rr], R(rr, b));
+        }
+      });
+    };
+    uint32_t prev = 0;
+    int pr0 = -1, prows = 0;
+    for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS) {  // passes of RS rows
+      const int rows = min(g.RS, t.a + t.b - r0);
+      float c[4][4] = {};
+      // per routed expert: its weight stage, then its activation stage (both held at once)
+      for (int a = 0; a < na; ++a) {
+        const uint8_t* sw = acquire();
+        const uint8_t* sa = sw ? acquire_at(1) : nullptr;
+        if (!sa) return;
+        if (active)
+          mma_rows_sa(sw, g, rg, ks, sa, m.rc_mask[a], c);
+        release();
+        release();
       }
-    });
+      const uint32_t pid = post_pass(active, c);
+      if (pr0 >= 0) epi(prev, pr0, prows);
+      prev = pid, pr0 = r0, prows = rows;
+    }
+    if (pr0 >= 0) epi(prev, pr0, prows);
     if (ok) release_counter(cm.layer(l));
   }
 

@@ -145,6 +145,13 @@ def test_greedy_loop_matches_single_steps():
     b.close()
 
 
+def test_30b_shape_4_layers_bs1_ctx8k_per_layer():
+    """The production layer shape at batch 1 (4 of 48 layers): the attention/expert SM partition,
+    attention chunks sized to the partition, and expert-down tasks of 8-row blocks in passes of
+    one stage's rows (more row blocks than expert SMs), checked layer by layer."""
+    _run(W.M30B_L4, 2, per_layer=True)
+
+
 @pytest.mark.slow
 def test_30b_bs1_ctx8k_full_size():
     _run(W.M30B_BS1, 2)

@@ -63,7 +63,15 @@ def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
         assert sorted(_ranges(o).tolist()) == list(range(w.H))
         assert np.all((o["b"] % rs_o == 0) | (o["a"] + o["b"] == w.H))
         dn = t[t["op"] == OP_DOWN]
-        assert sorted(_ranges(dn).tolist()) == list(range(w.H)) and np.all(dn["b"] <= rows_per_stage(w.I))
+        assert sorted(_ranges(dn).tolist()) == list(range(w.H))
+        # down: blocks of one stage's rows, or (when those outnumber the expert SMs) one task per
+        # expert SM made of 8-row blocks, so no expert SM takes two down tasks
+        n_moe = n_sm - info.n_attn_sm if info.n_attn_sm < n_sm else n_sm
+        rs_d = rows_per_stage(w.I)
+        if -(-w.H // rs_d) <= n_moe:
+            assert np.all(dn["b"] <= rs_d)
+        else:
+            assert len(dn) <= n_moe and np.all((dn["b"] % 8 == 0) | (dn["a"] + dn["b"] == w.H))
     lm = tasks[tasks["op"] == OP_LM]
     assert sorted(_ranges(lm).tolist()) == list(range(w.V))
     assert np.all(lm["flags"] & 2) and len(lm) == info.n_lm_sm and sorted(lm["c"].tolist()) == list(range(len(lm)))
