@@ -601,7 +601,7 @@ extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* 
   bool okm = dalloc(&c->d_tasks, P.all.size()) == cudaSuccess && dalloc(&c->d_sm_begin, P.begin.size()) == cudaSuccess &&
              dalloc(&c->d_cnt, P.cnt.size()) == cudaSuccess && dalloc(&c->d_chunk_pages, B) == cudaSuccess &&
              dalloc(&c->d_n_chunks, B) == cudaSuccess && dalloc(&c->apart, part) == cudaSuccess &&
-             dalloc(&c->counters, P.cnt.size()) == cudaSuccess;
+             dalloc(&c->counters, P.cnt.size() * kCounterStride) == cudaSuccess;
   if (!okm) {
     cudaGetLastError();
     free_schedule(c);
@@ -612,7 +612,7 @@ extern "C" mk_status mk_build_schedule(mk_ctx* c, int32_t batch, const int32_t* 
   CK(cudaMemcpy(c->d_cnt, P.cnt.data(), P.cnt.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
   CK(cudaMemcpy(c->d_chunk_pages, P.chunk_pages.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice));
   CK(cudaMemcpy(c->d_n_chunks, P.n_chunks.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice));
-  CK(cudaMemset(c->counters, 0, P.cnt.size() * sizeof(uint32_t)));
+  CK(cudaMemset(c->counters, 0, P.cnt.size() * kCounterStride * sizeof(uint32_t)));
   CK(cudaMemset(c->status, 0, ST_WORDS * sizeof(int32_t)));
   c->n_tasks = P.n_tasks;
   c->n_counters = (int)P.cnt.size();
@@ -755,7 +755,7 @@ extern "C" mk_status mk_status_sync(mk_ctx* c) {
   c->err = buf;
   cudaMemset(c->status, 0, ST_WORDS * sizeof(int32_t));
   *(volatile int32_t*)c->status_host = 0;
-  if (c->counters) cudaMemset(c->counters, 0, (size_t)c->n_counters * sizeof(uint32_t));
+  if (c->counters) cudaMemset(c->counters, 0, (size_t)c->n_counters * kCounterStride * sizeof(uint32_t));
   c->epoch = 0;
   cudaDeviceSynchronize();
   return (mk_status)st[ST_CODE];

@@ -22,6 +22,9 @@ static_assert(kProducerRegs * 128 + kConsumerRegs * 256 <= (65536 / kThreads) / 
 constexpr int kStagePayload = 32768;                 // data bytes of a ring stage
 constexpr int kStageBytes = kStagePayload;           // ring slot
 constexpr int kStages = 6;
+// Counters sit kCounterStride words (128 bytes) apart, so the lines that waiting warps poll spread
+// over the L2 slices instead of all landing on one.
+constexpr int kCounterStride = 32;
 constexpr int kMaxB = 8;
 constexpr int kMaxK = 8;
 constexpr int kMaxActive = kMaxB * kMaxK;  // distinct experts a batch can route to

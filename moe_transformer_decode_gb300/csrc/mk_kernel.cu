@@ -102,6 +102,17 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// explicit shared-memory loads (a generic load of shared data waits on the long scoreboard)
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -177,7 +188,7 @@ struct WaitClock {
 // single-thread bounded wait; false on timeout or abort
 __device__ bool wait_counter(const Params& p, int idx) {
   const uint32_t tgt = target_of(p, idx);
-  const uint32_t* c = p.counters + idx;
+  const uint32_t* c = p.counters + (size_t)idx * kCounterStride;
   WaitClock wc;
   for (;;) {
     const uint32_t v = ld_acquire(c);
@@ -188,7 +199,7 @@ __device__ bool wait_counter(const Params& p, int idx) {
 // whole-warp wait (every lane performs the acquire)
 __device__ bool warp_wait(const Params& p, int idx) {
   const uint32_t tgt = target_of(p, idx);
-  const uint32_t* c = p.counters + idx;
+  const uint32_t* c = p.counters + (size_t)idx * kCounterStride;
   WaitClock wc;
   for (;;) {
     const uint32_t v = ld_acquire(c);
@@ -319,7 +330,10 @@ struct Misc {
   int pr_ids[kIdCache];
   // batch 1: the normalized input's mma fragments (only lanes 0-7 hold data: hi and lo of
   // token 0), per warp and k-step
-  alignas(16) uint2 nf1[kConsumerWarps][16][8];
+  // batch 1: per warp, lanes 0-7 each own 128 bytes holding their (a0, a2) fragment registers of
+  // k-steps 0-15; the 16-byte chunk of k-steps (2 j, 2 j + 1) sits at chunk j ^ lane, so the eight
+  // lanes' 16-byte loads of one pair hit distinct banks
+  alignas(16) uint2 nf1[kConsumerWarps][8][16];
   // per-warp LM argmax candidates per token
   float lmw_v[kConsumerWarps][kMaxB];
   int lmw_i[kConsumerWarps][kMaxB];
@@ -770,7 +784,7 @@ struct Consumer {
         for (int s = 0; s < 16; ++s) {
           const float4 v = *reinterpret_cast<const float4*>(xw + 32 * (s >> 1) + 8 * t4 + 4 * (s & 1));
           if constexpr (NB == 1) {
-            m.nf1[warp][s][lane] = make_uint2(pack_part(v.x, v.y, hl), pack_part(v.z, v.w, hl));
+            m.nf1[warp][lane][2 * ((s >> 1) ^ lane) + (s & 1)] = make_uint2(pack_part(v.x, v.y, hl), pack_part(v.z, v.w, hl));
           } else {
             nf[s][0] = pack_part(v.x, v.y, hl);
             nf[s][1] = pack_part(v.z, v.w, hl);
@@ -835,8 +849,9 @@ struct Consumer {
   // slice start + 16 t); odd rows load the two groups in the other order (distinct banks)
   __device__ __forceinline__ void ld_pair(const uint8_t* rowp, int jj, uint4& w0, uint4& w1) const {
     const int odd = (lane >> 2) & 1;
-    const uint4 x = *reinterpret_cast<const uint4*>(rowp + (2 * jj + odd) * 64);
-    const uint4 y = *reinterpret_cast<const uint4*>(rowp + (2 * jj + (odd ^ 1)) * 64);
+    const uint32_t ra = (uint32_t)__cvta_generic_to_shared(rowp);
+    const uint4 x = lds128(ra + (2 * jj + odd) * 64);
+    const uint4 y = lds128(ra + (2 * jj + (odd ^ 1)) * 64);
     w0 = odd ? y : x;
     w1 = odd ? x : y;
   }
@@ -916,11 +931,11 @@ struct Consumer {
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&m.gfree[buf]));
   }
-  // batch 1: as mma_rows, A fragments of the normalized input from m.nf1 (lanes 0-7 hold the
-  // hi and lo parts of token 0; every other lane's are zero)
+  // batch 1: as mma_rows, A fragments of the normalized input from m.nf1, two k-steps per 16-byte
+  // load (lanes 0-7 hold the hi and lo parts of token 0; every other lane's are zero)
   __device__ __forceinline__ void mma_rows_nf1(const uint8_t* st, const Geo& g, int rg, int ks, float (&c)[4][4]) const {
     const uint8_t* rowp = b_row(st, g, rg, ks);
-    const uint2* fr = &m.nf1[warp][0][lane & 7];
+    const uint32_t fr = (uint32_t)__cvta_generic_to_shared(&m.nf1[warp][lane & 7][0]);
     const bool has = lane < 8;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
@@ -928,10 +943,11 @@ struct Consumer {
       ld_pair(rowp, jj, w0, w1);
       const uint32_t bw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint2 f = has ? fr[(4 * jj + h) * 8] : make_uint2(0u, 0u);
-        const uint32_t a[4] = {f.x, 0u, f.y, 0u};
-        mma_bf16(c[h], a, bw[2 * h], bw[2 * h + 1]);
+      for (int hp = 0; hp < 2; ++hp) {  // k-steps 4 jj + 2 hp and 4 jj + 2 hp + 1
+        const uint4 f = has ? lds128(fr + (((2 * jj + hp) ^ (lane & 7)) & 7) * 16) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t a0[4] = {f.x, 0u, f.y, 0u}, a1[4] = {f.z, 0u, f.w, 0u};
+        mma_bf16(c[2 * hp], a0, bw[4 * hp], bw[4 * hp + 1]);
+        mma_bf16(c[2 * hp + 1], a1, bw[4 * hp + 2], bw[4 * hp + 3]);
       }
     }
   }
@@ -954,13 +970,13 @@ struct Consumer {
   __device__ void release_counter(int idx) {
     if (!csync()) return;
     // the barrier orders every consumer's writes before thread 0's gpu-scope release
-    if (threadIdx.x == 0) red_release_add(p.counters + idx, 1u);
+    if (threadIdx.x == 0) red_release_add(p.counters + (size_t)idx * kCounterStride, 1u);
   }
   // arrival on `idx`; true in every consumer thread of the task that arrived last
   __device__ bool arrive_last(int idx, int count) {
     if (!csync()) return false;
     if (threadIdx.x == 0) {
-      const uint32_t old = atom_acq_rel_add(p.counters + idx, 1u);
+      const uint32_t old = atom_acq_rel_add(p.counters + (size_t)idx * kCounterStride, 1u);
       m.flag = ((old + 1u) % (uint32_t)count) == 0u;
     }
     if (!csync()) return false;
@@ -1129,7 +1145,7 @@ struct Consumer {
     if (!csync()) return false;
     if (warp != 0) return false;
     uint32_t last = 0;
-    if (lane == 0) last = ((atom_acq_rel_add(p.counters + idx, 1u) + 1u) % (uint32_t)count) == 0u;
+    if (lane == 0) last = ((atom_acq_rel_add(p.counters + (size_t)idx * kCounterStride, 1u) + 1u) % (uint32_t)count) == 0u;
     return __shfl_sync(0xffffffffu, last, 0) != 0u;
   }
 
@@ -1219,7 +1235,7 @@ struct Consumer {
     }
     if (lane == 0) __stcg(&rt->n_active, na);
     __syncwarp();
-    if (lane == 0) red_release_add(p.counters + cm.route(l), 1u);
+    if (lane == 0) red_release_add(p.counters + (size_t)cm.route(l) * kCounterStride, 1u);
   }
 
   __device__ void op_qkv(const Task& t) {

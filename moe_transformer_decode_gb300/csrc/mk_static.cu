@@ -161,7 +161,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_we
   const size_t o_moe = cv.take<float>(L * B * H), o_route = cv.take<Route>(L);
   const size_t o_lmv = cv.take<float>((size_t)ds.n_sm * kMaxB), o_lmi = cv.take<int32_t>((size_t)ds.n_sm * kMaxB);
   const size_t o_tki = cv.take<int32_t>(L * B * m.top_k), o_tkw = cv.take<float>(L * B * m.top_k);
-  const size_t o_cnt = cv.take<uint32_t>(P.cnt.size()), o_status = cv.take<int32_t>(ST_WORDS);
+  const size_t o_cnt = cv.take<uint32_t>(P.cnt.size() * kCounterStride), o_status = cv.take<int32_t>(ST_WORDS);
   const size_t o_rope = cv.take<float2>((size_t)max_pos * (d / 2));
   const size_t o_tasks = cv.take<Task>((size_t)P.n_tasks), o_begin = cv.take<int32_t>((size_t)ds.n_sm + 1);
   const size_t o_cps = cv.take<int32_t>(P.cnt.size());
@@ -200,7 +200,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_we
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(s + o_nch, P.n_chunks.data(), B * sizeof(int32_t), cudaMemcpyHostToDevice, st);
   // the scratch keeps the previous call's contents: counters and status must start at zero
-  if (e == cudaSuccess) e = cudaMemsetAsync(s + o_cnt, 0, P.cnt.size() * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s + o_cnt, 0, P.cnt.size() * kCounterStride * sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(s + o_status, 0, ST_WORDS * sizeof(int32_t), st);
   if (e != cudaSuccess) {
     set_msg(msg, msg_len, cudaGetErrorString(e));
