@@ -48,6 +48,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -211,7 +220,7 @@ __device__ bool warp_wait(const Params& p, int idx) {
 }
 // bounded mbarrier wait
 __device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   WaitClock wc;
   for (;;) {  // suspended between checks, so waiting warps leave the issue slots to working ones
     if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
@@ -222,6 +231,7 @@ __device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity) {
 // For the consumer warps' own barrier: re-test with the default short blocking wait instead of
 // a long suspend, so the warps resume as soon as the last one arrives.
 __device__ bool mbar_wait_cta(const Params& p, uint32_t bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
   WaitClock wc;
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
