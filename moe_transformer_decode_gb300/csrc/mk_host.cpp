@@ -633,12 +633,13 @@ static mk_status tensor_maps(mk_ctx* c, const mk_kv_pages* kv) {
   const mk_model_cfg& m = c->cfg;
   const uint64_t rows = (uint64_t)m.n_layers * kv->num_pages * m.n_kv_heads * kPage;
   if (rows >= (1ull << 31)) return fail(c, MK_ERR_UNSUPPORTED, "KV pool too large for 32-bit TMA coordinates");
-  cuuint64_t dims[2] = {(cuuint64_t)m.head_dim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)m.head_dim * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
-  cuuint32_t estr[2] = {1, 1};
+  const cuuint32_t halves = (cuuint32_t)m.head_dim / 64;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, halves};
+  cuuint64_t strides[2] = {(cuuint64_t)m.head_dim * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)kPage, halves};
+  cuuint32_t estr[3] = {1, 1, 1};
   for (int i = 0; i < 2; ++i) {
-    CUresult r = c->encode(i ? &c->tm.v : &c->tm.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, i ? kv->v : kv->k, dims,
+    CUresult r = c->encode(i ? &c->tm.v : &c->tm.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, i ? kv->v : kv->k, dims,
                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(c, MK_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pool");

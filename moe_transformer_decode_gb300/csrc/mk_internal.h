@@ -139,7 +139,10 @@ struct Plan {
 mk_status plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_t* seq_lens, Plan& P);
 
 struct TensorMaps {
-  CUtensorMap k, v;  // KV pools as 2D [rows][head_dim] bf16, box {64, 16}, 128B swizzle
+  // KV pools as 3D {64, rows, head_dim / 64} bf16 views (a row is 2 head_dim bytes, a 64-wide
+  // half of it 128 bytes), box {64, 16, head_dim / 64}, 128B swizzle: one copy lands a page's
+  // rows as [half][row][128 bytes]
+  CUtensorMap k, v;
 };
 
 }  // namespace mk

@@ -75,11 +75,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar), "l"(pol)
       : "memory");
 }
-// 2D tiled tensor copy global -> shared (x: innermost coordinate in elements), with an L2 cache policy
-__device__ __forceinline__ void tma_2d_g2s(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar, uint64_t pol) {
+// 3D tiled tensor copy global -> shared (coordinates innermost first), with an L2 cache policy
+__device__ __forceinline__ void tma_3d_g2s(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar,
+                                           uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
       : "memory");
 }
 // L2 policy for data read once per step (weights, KV pages): evicted first, so that the code,
@@ -503,16 +504,17 @@ struct Producer {
           if (!(id_b == b && s0 >= id_p0 && s0 + np <= id_p0 + id_n)) fill_ids(b, s0, min(kIdCache, ar.cp1 - s0));
           const int* ids = m.pr_ids + (s0 - id_p0);
           if (!begin((uint32_t)np * 2 * halves * 2048)) return false;
-          // copy j: page j / (2 halves), K (0) or V (1), half h. An invalid page (reported when
-          // its id was read) loads as zeros: a tile load at an out-of-range row fills the box,
-          // so the stage never holds stale bytes.
-          const int per = 2 * halves;
-          if (lane < np * per) {
-            const int i = lane / per, kv = (lane / halves) & 1, h = lane % halves;
+          // copy j: page j / 2, K (0) or V (1): one 3D box of the page's 16 rows x all head-dim
+          // halves (each half 16 x 128 bytes, 128-byte swizzled). A bulk copy costs about the
+          // same to issue whatever its size, so one copy per page and pool instead of one per
+          // half. An invalid page (reported when its id was read) loads as zeros: a tile load at
+          // an out-of-range row fills the box, so the stage never holds stale bytes.
+          if (lane < np * 2) {
+            const int i = lane / 2, kv = lane & 1;
             const int id = ids[i];
             const int row = id >= 0 ? ((l * p.num_pages + id) * p.nkv + g) * kPage : -kPage;
-            const uint32_t pb = dst + (uint32_t)i * 4096 * halves + (uint32_t)(kv * halves + h) * 2048;
-            tma_2d_g2s(pb, kv ? &tm.v : &tm.k, h * 64, row, bar, pol);
+            const uint32_t pb = dst + (uint32_t)i * 4096 * halves + (uint32_t)(kv * halves) * 2048;
+            tma_3d_g2s(pb, kv ? &tm.v : &tm.k, 0, row, 0, bar, pol);
           }
           end();
         }
@@ -1513,8 +1515,11 @@ struct Consumer {
     if (!warp_wait(p, cm.qkv(l, g))) { ok = false; return; }
     t_ready = gtimer();
     const AttnRange ar = attn_range(m.st_pos[b], m.st_cpp[b], m.st_nch[b], t.c);
+    // warp (pi, sp) takes page pi of every stage s with s % npar == sp, over the whole head dim
+    // (2 stage parities at d = 128, 1 at d = 64), so no two warps compute the same scores
     const int pps = attn_pps(p), halves = p.d / 64, ksteps = p.d / 16;
-    const int pi = warp % pps, dp = warp / pps;
+    const int npar = kConsumerWarps / pps;
+    const int pi = warp % pps, sp = warp / pps;
     const int head = lane >> 2, tig = lane & 3;
     const float qscale = rsqrtf((float)p.d) * 1.4426950408889634f;  // scores in log2 units
     uint32_t qa[8][4];
@@ -1566,9 +1571,9 @@ struct Consumer {
       }
     }
     float mrun = -INFINITY, lsum = 0.f;
-    float oacc[8][4];
+    float oacc[16][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 16; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) oacc[i][j] = 0.f;
 
@@ -1578,7 +1583,7 @@ struct Consumer {
       const uint8_t* st = acquire();
       if (!st) return;
       const int page = ar.cp0 + s * pps + pi;
-      if (page < ar.cp1) {
+      if (s % npar == sp && page < ar.cp1) {
         const uint32_t kt = smem_addr(st) + (uint32_t)pi * 4096 * halves;
         const uint32_t vt = kt + (uint32_t)halves * 2048;
         float sc[2][4];
@@ -1617,7 +1622,7 @@ struct Consumer {
           const float alpha = exp2f(mrun - mnew);
           lsum *= alpha;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
+          for (int i = 0; i < 16; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) oacc[i][j] *= alpha;
           mrun = mnew;
@@ -1633,8 +1638,9 @@ struct Consumer {
           split_pack(pr[0][0], pr[0][1], pa[0], pa[1]);
           split_pack(pr[1][0], pr[1][1], pa[2], pa[3]);
 #pragma unroll
-          for (int c2 = 0; c2 < 4; ++c2) {  // two 8-wide d tiles per ldmatrix.x4.trans
-            const int chunk = dp * 8 + c2 * 2 + (mi >> 1);
+          for (int c2 = 0; c2 < 8; ++c2) {  // two 8-wide d tiles per ldmatrix.x4.trans
+            if (c2 >= ksteps) break;
+            const int chunk = c2 * 2 + (mi >> 1);
             const int prow = (mi & 1) * 8 + rr;
             const uint32_t addr = vt + (chunk >> 3) * 2048 + prow * 128 + (((chunk & 7) ^ (prow & 7)) << 4);
             uint32_t bv[4];
@@ -1650,35 +1656,42 @@ struct Consumer {
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
 
-    // merge the warps that share a d range (different pages), using the last slot as scratch
+    // merge the 8 warps (disjoint pages) in rounds of 64 head dims, using the last slot as scratch
     const size_t pidx = (((size_t)l * p.B + b) * p.nkv + g) * p.max_chunks + t.c;
     float* part = p.apart + pidx * (16 + 8 * (size_t)p.d);
     if (nst > 0) {
-      if (!csync()) return;
       float* scr = reinterpret_cast<float*>(__cvta_shared_to_generic(last_slot));
-      // per warp: m[8], l[8], O[8][64]
+      // per warp: m[8], l[8], O[8][64] of this round's dims
       float* mine = scr + warp * (16 + 8 * 64);
-      if (tig == 0) { mine[head] = mrun; mine[8 + head] = lsum; }
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
+      for (int r = 0; r < 2; ++r) {
+        if (r >= halves) break;
+        if (!csync()) return;
+        if (tig == 0) { mine[head] = mrun; mine[8 + head] = lsum; }
 #pragma unroll
-        for (int e = 0; e < 2; ++e) mine[16 + head * 64 + nt * 8 + tig * 2 + e] = oacc[nt][e] + oacc[nt][e + 2];
-      if (!csync()) return;
-      for (int i = threadIdx.x; i < 8 * p.d; i += 256) {
-        const int h = i / p.d, dd = i % p.d, dpi = dd / 64, dl = dd % 64;
-        float M = -INFINITY;
-        for (int w = dpi * pps; w < (dpi + 1) * pps; ++w) M = fmaxf(M, scr[w * (16 + 512) + h]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY)
-          for (int w = dpi * pps; w < (dpi + 1) * pps; ++w) {
-            const float* src = scr + w * (16 + 512);
-            if (src[h] == -INFINITY) continue;
-            const float f = exp2f(src[h] - M);
-            L += src[8 + h] * f;
-            O += src[16 + h * 64 + dl] * f;
-          }
-        if (dd == 0) { __stcg(part + h, M); __stcg(part + 8 + h, L); }
-        __stcg(part + 16 + i, O);
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            mine[16 + head * 64 + nt * 8 + tig * 2 + e] = oacc[8 * r + nt][e] + oacc[8 * r + nt][e + 2];
+        if (!csync()) return;
+        for (int i = threadIdx.x; i < 8 * 64; i += 256) {
+          const int h = i / 64, dl = i % 64;
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, scr[w * (16 + 512) + h]);
+          float L = 0.f, O = 0.f;
+          if (M != -INFINITY)
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+              const float* src = scr + w * (16 + 512);
+              if (src[h] == -INFINITY) continue;
+              const float f = exp2f(src[h] - M);
+              L += src[8 + h] * f;
+              O += src[16 + h * 64 + dl] * f;
+            }
+          if (r == 0 && dl == 0) { __stcg(part + h, M); __stcg(part + 8 + h, L); }
+          __stcg(part + 16 + h * p.d + 64 * r + dl, O);
+        }
       }
       if (!csync()) return;
       release();
