@@ -118,8 +118,12 @@ def test_plan_splits_branches_over_disjoint_sms(w, n_sm):
         assert np.bincount(q, minlength=n_sm).max() <= 1
     if w.H < 2048:  # the small models have fewer tasks than SMs
         return
-    # every SM of a partition gets work of its branch in every layer
+    # every SM of a partition gets work of its branch in every layer, and no SM takes two
+    # attention chunks, two O-proj tasks or two down tasks of one layer (a second one would
+    # double that phase on its SM)
     for l in (0, w.L - 1):
         lay = tasks["layer"] == l
         assert set(owner[attn & lay].tolist()) == set(range(na))
         assert set(owner[moe & lay].tolist()) == set(range(na, n_sm))
+        for op in (OP_ATTN, OP_O, OP_DOWN):
+            assert np.bincount(owner[(tasks["op"] == op) & lay], minlength=n_sm).max() == 1, op
