@@ -402,12 +402,11 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   }
 
   const int tiles = 2 * I / gh.RS;  // gate/up tiles: RS consecutive rows of [gate; up]
-  // about two QKV tasks per attention SM and two expert gate/up tasks per expert SM, per layer
-  // (whole stages each)
+  // Per layer, gate/up tasks are sized to about two per expert SM and QKV tasks to about two
+  // per SM (whole stages each, rounded up so that no SM gets a third). When the SMs are
+  // partitioned, QKV runs on every SM but the router's, about one task each: it needs only the
+  // layer's input, and the expert SMs would otherwise wait idle for the routing.
   const int upg_ = (G + 2) * (d / 8);
-  // (rounded up, so no SM of a partition gets a third). When the SMs are partitioned, QKV
-  // runs on every SM, about one task each: it needs only the layer's input, and the expert
-  // SMs would otherwise wait idle for the routing.
   const int qkv_tasks = n_attn < n_sm ? n_sm - (E + gh.RS - 1) / gh.RS : 2 * n_attn;
   int qkv_per_task = std::max(1, (nkv * upg_ + qkv_tasks - 1) / qkv_tasks);
   qkv_per_task = std::max(gh.RG, (qkv_per_task + gh.RG - 1) / gh.RG * gh.RG);
