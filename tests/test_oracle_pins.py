@@ -156,6 +156,14 @@ def test_route_ties_go_to_lower_expert_id():
     # values equal in fp32 but not in fp64 still tie (the decision is taken in fp32)
     lg2 = np.array([1.0, 1.0 + 1e-12, 0.5])
     assert list(oracle.route(lg2, 1)[0]) == [0]
+    # +0 and -0 are equal logits: the lower id goes first whatever the sign bit
+    lg3 = np.array([-1.0, 0.0, -0.0, -2.0])
+    assert list(oracle.route(lg3, 2)[0]) == [1, 2]
+    lg4 = np.array([-1.0, -0.0, 0.0, -2.0])
+    assert list(oracle.route(lg4, 2)[0]) == [1, 2]
+    # -inf logits still yield k distinct, valid experts (lowest free ids first)
+    lg5 = np.array([-np.inf, 3.0, -np.inf, -np.inf])
+    assert list(oracle.route(lg5, 3)[0]) == [1, 0, 2]
 
 
 def test_expert_matches_library_swiglu():
