@@ -147,6 +147,25 @@ def oracle_sample(w, tokens, ctx, steps=1):
     return (time.perf_counter() - t0) / steps
 
 
+def ranks_max(x: float, device: str) -> float:
+    """The maximum of x over all ranks (a job takes as long as its slowest rank); x itself when
+    no process group is up or it has one rank."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tok_s(batch: int, steps: int, seconds: float, world: int) -> float:
+    """Decode tokens per second of the whole job: every rank decodes `batch` tokens per step
+    (independent replicas, weak scaling), timed by the slowest rank."""
+    return batch * steps * world / seconds
+
+
 def run_reference(args, w, rank):
     """Reference arm: the CPU oracle as it stands, on this workload, rank 0 only."""
     if rank != 0:
@@ -241,11 +260,8 @@ def main():
         ev1.record(stream)
         torch.cuda.synchronize()
     dc.sync()
-    ms = ev0.elapsed_time(ev1)
+    ms = ranks_max(ev0.elapsed_time(ev1), device)
     if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     positions_timed = np.asarray(ctx, np.int64)[None, :] + done + np.arange(args.steps)[:, None]
     done += args.steps
@@ -285,17 +301,14 @@ def main():
         h_tok.copy_(h_out)
     e2e_s = time.perf_counter() - t0
     dc.sync()
-    if world > 1:
-        t = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = ranks_max(e2e_s, device)
 
     hbm_gbs, peak_kind = measured_peaks()
     sol = [metrics.step_bytes(w, positions_timed[i], de)["total"] for i in range(args.steps)]
     bytes_per_step = float(np.mean(sol))
     ms_step = ms / args.steps
     achieved = bytes_per_step / (ms_step * 1e-3) / 1e9
-    tok_s = w.B * args.steps / (ms * 1e-3) * world
+    tok_s = whole_job_tok_s(w.B, args.steps, ms * 1e-3, world)
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -313,7 +326,7 @@ def main():
         "sol": {"bytes_per_step": bytes_per_step, "frac_of_nominal_8tbs": bytes_per_step / (ms_step * 1e-3) / 8.0e12,
                 "frac_of_measured": achieved / hbm_gbs,
                 "sol_tok_s_measured_bw": metrics.sol_tok_s(bytes_per_step, w.B, hbm_gbs * 1e9)},
-        "e2e": {"value": w.B * n_e2e / e2e_s * world, "unit": "tok/s", "h2d_bytes_per_step": 2 * 4 * w.B,
+        "e2e": {"value": whole_job_tok_s(w.B, n_e2e, e2e_s, world), "unit": "tok/s", "h2d_bytes_per_step": 2 * 4 * w.B,
                 "d2h_bytes_per_step": 4 * w.B},
         "clocks": clk.summary(),
     }
