@@ -19,7 +19,9 @@
  * rotate-half RoPE over the full head, contiguous GQA groups (q head h reads kv head
  * h / (n_q / n_kv)), router bias added before both top-k and softmax, untied LM head.
  *
- * Numerics: bf16 weights and KV; fp32 activations, accumulation and residual stream.
+ * Numerics: bf16 weights and KV; fp32 residual stream, norms, softmax and accumulation. Every
+ * matrix product on the tensor cores takes its activation operand as a bf16 pair (hi = bf16(x),
+ * lo = bf16(x - hi): at least 16 significant bits), so results stay close to fp32 products.
  *
  * Threading and streams: a context is used by one host thread at a time. Calls that take
  * a stream are asynchronous on it; host-detectable errors return at once, device-detected
@@ -53,7 +55,8 @@ typedef enum {
  * head_dim a multiple of 256 (and of 2048 when above 2048); expert_inter a multiple of 256,
  * at most 2048, with 4 * max_batch * expert_inter <= 32768 (one expert's hi/lo activations
  * for the batch fit a ring stage: any max_batch up to expert_inter 1024, max_batch <= 4 at
- * 2048); top_k <= 8; max_batch <= 8; page_size == 16. */
+ * 2048); top_k <= 8; n_experts <= 256 and a multiple of 8; vocab a multiple of 64;
+ * max_batch <= 8; page_size == 16. */
 typedef struct {
   int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim;
   int32_t n_experts, top_k, expert_inter, vocab;
