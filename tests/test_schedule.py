@@ -127,3 +127,26 @@ def test_plan_splits_branches_over_disjoint_sms(w, n_sm):
         assert set(owner[moe & lay].tolist()) == set(range(na, n_sm))
         for op in (OP_ATTN, OP_O, OP_DOWN):
             assert np.bincount(owner[(tasks["op"] == op) & lay], minlength=n_sm).max() == 1, op
+
+
+@pytest.mark.parametrize("ctx_len", [100, 1000, 4096, 8192, 16384, 30000])
+def test_attention_chunks_fit_the_attention_partition(ctx_len):
+    """At batch 1 with the branches partitioned, the attention chunks of a layer are whole ring
+    stages (4 pages at d = 128), no more than one per attention SM, and their pages tile the
+    context exactly; every page of every chunk but the last is a full chunk's worth."""
+    w = W.M30B_BS1.with_(ctx_lo=ctx_len, ctx_hi=ctx_len, L=2)
+    ctx = W.context_lengths(w)
+    info, tasks, begin, load = B.mk_plan_schedule(cfg_of(w, ctx_len // 16 + 64), 152, ctx)
+    if info.n_attn_sm == 152:  # the attention bytes dominate: no partition at this length
+        return
+    att = tasks[(tasks["op"] == OP_ATTN) & (tasks["layer"] == 0)]
+    owner = np.searchsorted(begin, np.nonzero((tasks["op"] == OP_ATTN) & (tasks["layer"] == 0))[0], side="right") - 1
+    assert len(att) <= info.n_attn_sm and len(set(owner.tolist())) == len(att)
+    npg = -(-ctx_len // 16)
+    for g in range(w.nkv):
+        ch = sorted(att[att["b"] == g]["c"].tolist())
+        assert ch == list(range(len(ch))) and len(ch) == info.max_chunks
+    # chunk size: a whole number of 4-page stages, and the chunks cover the pages exactly
+    cp = -(-npg // info.max_chunks)
+    cp = -(-cp // 4) * 4
+    assert (info.max_chunks - 1) * cp < npg <= info.max_chunks * cp
