@@ -48,6 +48,17 @@ def test_host_side_argument_errors():
     assert lib.mk_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(out)) == B.MK_ERR_INVALID_ARG
     bad = B.mk_model_cfg(2, 256, 4, 2, 64, 8, 2, 512, 1024, 32, 1, 8, 1e4, 1e-6)  # page size 32
     assert lib.mk_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(out)) == B.MK_ERR_UNSUPPORTED
+    # each shape limit the header states is rejected before any device work
+    for fields, why in (((2, 256, 4, 2, 64, 264, 2, 512, 1024, 16, 1, 8), "n_experts > 256"),
+                        ((2, 256, 4, 2, 64, 12, 2, 512, 1024, 16, 1, 8), "n_experts not a multiple of 8"),
+                        ((2, 256, 4, 2, 64, 8, 2, 512, 1000, 16, 1, 8), "vocab not a multiple of 64"),
+                        ((2, 256, 4, 2, 96, 8, 2, 512, 1024, 16, 1, 8), "head_dim 96"),
+                        ((2, 256, 18, 2, 64, 8, 2, 512, 1024, 16, 1, 8), "9 query heads per KV head"),
+                        ((2, 256, 4, 2, 64, 8, 2, 320, 1024, 16, 1, 8), "expert_inter not a multiple of 256"),
+                        ((2, 256, 4, 2, 64, 8, 2, 2048, 1024, 16, 8, 8), "activations of batch 8 at 2048 > a stage"),
+                        ((2, 256, 4, 2, 64, 8, 2, 512, 1024, 16, 9, 8), "max_batch 9")):
+        bad = B.mk_model_cfg(*fields, 1e4, 1e-6)
+        assert lib.mk_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(out)) == B.MK_ERR_UNSUPPORTED, why
     w2 = B.mk_weight_ptrs(*([0x1008] * 5 + [None] + [0x1000] * 4))  # misaligned
     assert lib.mk_create(ctypes.byref(cfg), ctypes.byref(w2), ctypes.byref(out)) == B.MK_ERR_INVALID_ARG
     assert lib.mk_build_schedule(None, 1, None, None) == B.MK_ERR_INVALID_ARG
