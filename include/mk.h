@@ -82,7 +82,9 @@ typedef struct {
   const void *w_gate_up, *w_down, *final_gain, *lm_head;
 } mk_weight_ptrs;
 
-/* Paged KV cache, caller-owned device memory, bf16:
+/* Paged KV cache (aimodeling.com "cohere-megakernel-north-mini-code-h100", section "From demo
+ * to a full serving system": paged attention over ragged sequence lengths), caller-owned device
+ * memory, bf16:
  *   k, v  [n_layers][num_pages][n_kv_heads][page_size][head_dim]
  * Page ids come from the block table given to mk_build_schedule. 16-byte aligned. */
 typedef struct {
@@ -92,13 +94,22 @@ typedef struct {
 
 typedef struct mk_ctx mk_ctx;
 
-/* Validates cfg, queries the current device (SM count, shared memory), allocates the
- * device workspace (activations, counters, RoPE cos/sin table built on the host in fp64)
- * and returns a context in *out. Weights stay caller-owned and must outlive the context.
+/* Defined by: aimodeling.com "cohere-megakernel-north-mini-code-h100", section "One persistent
+ * kernel for the whole decode step" (one kernel resident on every SM for the whole step, over
+ * the model's bf16 weights), and "Decode is a bandwidth game" (the weights are streamed once per
+ * step, never copied).
+ * Validates cfg and the weight pointers (the same check mk_decode_step_noalloc makes), queries
+ * the current device (SM count, shared memory), allocates the device workspace (activations,
+ * counters, RoPE cos/sin table built on the host in fp64) and returns a context in *out. Weights stay caller-owned and must outlive the context.
  * Errors: MK_ERR_INVALID_ARG, MK_ERR_UNSUPPORTED, MK_ERR_OOM, MK_ERR_CUDA. */
 mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* weights, mk_ctx** out);
 
-/* Host-side scheduler: builds the per-SM task lists and dependency-counter targets for a
+/* Defined by: aibriefing.imbch.dev article 8171681, section "Scheduling and Performance
+ * Benchmarks" (a mostly static schedule built on the host, with dynamic work stealing), and
+ * aimodeling.com "cohere-megakernel-north-mini-code-h100", section "One persistent kernel for the
+ * whole decode step" (a task list in global memory, idle SMs backfilled deterministically); the
+ * block tables are the paged KV cache of section "From demo to a full serving system".
+ * Host-side scheduler: builds the per-SM task lists and dependency-counter targets for a
  * batch of `batch` sequences whose current lengths are seq_lens[b] (host array) and
  * uploads them (synchronously). block_tables is a device int32 array [batch][max_pages_per_seq]
  * that must stay valid while this schedule is used. Attention work is split in chunks
@@ -108,7 +119,12 @@ mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* weights, mk_c
  * the table), MK_ERR_OOM, MK_ERR_CUDA. */
 mk_status mk_build_schedule(mk_ctx* ctx, int32_t batch, const int32_t* seq_lens, const int32_t* block_tables);
 
-/* One decode step on `stream` (a cudaStream_t, NULL = legacy default stream), a single
+/* Defined by: aimodeling.com "cohere-megakernel-north-mini-code-h100", section "One persistent
+ * kernel for the whole decode step" (embedding to LM head in one launch: parallel attention and
+ * MoE branches over one normalized input, fused residual + RMSNorm, O-proj released per KV
+ * group); RoPE and SiLU-multiply fused per aibriefing.imbch.dev article 8171681, section "Key
+ * Technologies and Architecture"; the paged cache of "From demo to a full serving system".
+ * One decode step on `stream` (a cudaStream_t, NULL = legacy default stream), a single
  * kernel launch in MK_MODE_MEGAKERNEL. token_ids and positions are device int32 [batch];
  * positions[b] is the new token's position (= its sequence's current length). Writes the
  * bf16 K/V of the new token into kv at (block_tables[b][p / 16], p % 16), fp32 logits to
@@ -118,7 +134,9 @@ mk_status mk_build_schedule(mk_ctx* ctx, int32_t batch, const int32_t* seq_lens,
 mk_status mk_decode_step(mk_ctx* ctx, const int32_t* token_ids, const int32_t* positions, const mk_kv_pages* kv,
                          float* logits_out, int32_t* argmax_out, void* stream);
 
-/* n_steps greedy steps with the token fed back on the device: step i decodes at
+/* Greedy decoding as the pages benchmark it (aibriefing.imbch.dev article 8171681, section
+ * "Scheduling and Performance Benchmarks": 1K output tokens per sequence, token fed back).
+ * n_steps greedy steps with the token fed back on the device: step i decodes at
  * positions[b] + i the token chosen by step i - 1 (token_ids for i = 0) and writes it to
  * tokens_out [n_steps][batch] (device). logits_out [batch][vocab] (device, may be NULL)
  * receives the last step's logits. One kernel launch per step, no host synchronization. */
@@ -134,20 +152,24 @@ mk_status mk_status_sync(mk_ctx* ctx);
 const char* mk_last_error(const mk_ctx* ctx);
 
 /* Execution mode: MK_MODE_MEGAKERNEL (default, one persistent kernel per step) or
- * MK_MODE_PER_OP (ablation: the same opcodes, one launch per layer and opcode kind). */
+ * MK_MODE_PER_OP (ablation of aimodeling.com "cohere-megakernel-north-mini-code-h100", section
+ * "Decode is a bandwidth game": kernel boundaries between ops. The same opcodes and task lists,
+ * one launch of the persistent kernel per layer and opcode kind, so every boundary becomes a
+ * full drain of the GPU; it is not a pipeline of separately written small kernels). */
 #define MK_MODE_MEGAKERNEL 0
 #define MK_MODE_PER_OP 1
 mk_status mk_set_mode(mk_ctx* ctx, int mode);
 
-/* Time limit of every device-side wait of a step (a dependency counter, a ring slot, the
- * blocks' own barrier), in nanoseconds; default 2e9 (2 s), accepted range [1e3, 6e10]. A
+/* Failure detection (no counterpart on the pages): time limit of every device-side wait of a
+ * step (a dependency counter, a ring slot, the blocks' own barrier), in nanoseconds; default
+ * 2e9 (2 s), accepted range [1e3, 6e10]. A
  * wait that runs out latches MK_ERR_DEVICE_TIMEOUT and every block of the step leaves
  * early, its copies in flight drained (the error is returned by mk_status_sync, which
  * also resets the counters so the context stays usable). Errors: MK_ERR_INVALID_ARG. */
 mk_status mk_set_wait_limit(mk_ctx* ctx, int64_t ns);
 
-/* Per-task trace: when dev_buf is non-NULL, each step records one 32-byte entry per task
- * (mk_trace_entry) into dev_buf (device memory, caller-owned, `bytes` long; entries past
+/* Tracing (no counterpart on the pages): when dev_buf is non-NULL, each step records one
+ * 32-byte entry per task (mk_trace_entry) into dev_buf (device memory, caller-owned, `bytes` long; entries past
  * the end are dropped). The first 16 bytes of dev_buf hold the entry count (uint64) and
  * are reset at every step. NULL disables tracing. */
 typedef struct {
@@ -159,8 +181,9 @@ typedef struct {
 } mk_trace_entry;
 mk_status mk_enable_trace(mk_ctx* ctx, void* dev_buf, size_t bytes);
 
-/* Device pointers to the library-owned per-layer activations of the last step, for
- * inspection (fp32 unless noted; valid until mk_destroy or the next mk_build_schedule):
+/* Inspection (no counterpart on the pages): device pointers to the library-owned per-layer
+ * activations of the last step (fp32 unless noted; valid until mk_destroy or the next
+ * mk_build_schedule):
  *   x [n_layers+1][batch][hidden]  residual stream entering layer l (x[n_layers] final)
  *   q [n_layers][batch][n_q][head_dim] before RoPE (attention applies it when it loads q)
  *   attn [n_layers][batch][n_q][head_dim] attention output per head
@@ -174,7 +197,7 @@ typedef struct {
 } mk_activations;
 mk_status mk_get_activations(const mk_ctx* ctx, mk_activations* out);
 
-/* Host-only view of the scheduler (no device needed): plans the step for `batch`
+/* Host-only view of the scheduler of mk_build_schedule (same passages; no device needed): plans the step for `batch`
  * sequences of lengths seq_lens (host) on n_sm SMs, as mk_build_schedule would. Writes
  * the plan's sizes to *info; if `tasks` is non-NULL, copies the megakernel's task list
  * (info->n_tasks 16-byte descriptors {uint8 op, uint8 flags, uint16 layer, int32 a, b, c},
@@ -208,12 +231,16 @@ mk_status mk_get_launch_info(const mk_ctx* ctx, int32_t* n_sm, int32_t* tasks_pe
  * and mk_decode_step (positions[b] must equal seq_lens[b], the lengths the step is planned
  * for). The call plans the step on the host, copies the plan into the array, launches on
  * `stream` and waits for that stream, so device errors (bad page, bad token, timeout) are
- * returned directly. The first call on a device, with that device current, looks up the
- * array's device address and configures the kernel; make that first call before any stream
- * capture. Every call shares the array and overwrites it (counters and status are cleared
+ * returned directly; the call is synchronous with respect to `stream`. Every device-side
+ * wait of this entry point has a fixed limit of 2 s (mk_set_wait_limit, which acts on a
+ * context, does not apply here). The first call on a device, with that device current,
+ * looks up the array's device address and configures the kernel; make that first call
+ * before any stream capture. Every call shares the array and overwrites it (counters and status are cleared
  * at each call), so calls that overlap on the GPU, from any thread or stream, race and must
- * be serialised by the caller. Workloads whose workspace exceeds the array (for example the
- * 30B-shaped model) are rejected with MK_ERR_UNSUPPORTED; msg (may be NULL) receives a
+ * be serialised by the caller. The config and weight pointers get the same checks as in mk_create
+ * (MK_ERR_INVALID_ARG or MK_ERR_UNSUPPORTED before any device work), the KV pools must be
+ * non-null and 16-byte aligned, and workloads whose workspace exceeds the array (for example
+ * the 30B-shaped model) are rejected with MK_ERR_UNSUPPORTED; msg (may be NULL) receives a
  * NUL-terminated explanation of at most msg_len bytes. */
 #define MK_NOALLOC_SCRATCH_BYTES (32u << 20)
 mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_weight_ptrs* weights, int32_t batch,

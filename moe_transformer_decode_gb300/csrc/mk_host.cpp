@@ -125,22 +125,31 @@ extern "C" void mk_destroy(mk_ctx* c) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, mk_ctx** out) {
-  if (!cfg || !w || !out) return MK_ERR_INVALID_ARG;
-  *out = nullptr;
+// The one check of a model config and its weight pointers, shared by every entry point that
+// takes them (mk_create, mk_decode_step_noalloc), so their limits cannot drift apart. It runs
+// before any size or offset is computed from the config. *why (may be NULL) gets a static
+// description of the first failed check.
+mk_status mk::validate_model(const mk_model_cfg* cfg, const mk_weight_ptrs* w, const char** why) {
+  auto no = [&](mk_status s, const char* text) {
+    if (why) *why = text;
+    return s;
+  };
+  if (!cfg || !w) return no(MK_ERR_INVALID_ARG, "null config or weight pointers");
   const mk_model_cfg& m = *cfg;
   if (m.n_layers <= 0 || m.hidden <= 0 || m.n_q_heads <= 0 || m.n_kv_heads <= 0 || m.head_dim <= 0 ||
       m.n_experts <= 0 || m.top_k <= 0 || m.top_k > m.n_experts || m.expert_inter <= 0 || m.vocab <= 0 ||
-      m.max_batch <= 0 || m.max_pages_per_seq <= 0 || m.n_q_heads % m.n_kv_heads != 0 || !(m.rms_eps >= 0.f) ||
-      !(m.rope_theta > 0.f) || m.n_layers > 65535)
-    return MK_ERR_INVALID_ARG;
+      m.max_batch <= 0 || m.max_pages_per_seq <= 0 || m.n_q_heads % m.n_kv_heads != 0 || m.n_layers > 65535)
+    return no(MK_ERR_INVALID_ARG, "inconsistent model config (a size <= 0, top_k > n_experts, or n_kv_heads not "
+                                  "dividing n_q_heads)");
+  if (!(m.rms_eps >= 0.f) || !(m.rope_theta > 0.f) || !std::isfinite(m.rms_eps) || !std::isfinite(m.rope_theta))
+    return no(MK_ERR_INVALID_ARG, "rms_eps must be finite and >= 0, rope_theta finite and > 0");
   if (!w->embed || !w->norm_gain || !w->w_qkv || !w->w_o || !w->w_router || !w->w_gate_up || !w->w_down ||
       !w->final_gain || !w->lm_head)
-    return MK_ERR_INVALID_ARG;
+    return no(MK_ERR_INVALID_ARG, "null weight pointer");
   const void* ptrs[] = {w->embed, w->norm_gain, w->w_qkv, w->w_o, w->w_router, w->w_gate_up, w->w_down,
-                        w->final_gain, w->lm_head};
+                        w->final_gain, w->lm_head, w->router_bias};
   for (const void* p : ptrs)
-    if (!aligned16(p)) return MK_ERR_INVALID_ARG;
+    if (!aligned16(p)) return no(MK_ERR_INVALID_ARG, "weight pointer not 16-byte aligned");
   const int od = m.n_q_heads * m.head_dim;
   const bool shape_ok = (m.hidden == 256 || m.hidden == 512 || m.hidden == 1024 || m.hidden == 2048) &&
                         (m.head_dim == 64 || m.head_dim == 128) && m.n_q_heads / m.n_kv_heads <= 8 &&
@@ -150,7 +159,17 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
                         m.vocab % 64 == 0 &&
                         // an expert's activations for the whole batch fit one ring stage
                         2 * m.max_batch * 2 * m.expert_inter <= kStagePayload;
-  if (!shape_ok) return MK_ERR_UNSUPPORTED;
+  if (!shape_ok) return no(MK_ERR_UNSUPPORTED, "model shape not supported by this build");
+  return MK_OK;
+}
+
+extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w, mk_ctx** out) {
+  if (!cfg || !w || !out) return MK_ERR_INVALID_ARG;
+  *out = nullptr;
+  const mk_status vs = validate_model(cfg, w, nullptr);
+  if (vs != MK_OK) return vs;
+  const mk_model_cfg& m = *cfg;
+  const int od = m.n_q_heads * m.head_dim;
 
   mk_ctx* c = new mk_ctx();  // value-initialized: every pointer starts null
   c->cfg = m;

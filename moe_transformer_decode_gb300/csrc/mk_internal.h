@@ -137,6 +137,9 @@ struct Plan {
   int n_attn_sm = 0;               // SMs [0, n_attn_sm) take the attention branch, the rest the experts
 };
 mk_status plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_t* seq_lens, Plan& P);
+// Checks a model config and its weight pointers (sizes, supported shapes, 16-byte alignment)
+// for every entry point that takes them; *why (may be NULL) receives a static reason.
+mk_status validate_model(const mk_model_cfg* cfg, const mk_weight_ptrs* w, const char** why);
 
 struct TensorMaps {
   // KV pools as 3D {64, rows, head_dim / 64} bf16 views (a row is 2 head_dim bytes, a 64-wide

@@ -99,6 +99,12 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Cross-proxy ordering. Bulk and tensor copies run in the async proxy; plain loads and stores
+// in the generic proxy. Global data written by generic stores (on any SM) and read here by a
+// bulk copy needs this fence after the acquire that made the writes visible, and a shared-memory
+// region written by generic stores and then overwritten by a copy needs the shared-memory form.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -570,6 +576,11 @@ struct Producer {
               int fine = 1;
               if (lane == 0) fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.gu(l));
               if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
+              // p.h was written by the gate/up epilogues' generic stores (other SMs) and published by
+              // their release; lane 0's acquire made it visible to the warp, and this fence orders it
+              // before the bulk copies below, which read it through the async proxy
+              __syncwarp();
+              fence_proxy_async_global();
               gu_done = true;
             }
             if (!begin((uint32_t)2 * p.B * p.I * 2)) return false;
@@ -1586,6 +1597,23 @@ struct Consumer {
       if (s % npar == sp && page < ar.cp1) {
         const uint32_t kt = smem_addr(st) + (uint32_t)pi * 4096 * halves;
         const uint32_t vt = kt + (uint32_t)halves * 2048;
+        // Rows of the sequence's last page at or past the new token's position are masked out of
+        // the scores, but their V bytes still enter P V (with weight 0), and 0 * NaN is NaN: the
+        // cache there holds whatever the caller left. This warp alone reads this page, so it
+        // zeroes those V rows (whole 128-byte rows: the swizzle only permutes within a row).
+        const int live = ar.pos_end - page * kPage;
+        if (live < kPage) {
+          const int nz = (kPage - max(live, 0)) * 8 * halves;  // 16-byte words to clear
+          for (int i = lane; i < nz; i += 32) {
+            const int h = i / ((kPage - max(live, 0)) * 8), rem = i % ((kPage - max(live, 0)) * 8);
+            const int row = max(live, 0) + rem / 8;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt + h * 2048 + row * 128 + (rem % 8) * 16),
+                         "r"(0u)
+                         : "memory");
+          }
+          fence_proxy_async_smem();  // generic stores into a ring slot the producer refills later
+          __syncwarp();
+        }
         float sc[2][4];
 #pragma unroll
         for (int i = 0; i < 2; ++i)
@@ -1693,6 +1721,9 @@ struct Consumer {
           __stcg(part + 16 + h * p.d + 64 * r + dl, O);
         }
       }
+      // the slot was scratch for generic stores; the producer's next copy into it is an
+      // async-proxy write, ordered after them by this fence (every writer thread) and the release
+      fence_proxy_async_smem();
       if (!csync()) return;
       release();
     } else {

@@ -71,32 +71,23 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_we
                                             const int32_t* token_ids, const int32_t* positions, const mk_kv_pages* kv,
                                             float* logits_out, int32_t* argmax_out, void* stream, char* msg,
                                             int32_t msg_len) {
-  if (!cfg || !w || !seq_lens || !block_tables || !token_ids || !positions || !kv || !kv->k || !kv->v ||
-      kv->num_pages <= 0) {
-    set_msg(msg, msg_len, "null argument or empty KV pool");
+  if (!cfg || !w || !seq_lens || !block_tables || !token_ids || !positions || !kv) {
+    set_msg(msg, msg_len, "null argument");
+    return MK_ERR_INVALID_ARG;
+  }
+  // the same checks as mk_create, before any size or offset is derived from the config
+  const char* why = "";
+  const mk_status vs = validate_model(cfg, w, &why);
+  if (vs != MK_OK) {
+    set_msg(msg, msg_len, why);
+    return vs;
+  }
+  if (!kv->k || !kv->v || kv->num_pages <= 0 || ((uintptr_t)kv->k & 15u) != 0 || ((uintptr_t)kv->v & 15u) != 0) {
+    set_msg(msg, msg_len, "KV pools null, empty or not 16-byte aligned");
     return MK_ERR_INVALID_ARG;
   }
   const mk_model_cfg& m = *cfg;
-  if (!w->embed || !w->norm_gain || !w->w_qkv || !w->w_o || !w->w_router || !w->w_gate_up || !w->w_down ||
-      !w->final_gain || !w->lm_head) {
-    set_msg(msg, msg_len, "null weight pointer");
-    return MK_ERR_INVALID_ARG;
-  }
   const int od = m.n_q_heads * m.head_dim;
-  if (m.n_layers <= 0 || m.n_layers > 65535 || m.n_kv_heads <= 0 || m.n_q_heads % m.n_kv_heads != 0 ||
-      m.top_k <= 0 || m.top_k > m.n_experts || m.vocab <= 0 || m.max_pages_per_seq <= 0 || m.max_batch <= 0) {
-    set_msg(msg, msg_len, "inconsistent model config");
-    return MK_ERR_INVALID_ARG;
-  }
-  const bool shape_ok = (m.hidden == 256 || m.hidden == 512 || m.hidden == 1024 || m.hidden == 2048) &&
-                        (m.head_dim == 64 || m.head_dim == 128) && m.n_q_heads / m.n_kv_heads <= 8 &&
-                        od % 256 == 0 && (od <= 2048 || od % 2048 == 0) && m.expert_inter % 256 == 0 &&
-                        m.expert_inter <= 2048 && m.top_k <= kMaxK && m.max_batch <= kMaxB && m.page_size == kPage &&
-                        m.n_experts <= kMaxExperts && m.n_experts % 8 == 0 && m.vocab % 64 == 0;
-  if (!shape_ok) {
-    set_msg(msg, msg_len, "model shape not supported by this build");
-    return MK_ERR_UNSUPPORTED;
-  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {

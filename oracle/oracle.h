@@ -11,8 +11,14 @@
  * system" (paged attention, ragged lengths); aibriefing.imbch.dev article 8171681,
  * "Key Technologies and Architecture" (fused RoPE and SiLU-multiply); BF16 weights and
  * KV on all three pages). The pages give no dims, norm epsilon, RoPE layout or router
- * rule; the readings taken where they are silent are listed in the design notes and
- * repeated at each function below.
+ * rule. Readings taken where they are silent: one RMSNorm per layer shared by both branches,
+ * gain after normalization, eps from the config; residual x + attn + moe with no scaling;
+ * rotate-half RoPE over the full head (pairs i, i + d/2; angle pos * theta^(-2i/d)) on q and
+ * k only; contiguous GQA groups; scale 1/sqrt(d), no soft-cap or window; router bias added
+ * before top-k and softmax, softmax over the k selected, ties to the lower id; routing
+ * weight applied to the expert's down output, summed in rank order; untied LM head, argmax
+ * ties to the lowest id; the new token's k and v rounded to bf16 before attention reads
+ * them. Each reading is repeated at the function that takes it.
  *
  * Arithmetic: weights and the KV cache are bf16 (as stored); every other value is
  * carried in fp64. Decisions that produce integers (router top-k, LM-head argmax) are

@@ -1,15 +1,15 @@
 """mk_decode_step_noalloc: the decode step for callers that cannot allocate device memory
 (an arena or pool owns all device memory, or allocation is forbidden after start-up). It keeps
-its workspace in the library's static device array; this checks it against mk_decode_step on
-the same model and KV cache, over two calls in a row with the greedy token fed back."""
+its workspace in the library's static device array; the GPU tests check it against
+mk_decode_step on the same model and KV cache, over two calls in a row with the greedy token
+fed back. The CPU tests show that it makes the same checks of its arguments as mk_create, and
+returns before any device work when one fails (fake pointers, never dereferenced)."""
 import ctypes
 
 import numpy as np
 import pytest
 
 from synth import workloads as W
-
-pytestmark = pytest.mark.gpu
 
 
 def _cfg(w, max_pages):
@@ -18,6 +18,7 @@ def _cfg(w, max_pages):
     return B.mk_model_cfg(w.L, w.H, w.nq, w.nkv, w.d, w.E, w.topk, w.I, w.V, 16, w.B, max_pages, w.rope_theta, w.eps)
 
 
+@pytest.mark.gpu
 @pytest.mark.parametrize("w", [W.TINY, W.SMALL], ids=["tiny", "small_bs8"])
 def test_noalloc_step_matches_decode_step(w):
     import torch
@@ -59,6 +60,7 @@ def test_noalloc_step_matches_decode_step(w):
     dc.close()
 
 
+@pytest.mark.gpu
 def test_noalloc_rejects_workspace_beyond_the_static_array():
     from moe_transformer_decode_gb300 import binding as B
 
@@ -73,3 +75,85 @@ def test_noalloc_rejects_workspace_beyond_the_static_array():
                                         ctypes.byref(kv), None, None, None, msg, len(msg))
     assert st == B.MK_ERR_UNSUPPORTED
     assert b"static scratch" in msg.value
+
+
+FAKE = 1 << 20  # a 16-byte-aligned address that is never dereferenced
+
+
+def _call(cfg, ptrs, kv, lens):
+    from moe_transformer_decode_gb300 import binding as B
+
+    msg = ctypes.create_string_buffer(256)
+    lens = np.asarray(lens, np.int32)
+    st = B.lib().mk_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(ptrs), len(lens), lens.ctypes.data, FAKE,
+                                        FAKE, FAKE, ctypes.byref(kv), None, None, None, msg, len(msg))
+    return st, msg.value.decode()
+
+
+def _good():
+    from moe_transformer_decode_gb300 import binding as B
+
+    cfg = B.mk_model_cfg(2, 256, 4, 2, 64, 8, 2, 512, 1024, 16, 1, 8, 1e4, 1e-6)
+    ptrs = B.mk_weight_ptrs(*([FAKE] * 5 + [None] + [FAKE] * 4))
+    kv = B.mk_kv_pages(FAKE, FAKE, 8)
+    return cfg, ptrs, kv
+
+
+def test_noalloc_rejects_what_mk_create_rejects_before_device_work():
+    """Every bad config, pointer or KV pool is refused on the host, before the call looks for a
+    device: these run (and must pass) on a machine without a GPU."""
+    from moe_transformer_decode_gb300 import binding as B
+
+    lib = B.lib()
+    out = ctypes.c_void_p()
+    cases = []
+    # (fields of mk_model_cfg without theta/eps, theta, eps, expected status, why)
+    base = [2, 256, 4, 2, 64, 8, 2, 512, 1024, 16, 1, 8]
+
+    def with_(**kw):
+        f = list(base)
+        names = ["n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "n_experts", "top_k", "expert_inter",
+                 "vocab", "page_size", "max_batch", "max_pages_per_seq"]
+        for k, v in kw.items():
+            f[names.index(k)] = v
+        return f
+
+    # the ring-stage bound: one expert's hi/lo activations for the batch exceed a 32 KB stage
+    cases.append((with_(max_batch=8, expert_inter=2048), 1e4, 1e-6, B.MK_ERR_UNSUPPORTED, "batch 8 at inter 2048"))
+    cases.append((with_(max_batch=8, expert_inter=1280), 1e4, 1e-6, B.MK_ERR_UNSUPPORTED, "batch 8 at inter 1280"))
+    # sizes <= 0 (a negative expert_inter must not reach any offset arithmetic)
+    cases.append((with_(expert_inter=-256), 1e4, 1e-6, B.MK_ERR_INVALID_ARG, "negative expert_inter"))
+    cases.append((with_(n_q_heads=0), 1e4, 1e-6, B.MK_ERR_INVALID_ARG, "no query heads"))
+    cases.append((with_(n_kv_heads=0), 1e4, 1e-6, B.MK_ERR_INVALID_ARG, "no kv heads"))
+    cases.append((with_(n_layers=-1), 1e4, 1e-6, B.MK_ERR_INVALID_ARG, "negative layers"))
+    cases.append((with_(top_k=9), 1e4, 1e-6, B.MK_ERR_INVALID_ARG, "top_k > experts"))
+    cases.append((base, 1e4, -1e-6, B.MK_ERR_INVALID_ARG, "negative rms_eps"))
+    cases.append((base, 0.0, 1e-6, B.MK_ERR_INVALID_ARG, "rope_theta 0"))
+    cases.append((base, -1e4, 1e-6, B.MK_ERR_INVALID_ARG, "negative rope_theta"))
+    cases.append((base, float("nan"), 1e-6, B.MK_ERR_INVALID_ARG, "NaN rope_theta"))
+    cases.append((with_(hidden=300), 1e4, 1e-6, B.MK_ERR_UNSUPPORTED, "hidden 300"))
+    cases.append((with_(page_size=32), 1e4, 1e-6, B.MK_ERR_UNSUPPORTED, "page size 32"))
+    _, ptrs, kv = _good()
+    for fields, theta, eps, want, why in cases:
+        cfg = B.mk_model_cfg(*fields, theta, eps)
+        st, msg = _call(cfg, ptrs, kv, [32])
+        assert st == want, f"{why}: got {st} ({msg})"
+        assert msg, why
+        # mk_create makes the same decision (shared validator)
+        assert lib.mk_create(ctypes.byref(cfg), ctypes.byref(ptrs), ctypes.byref(out)) == want, why
+
+    cfg, ptrs, kv = _good()
+    for i, name in enumerate(["embed", "norm_gain", "w_qkv", "w_o", "w_router", "w_gate_up", "w_down", "final_gain",
+                              "lm_head"]):
+        bad = B.mk_weight_ptrs(*([FAKE] * 5 + [None] + [FAKE] * 4))
+        setattr(bad, name, FAKE + 8)  # misaligned
+        st, msg = _call(cfg, bad, kv, [32])
+        assert st == B.MK_ERR_INVALID_ARG and "aligned" in msg, name
+        setattr(bad, name, None)  # missing
+        st, msg = _call(cfg, bad, kv, [32])
+        assert st == B.MK_ERR_INVALID_ARG, name
+    bad = B.mk_weight_ptrs(*([FAKE] * 5 + [FAKE + 4] + [FAKE] * 4))  # misaligned router bias
+    assert _call(cfg, bad, kv, [32])[0] == B.MK_ERR_INVALID_ARG
+    for k, v, n in ((FAKE + 8, FAKE, 8), (FAKE, FAKE + 2, 8), (None, FAKE, 8), (FAKE, FAKE, 0)):
+        st, msg = _call(cfg, ptrs, B.mk_kv_pages(k, v, n), [32])
+        assert st == B.MK_ERR_INVALID_ARG and "KV" in msg
