@@ -133,18 +133,45 @@ def distinct_experts(dc, w):
     return np.array([len(np.unique(ids[l])) for l in range(w.L)])
 
 
-def oracle_sample(w, tokens, ctx, steps=1):
-    """CPU oracle on the host cores: one warm-up step (generates and caches the weights it
-    touches), then `steps` timed steps at the same position. Returns seconds per step."""
+ORACLE_BUDGET_S = 30.0  # CPU work the oracle timing may take, per arm
+
+
+def oracle_protocol(w, max_steps: int, budget_s: float = ORACLE_BUDGET_S):
+    """The one timing protocol of the CPU oracle (both the main line's cpu_baseline and the
+    reference arm): one warm-up step (it synthesises and caches the weights it touches), one
+    step to size the sample, then as many steps as fit the budget (at most max_steps, at least
+    one), all at the workload's first position. Returns (seconds per step, steps timed, threads,
+    sample description)."""
     import oracle
     from synth import workloads as W
 
+    ctx = np.asarray(W.context_lengths(w), np.int32)
+    tokens = W.first_tokens(w)
     src = oracle.SynthSource(w, ctx, 4, W.router_bias(w), keep_all_experts=True)
     oracle.decode_step(w, src, tokens, ctx)
     t0 = time.perf_counter()
-    for _ in range(steps):
+    oracle.decode_step(w, src, tokens, ctx)
+    first = time.perf_counter() - t0
+    timed = max(1, min(max_steps, int(budget_s / max(first, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(timed):
         oracle.decode_step(w, src, tokens, ctx)
-    return (time.perf_counter() - t0) / steps
+    per_step = (time.perf_counter() - t0) / timed
+    sample = (f"{timed} oracle decode step(s) of {w.name} (batch {w.B}, all {w.L} layers and the LM head) at the "
+              f"workload's first position, after one warm-up step that synthesises and caches the weights it "
+              f"touches and one sizing step; KV values synthesised on read; at most {budget_s:.0f} s of CPU work")
+    return per_step, timed, oracle.threads(), sample
+
+
+def bench_config(w, mode: str, world: int) -> dict:
+    """The `config` object of both arms' lines (identical keys and values for one workload)."""
+    from synth import workloads as W
+
+    ctx = W.context_lengths(w)
+    return {"workload": w.name, "batch": w.B, "ctx_start": int(np.max(ctx)), "ctx_min": int(np.min(ctx)),
+            "layers": w.L, "experts": f"{w.E} top-{w.topk}", "routing": w.routing, "mode": mode,
+            "parallelism": "replicas" if world > 1 else "single_gpu",
+            "l2": "inputs larger than L2: each step streams its weights and KV once (GBs vs 129 MB of L2)"}
 
 
 def ranks_max(x: float, device: str) -> float:
@@ -170,69 +197,36 @@ def run_reference(args, w, rank):
     """Reference arm: the CPU oracle as it stands, on this workload, rank 0 only."""
     if rank != 0:
         return
-    from synth import workloads as W
-
-    ctx = W.context_lengths(w)
-    tokens = W.first_tokens(w)
     t0 = time.perf_counter()
-    per_step = oracle_sample(w, tokens, ctx, 1)
-    budget = 150.0
-    timed = max(1, min(args.steps, int(budget / max(per_step, 1e-3))))
-    if timed > 1:
-        per_step = oracle_sample(w, tokens, ctx, timed)
+    per_step, timed, cores, sample = oracle_protocol(w, args.steps)
     value = w.B / per_step
-    import oracle
-    cores = oracle.threads()
-    sample = (f"{timed} oracle decode step(s) of {w.name} (batch {w.B}) at the prefill position after one warm-up "
-              f"step that synthesises and caches the weights it touches; KV values synthesised on read")
     line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "tok/s", "n_gpus": args.gpus,
             "steps": args.steps, "steps_timed": timed, "warmup": args.warmup, "ms_per_step": 1e3 * per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded SplitMix64/Irwin-Hall bf16 weights and KV)",
-            "config": {"workload": w.name, "batch": w.B, "ctx": int(ctx.max()), "layers": w.L},
+            "config": bench_config(w, args.mode, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t0}
     print(json.dumps(line), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=8)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=64)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="megakernel", choices=["megakernel", "per_op"])
-    args = ap.parse_args()
+def measure(w, args, device, world):
+    """Timed greedy decode (device-side token feedback) and the end-to-end loop through the C ABI
+    for workload w; returns the per-workload record (the headline line's fields, or one entry of
+    by_config)."""
+    import torch
 
+    from moe_transformer_decode_gb300 import binding as B
+    from moe_transformer_decode_gb300 import metrics
     from synth import workloads as W
 
-    w = W.ALL[args.workload]
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
-        run_reference(args, w, rank)
-        return
-
-    import torch
     import torch.distributed as dist
 
-    torch.cuda.set_device(local)
-    device = f"cuda:{local}"
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device(device))
-    assert args.warmup >= 3, "at least 3 warm-up steps"
     capacity = args.warmup + args.steps + args.e2e_steps + 16
     if capacity > w.steps:
         w = w.with_(steps=capacity)
     dc, model, K, V, ctx, bt_d = setup_gpu(w, capacity, device)
-    from moe_transformer_decode_gb300 import binding as B
-    from moe_transformer_decode_gb300 import metrics
-
     if args.mode == "per_op":
         dc.set_mode(B.MK_MODE_PER_OP)
     launches_per_step = dc.launch_info()[2]
@@ -253,7 +247,7 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(int(str(device).split(":")[-1])) as clk:
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
         dc.greedy(args.steps, last_tok, pos_t, K, V, logits, toks, stream.cuda_stream)
@@ -302,44 +296,88 @@ def main():
     e2e_s = time.perf_counter() - t0
     dc.sync()
     e2e_s = ranks_max(e2e_s, device)
+    dc.close()
+    del dc, model, K, V
+    torch.cuda.empty_cache()
 
     hbm_gbs, peak_kind = measured_peaks()
-    sol = [metrics.step_bytes(w, positions_timed[i], de)["total"] for i in range(args.steps)]
-    bytes_per_step = float(np.mean(sol))
+    sol = [metrics.step_bytes(w, positions_timed[i], de) for i in range(args.steps)]
+    bytes_per_step = float(np.mean([x["total"] for x in sol]))
+    kv_share = float(np.mean([(x["kv_read"] + x["kv_write"]) / x["total"] for x in sol]))
     ms_step = ms / args.steps
     achieved = bytes_per_step / (ms_step * 1e-3) / 1e9
-    tok_s = whole_job_tok_s(w.B, args.steps, ms * 1e-3, world)
-    line = {
-        "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded SplitMix64/Irwin-Hall bf16 weights and KV, generated on the device)",
-        "config": {"workload": w.name, "batch": w.B, "ctx_start": int(np.max(ctx)), "layers": w.L,
-                   "experts": f"{w.E} top-{w.topk}", "routing": w.routing, "mode": args.mode,
-                   "parallelism": "replicas" if world > 1 else "single_gpu",
-                   "l2": "inputs larger than L2: each step streams its weights and KV once (GBs vs 129 MB of L2)"},
-        "gpu_launches": launches_per_step * args.steps,
+    return {
+        "workload": w.name, "value": whole_job_tok_s(w.B, args.steps, ms * 1e-3, world), "unit": "tok/s",
+        "ms_per_step": ms_step, "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                      "frac": achieved / hbm_gbs, "traffic": measured_traffic(w.name), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": bytes_per_step / launches_per_step,
                      "distinct_experts_per_layer": float(np.mean(de))},
         "sol": {"bytes_per_step": bytes_per_step, "frac_of_nominal_8tbs": bytes_per_step / (ms_step * 1e-3) / 8.0e12,
-                "frac_of_measured": achieved / hbm_gbs,
+                "frac_of_measured": achieved / hbm_gbs, "kv_share_of_bytes": kv_share,
                 "sol_tok_s_measured_bw": metrics.sol_tok_s(bytes_per_step, w.B, hbm_gbs * 1e9)},
         "e2e": {"value": whole_job_tok_s(w.B, n_e2e, e2e_s, world), "unit": "tok/s", "h2d_bytes_per_step": 2 * 4 * w.B,
                 "d2h_bytes_per_step": 4 * w.B},
         "clocks": clk.summary(),
+        "config": bench_config(w, args.mode, world),
     }
+
+
+# the metric's other half (batch 8 at 1K-8K contexts, both routing modes) and the long context,
+# measured in the same process after the headline workload
+EXTRA_WORKLOADS = ("moe30b_a3b_bs8_ctx1k8k", "moe30b_a3b_bs8_ctx1k8k_zipf", "moe30b_a3b_bs1_ctx256k")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only (no by_config lines)")
+    ap.add_argument("--mode", default="megakernel", choices=["megakernel", "per_op"])
+    args = ap.parse_args()
+
+    from synth import workloads as W
+
+    w = W.ALL[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(device))
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    head = measure(w, args, device, world)
+    line = {"metric": METRIC, "value": head["value"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded SplitMix64/Irwin-Hall bf16 weights and KV, generated on the device)",
+            "config": head["config"], "gpu_launches": head["gpu_launches"], "roofline": head["roofline"],
+            "sol": head["sol"], "e2e": head["e2e"], "clocks": head["clocks"]}
+    if not args.no_extra and args.workload == DEFAULT_WORKLOAD:
+        line["by_config"] = {}
+        for name in EXTRA_WORKLOADS:
+            r = measure(W.ALL[name], args, device, world)
+            line["by_config"][name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "gpu_launches", "roofline",
+                                                         "sol", "e2e", "clocks", "config")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tokens = W.first_tokens(w)
-        sec = oracle_sample(w, tokens, np.asarray(ctx, np.int32), 1)
-        import oracle
-        line["cpu_baseline"] = {"value": w.B / sec, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
-                                "sample": f"1 oracle decode step of {w.name} after one warm-up step that "
-                                          f"synthesises and caches the weights it touches"}
+        per_step, timed, cores, sample = oracle_protocol(w, args.steps)
+        line["cpu_baseline"] = {"value": w.B / per_step, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    dc.close()
     if world > 1:
         dist.destroy_process_group()
 

@@ -325,6 +325,7 @@ struct Misc {
   };
   float norm[kConsumerWarps][kMaxB]; // sum of squares partials
   int flag;
+  int wait_failed;  // set by the polling warp of a block-wide wait that gave up
   // routing scratch of the warp that computes a layer's routing
   uint32_t em[kMaxExperts];  // bit b: token b picked the expert
   int ids[kMaxB][kMaxK];
@@ -726,16 +727,26 @@ struct Consumer {
     return done;
   }
 
+  // Block-wide wait on counter idx. One warp polls and the others wait at the block barrier,
+  // which orders their later reads after the poller's acquire: every consumer warp of every SM
+  // polling the same line would make that L2 slice a hot spot.
+  __device__ bool block_wait(int idx) {
+    if (warp == 0) {
+      const bool done = warp_wait(p, idx);
+      if (lane == 0) m.wait_failed = done ? 0 : 1;
+    }
+    if (!csync()) return false;
+    if (m.wait_failed) ok = false;  // every warp learns that the poller gave up
+    return ok;
+  }
+
   // The normalized input of layer l (l == L: the final norm before the LM head), for this
   // lane's 8 columns: x = residual stream (embedding at l = 0), n = x / rms(x) * gain.
   __device__ void load_norm(int l, bool write_x) {
     const Geo g = geo_of(p.H);
     const int ks = warp % g.KW;
     const int col = ks * 256 + lane * 8;
-    if (l > 0 && !warp_wait(p, cm.layer(l - 1))) {
-      ok = false;
-      return;
-    }
+    if (l > 0 && !block_wait(cm.layer(l - 1))) return;
     float x[NB][8];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -1034,7 +1045,7 @@ struct Consumer {
   // Routing of layer l in shared memory, loaded once per layer and block.
   __device__ bool load_route(int l) {
     if (route_layer == l) return true;
-    if (!warp_wait(p, cm.route(l))) { ok = false; return false; }
+    if (!block_wait(cm.route(l))) return false;
     const Route* rt = p.route + l;
     // the count and the whole tables in one round of loads (rows past the count are unused)
     if (threadIdx.x == 0) m.rc_n = __ldcg(&rt->n_active);
@@ -1050,7 +1061,7 @@ struct Consumer {
   }
   __device__ bool wait_gu(int l) {
     if (gu_layer == l) return true;
-    if (!warp_wait(p, cm.gu(l))) { ok = false; return false; }
+    if (!block_wait(cm.gu(l))) return false;
     gu_layer = l;
     return true;
   }
@@ -1523,7 +1534,7 @@ struct Consumer {
   // way for P V. K/V tiles arrive 128B-swizzled from the tensor maps (conflict-free ldmatrix).
   __device__ void op_attn(const Task& t) {
     const int l = t.layer, b = t.a, g = t.b;
-    if (!warp_wait(p, cm.qkv(l, g))) { ok = false; return; }
+    if (!block_wait(cm.qkv(l, g))) return;
     t_ready = gtimer();
     const AttnRange ar = attn_range(m.st_pos[b], m.st_cpp[b], m.st_nch[b], t.c);
     // warp (pi, sp) takes page pi of every stage s with s % npar == sp, over the whole head dim

@@ -23,10 +23,10 @@ def step_bytes(w, positions, distinct_experts_per_layer) -> dict:
     """w: workload shape; positions[b]: the new token's position (= cached length);
     distinct_experts_per_layer: number of distinct experts routed in each layer."""
     positions = np.asarray(positions, dtype=np.int64)
-    de = np.asarray(distinct_experts_per_layer, dtype=np.int64)
+    de = np.asarray(distinct_experts_per_layer, dtype=np.float64)  # may be a mean over steps
     assert de.shape == (w.L,)
     dense = w.L * (w.qkv_rows * w.H + w.H * w.nq * w.d + w.E * w.H + w.H) * BF16
-    experts = int(de.sum()) * 3 * w.I * w.H * BF16
+    experts = int(round(float(de.sum()) * 3 * w.I * w.H * BF16))
     head = (w.V * w.H + w.H + len(positions) * w.H) * BF16
     kv_row = w.L * 2 * w.nkv * w.d * BF16
     kv_read = int((positions + 1).sum()) * kv_row

@@ -53,18 +53,26 @@ def _run(w, steps, per_layer=False, mode=0):
                             keep[:, :, pos[b] % w.page] = False
                     assert np.array_equal(after[keep], before[pg][keep]), "KV bytes outside the new slots changed"
             # values: one bf16 rounding apart, plus the error the step's input carries at depth.
-            # The GPU carries every GEMV input as a bf16 hi + lo pair (>= 16 significant bits),
-            # so each layer adds up to ~2^-16 relative error to the residual stream: over L layers
-            # at most L * 2^-16 (7.3e-4 at 48 layers) of the head's rms, bounded here by 1e-3.
-            kv_abs = max(1e-4, w.L * 2.0 ** -16)
+            # The new k and v are outputs of the same QKV GEMV as q, from the same normalized
+            # input, so they get q's absolute tolerance (2e-4 of the largest magnitude in the
+            # head, as in _check_layers) on top of one bf16 rounding of the value itself.
+            kv_abs = 2e-4
             for b in range(w.B):
                 pg, sl = s.bt[b, pos[b] // w.page], pos[b] % w.page
-                for got, ref in ((_bits(s.K[:, pg, :, sl]), tr["k_new"][:, b]), (_bits(s.V[:, pg, :, sl]), tr["v_new"][:, b])):
+                for kv, got, ref in (("K", _bits(s.K[:, pg, :, sl]), tr["k_new"][:, b]),
+                                     ("V", _bits(s.V[:, pg, :, sl]), tr["v_new"][:, b])):
                     g32 = synth.bf16_bits_to_f32(got).astype(np.float64)
                     r32 = synth.bf16_bits_to_f32(ref).astype(np.float64)
-                    scale = np.sqrt(np.mean(r32 ** 2, axis=-1, keepdims=True))
-                    assert np.all(np.abs(g32 - r32) <= 2.0 ** -7 * np.abs(r32) + kv_abs * scale), \
-                        "appended K/V differ from the oracle beyond bf16 rounding and the input's error"
+                    scale = np.abs(r32).max(axis=-1, keepdims=True)
+                    bound = 2.0 ** -7 * np.abs(r32) + kv_abs * scale
+                    bad = np.abs(g32 - r32) > bound
+                    if bad.any():
+                        l_, g_, e_ = np.argwhere(bad)[0]
+                        raise AssertionError(
+                            f"step {i} row {b} pos {pos[b]}: appended {kv} differs from the oracle beyond bf16 "
+                            f"rounding and the input's error at {bad.sum()} elements; first at layer {l_} group {g_} "
+                            f"dim {e_}: gpu {g32[l_, g_, e_]:.6g} oracle {r32[l_, g_, e_]:.6g} bound {bound[l_, g_, e_]:.3g}"
+                            f" (scale {scale[l_, g_, 0]:.3g})")
             tokens = ref_next  # teacher forcing
     finally:
         s.close()
@@ -99,7 +107,9 @@ def test_tiny_batch3_ragged():
 
 
 def test_small_bs8_ragged_teacher_forced():
-    _run(W.SMALL, 16, per_layer=True)
+    """All 128 greedy steps of the small batch-8 workload, so the >= 99 % greedy-agreement bar
+    is taken over 1,024 tokens."""
+    _run(W.SMALL, 128, per_layer=True)
 
 
 def test_per_op_mode_matches_megakernel_bitwise():
@@ -154,14 +164,22 @@ def test_30b_shape_4_layers_bs1_ctx8k_per_layer():
 
 @pytest.mark.slow
 def test_30b_bs1_ctx8k_full_size():
-    _run(W.M30B_BS1, 2)
+    """The headline workload at full size (61 GB of weights), 32 teacher-forced steps."""
+    _run(W.M30B_BS1, 32)
 
 
 @pytest.mark.slow
 def test_30b_bs8_uniform_full_size():
-    _run(W.M30B_BS8, 1)
+    _run(W.M30B_BS8, 8)
 
 
 @pytest.mark.slow
 def test_30b_bs8_zipf_full_size():
-    _run(W.M30B_BS8_ZIPF, 1)
+    _run(W.M30B_BS8_ZIPF, 8)
+
+
+@pytest.mark.slow
+def test_30b_bs1_ctx256k_full_size():
+    """The long-context workload: 262,144 cached positions (26 GB of paged KV), 2 steps. The
+    oracle synthesises the cache on read, so no host copy of it is made."""
+    _run(W.M30B_256K, 2)
