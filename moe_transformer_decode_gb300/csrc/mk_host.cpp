@@ -43,8 +43,9 @@ struct mk_ctx {
   long long wait_ns = 2000000000LL;  // device-side wait limit
   std::string err;
   // workspace (device)
-  float *xs, *q, *knew, *vnew, *attn_o, *attn_out, *rlogits, *moe_out, *apart, *lm_best_v;
-  uint16_t *attn_hl, *h;
+  float *xs, *q, *knew, *vnew, *attn_o, *attn_out, *rlogits, *moe_out, *moe_part, *apart, *lm_best_v;
+  uint16_t* attn_hl;
+  uint8_t* hsw;
   int32_t* lm_best_i;
   int32_t* topk_ids;
   float* topk_w;
@@ -76,6 +77,35 @@ struct mk_ctx {
   unsigned long long* trace_count;
   long long trace_cap;
 };
+
+// The expert weights as 3D bf16 views {64, rows, K / 64} (strides: a row, 128 bytes) with 128B
+// swizzle, so that one box lands kGuRows or kTcN rows x 64 columns as the tcgen05 B operand.
+mk_status mk::encode_expert_maps(void* encode_fn, const mk_model_cfg& m, const mk_weight_ptrs* w, TensorMaps& tm) {
+  EncodeTiledFn enc = (EncodeTiledFn)encode_fn;
+  const uint64_t gu_rows = (uint64_t)m.n_layers * m.n_experts * 2 * m.expert_inter;
+  const uint64_t dn_rows = (uint64_t)m.n_layers * m.n_experts * m.hidden;
+  if (gu_rows >= (1ull << 31) || dn_rows >= (1ull << 31)) return MK_ERR_UNSUPPORTED;
+  cuuint32_t estr[3] = {1, 1, 1};
+  {
+    cuuint64_t dims[3] = {64, (cuuint64_t)gu_rows, (cuuint64_t)m.hidden / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)m.hidden * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kGuRows, 1};
+    if (enc(&tm.gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w->w_gate_up), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MK_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[3] = {64, (cuuint64_t)dn_rows, (cuuint64_t)m.expert_inter / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)m.expert_inter * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTcN, 1};
+    if (enc(&tm.dn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w->w_down), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MK_ERR_CUDA;
+  }
+  return MK_OK;
+}
 
 static mk_status fail(mk_ctx* c, mk_status s, const std::string& msg) {
   if (c) c->err = msg;
@@ -117,7 +147,7 @@ extern "C" void mk_destroy(mk_ctx* c) {
   if (!c) return;
   free_schedule(c);
   cudaFree(c->xs); cudaFree(c->q); cudaFree(c->knew); cudaFree(c->vnew); cudaFree(c->attn_o); cudaFree(c->attn_out);
-  cudaFree(c->rlogits); cudaFree(c->h); cudaFree(c->attn_hl); cudaFree(c->moe_out); cudaFree(c->lm_best_v); cudaFree(c->lm_best_i);
+  cudaFree(c->rlogits); cudaFree(c->hsw); cudaFree(c->attn_hl); cudaFree(c->moe_out); cudaFree(c->moe_part); cudaFree(c->lm_best_v); cudaFree(c->lm_best_i);
   cudaFree(c->route); cudaFree(c->rope); cudaFree(c->status); cudaFree(c->topk_ids); cudaFree(c->topk_w);
   if (c->status_host) cudaFreeHost(c->status_host);
   delete c;
@@ -211,7 +241,8 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
              dalloc(&c->vnew, L * Bm * m.n_kv_heads * d) == cudaSuccess && dalloc(&c->attn_o, L * Bm * od) == cudaSuccess && dalloc(&c->attn_hl, L * 2 * Bm * od) == cudaSuccess &&
              dalloc(&c->attn_out, L * Bm * H) == cudaSuccess && dalloc(&c->moe_out, L * Bm * H) == cudaSuccess &&
              dalloc(&c->rlogits, L * Bm * m.n_experts) == cudaSuccess &&
-             dalloc(&c->h, L * kMaxActive * 2 * kMaxB * (size_t)m.expert_inter) == cudaSuccess &&
+             dalloc(&c->hsw, L * kMaxActive * hsw_slot_bytes(m.expert_inter)) == cudaSuccess &&
+             dalloc(&c->moe_part, L * kMoeParts * Bm * H) == cudaSuccess &&
              dalloc(&c->route, L) == cudaSuccess && dalloc(&c->lm_best_v, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
              dalloc(&c->lm_best_i, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
              dalloc(&c->rope, (size_t)c->max_pos * (d / 2)) == cudaSuccess && dalloc(&c->status, ST_WORDS) == cudaSuccess &&
@@ -243,6 +274,14 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
       }
     e = cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) { mk_destroy(c); return MK_ERR_CUDA; }
+  }
+  // the expert weights as tcgen05 B operand tiles (3D views {64, rows, K / 64}, 128B swizzle)
+  {
+    const mk_status ts = encode_expert_maps((void*)c->encode, m, w, c->tm);
+    if (ts != MK_OK) {
+      mk_destroy(c);
+      return ts;
+    }
   }
   e = configure_kernels();
   if (e != cudaSuccess) {
@@ -357,7 +396,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     if (seq_lens[b] < 0 || seq_lens[b] >= m.max_pages_per_seq * kPage) return MK_ERR_INVALID_ARG;
   const int L = m.n_layers, H = m.hidden, d = m.head_dim, nkv = m.n_kv_heads, G = m.n_q_heads / nkv;
   const int E = m.n_experts, I = m.expert_inter, V = m.vocab, od = m.n_q_heads * d;
-  const Geo gh = geo_of(H), go = geo_of(od), gi = geo_of(I);
+  const Geo gh = geo_of(H), go = geo_of(od);
   const int pps = kStagePayload / (4096 * (d / 64));
   CounterMap cmap{L, nkv, B};
   std::vector<int32_t>& cnt = P.cnt;
@@ -420,7 +459,10 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     P.max_chunks = std::max(P.max_chunks, P.n_chunks[b]);
   }
 
-  const int tiles = 2 * I / gh.RS;  // gate/up tiles: RS consecutive rows of [gate; up]
+  // expert GEMVs (tcgen05): gate/up units of kGuRows gate rows + the matching up rows over H;
+  // down units of kTcN output rows for one of `parts` partials (experts of rank j mod parts)
+  const int tiles = I / kGuRows;
+  const int parts = std::min(kMoeParts, maxa);
   // Per layer, gate/up tasks are sized to about two per expert SM and QKV tasks to about two
   // per SM (whole stages each, rounded up so that no SM gets a third). When the SMs are
   // partitioned, QKV runs on every SM but the router's, about one task each: it needs only the
@@ -429,7 +471,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   const int qkv_tasks = n_attn < n_sm ? n_sm - (E + gh.RS - 1) / gh.RS : 2 * n_attn;
   int qkv_per_task = std::max(1, (nkv * upg_ + qkv_tasks - 1) / qkv_tasks);
   qkv_per_task = std::max(gh.RG, (qkv_per_task + gh.RG - 1) / gh.RG * gh.RG);
-  const int gu_per_task = std::max(1, (maxa * tiles + 2 * n_moe - 1) / (2 * n_moe));
+  const int gu_per_task = std::max(1, (maxa * tiles + n_moe - 1) / n_moe);
   const long long row_h = 2LL * H;
 
   Assigner as(n_sm, part, PM + 1);
@@ -483,11 +525,11 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
       cnt[cmap.qkv(l, g)] = n;
     }
     emit(ts, n_attn < n_sm ? -1 : PA);
-    // expert gate/up: units u = tile * maxa + active_rank
+    // expert gate/up: units u = tile * maxa + active_rank, about one task per expert SM
     int n_gu = 0;
     for (int u = 0; u < maxa * tiles; u += gu_per_task, ++n_gu) {
       const int n = std::min(gu_per_task, maxa * tiles - u);
-      ts.push_back({mkt(OP_GU, l, u, n, 0), (long long)(n * live * gh.RS * row_h)});
+      ts.push_back({mkt(OP_GU, l, u, n, 0), (long long)(n * live * 2 * kGuRows * row_h)});
     }
     cnt[cmap.gu(l)] = n_gu;
     emit(ts, PM);
@@ -507,21 +549,11 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
       per_op.push_back(std::move(lists));
     }
     for (int g = 0; g < nkv; ++g) cnt[cmap.attn(l, g)] = B;
-    // expert down rows over all active experts: blocks of RS rows while they number at most one
-    // per expert SM; else one task per expert SM of 8-row blocks (passes of RS rows), so that
-    // no SM takes two tasks while another takes one (the layer ends with its last down task)
+    // expert down: units u = row block * parts + part (kTcN rows over the routed experts of rank
+    // part, part + parts, ...), one per task
     int n_down = 0;
-    {
-      const int nb = (H + gi.RS - 1) / gi.RS, nb8 = (H + 7) / 8;
-      const int n_t = nb <= n_moe ? nb : std::min(n_moe, nb8);
-      int r0 = 0;
-      for (int i = 0; i < n_t; ++i, ++n_down) {
-        const int rows = nb <= n_moe ? gi.RS : 8 * (nb8 / n_t + (i < nb8 % n_t ? 1 : 0));
-        const int n = std::min(rows, H - r0);
-        ts.push_back({mkt(OP_DOWN, l, r0, n, 0), (long long)(n * 2.0 * I * maxa * live)});
-        r0 += n;
-      }
-    }
+    for (int u = 0; u < (H / kTcN) * parts; ++u, ++n_down)
+      ts.push_back({mkt(OP_DOWN, l, u, 1, 0), (long long)((double)kTcN * I * 2 * live * maxa / parts)});
     emit(ts, PM);
     // O-proj: blocks of RS rows; at batch <= 4 (and at most two 2048-column chunks) a task takes
     // several blocks, reusing one load of the attention output, about one task per SM
@@ -693,7 +725,8 @@ static Params make_params(mk_ctx* c, const int32_t* tokens, const int32_t* posit
   p.tasks = c->d_tasks; p.sm_begin = c->d_sm_begin; p.cnt_per_step = c->d_cnt;
   p.chunk_pages = c->d_chunk_pages; p.n_chunks = c->d_n_chunks;
   p.xs = c->xs; p.q = c->q; p.knew = c->knew; p.vnew = c->vnew; p.apart = c->apart; p.attn_o = c->attn_o;
-  p.attn_out = c->attn_out; p.rlogits = c->rlogits; p.h = c->h; p.attn_hl = c->attn_hl; p.moe_out = c->moe_out; p.route = c->route;
+  p.attn_out = c->attn_out; p.rlogits = c->rlogits; p.hsw = c->hsw; p.attn_hl = c->attn_hl; p.moe_out = c->moe_out;
+  p.moe_part = c->moe_part; p.moe_parts = std::min(kMoeParts, std::min(c->B * m.top_k, m.n_experts)); p.route = c->route;
   p.lm_best_v = c->lm_best_v; p.lm_best_i = c->lm_best_i; p.counters = c->counters; p.status = c->status;
   p.status_host = c->status_host_dev; p.topk_ids = c->topk_ids; p.topk_w = c->topk_w;
   p.trace = c->trace; p.trace_count = c->trace_count; p.trace_cap = c->trace_cap;

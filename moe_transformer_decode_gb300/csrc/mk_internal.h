@@ -20,8 +20,21 @@ static_assert(kConsumerWarps == 8, "two consumer warpgroups");
 static_assert(kProducerRegs * 128 + kConsumerRegs * 256 <= (65536 / kThreads) / 8 * 8 * kThreads,
               "register split exceeds the launch's allotment");
 constexpr int kStagePayload = 32768;                 // data bytes of a ring stage
-constexpr int kStageBytes = kStagePayload;           // ring slot
-constexpr int kStages = 6;
+// ring slot: a stage, plus room for the tcgen05 A chunk (2 KB) an expert-down stage carries
+constexpr int kStageBytes = kStagePayload + 2048;
+constexpr int kStages = 4;
+// Expert GEMVs on tcgen05 (weights as the N operand, tokens x {hi, lo} as M): a stage is
+// kTcN weight rows x kTcK columns; a gate/up unit is kGuRows gate rows and the matching up rows
+// (N = kTcN); a down unit is kTcN output rows over the experts of one of kMoeParts partials.
+constexpr int kTcN = 256;
+constexpr int kTcK = 64;
+constexpr int kGuRows = kTcN / 2;
+constexpr int kMoeParts = 8;
+constexpr int kTmemCols = 512;
+// the A operand (tokens x {hi, lo}, 8 rows per group, groups of 4 tokens) for one 64-column
+// chunk: kMaxB / 4 groups of 1 KB
+constexpr int kAChunkMax = (8 / 4) * 1024;  // 8 = kMaxB
+constexpr int kABufBytes = 32 * kAChunkMax;          // the normalized input, hidden <= 2048
 // Counters sit kCounterStride words (128 bytes) apart, so the lines that waiting warps poll spread
 // over the L2 slices instead of all landing on one.
 constexpr int kCounterStride = 32;
@@ -36,9 +49,9 @@ enum Op : uint8_t {
   OP_ROUTER = 1,  // router logits for a block of experts; last one computes top-k routing
   OP_QKV = 2,     // QKV rows + RoPE + KV append, a range of 8-row units of one KV group
   OP_ATTN = 3,    // paged GQA attention of one (sequence, KV group, chunk); last chunk combines
-  OP_GU = 4,      // expert gate/up rows + SiLU*mul, a range of (tile, active-expert) units
+  OP_GU = 4,      // expert gate/up + SiLU*mul, a range of (row block, active expert) units
   OP_O = 5,       // O-proj rows, each warp released by its KV group's counter
-  OP_DOWN = 6,    // expert down rows over all active experts + weighted combine
+  OP_DOWN = 6,    // expert down: (row block, partial) units, each over its share of the experts
   OP_LM = 7       // LM-head rows + running argmax; the last LM task of the step reduces
 };
 enum TaskFlag : uint8_t {
@@ -109,10 +122,17 @@ struct Params {
   const int32_t* n_chunks;     // [B]
   // workspace
   float *xs, *q, *knew, *vnew, *apart, *attn_o, *attn_out, *rlogits, *moe_out;
+  // expert down outputs as kMoeParts partials [L][kMoeParts][B][H] (part j sums the routed
+  // experts of rank j mod parts), added in order by the next layer's residual + norm
+  float* moe_part;
+  int moe_parts;
   // activations stored as bf16 hi/lo planes (hi = bf16(v), lo = bf16(v - hi)), the form the
-  // tensor-core GEMV consumes: attention output [L][2][B][n_q d]; expert activations
-  // SiLU(gate) * up * routing weight [L][max active][2][max batch][I]
-  uint16_t *attn_hl, *h;
+  // tensor-core GEMV consumes: attention output [L][2][B][n_q d]
+  uint16_t* attn_hl;
+  // expert activations SiLU(gate) * up * routing weight as the tcgen05 A operand, per (layer,
+  // active-expert rank): [I / 64 chunks][B > 4 ? 2 : 1 groups][8 rows = 4 tokens x {hi, lo}]
+  // [128 bytes, 16-byte units XOR-swizzled by row], a slot of kHSlotBytes(I)
+  uint8_t* hsw;
   Route* route;
   float* lm_best_v;
   int32_t* lm_best_i;
@@ -146,6 +166,14 @@ struct TensorMaps {
   // half of it 128 bytes), box {64, 16, head_dim / 64}, 128B swizzle: one copy lands a page's
   // rows as [half][row][128 bytes]
   CUtensorMap k, v;
+  // expert weights as 3D {64, rows, K / 64} bf16 views with 128B swizzle (the tcgen05 operand
+  // layout): gate/up rows [L][E][2I] over K = hidden, box {64, kGuRows, 1}; down rows [L][E][H]
+  // over K = I, box {64, kTcN, 1}
+  CUtensorMap gu, dn;
 };
+// bytes of one expert's activation slot in Params::hsw
+inline __host__ __device__ size_t hsw_slot_bytes(int I) { return (size_t)(I / 64) * kAChunkMax; }
+// encodes TensorMaps::gu and ::dn over the caller's expert weights (encode_fn: cuTensorMapEncodeTiled)
+mk_status encode_expert_maps(void* encode_fn, const mk_model_cfg& m, const mk_weight_ptrs* w, TensorMaps& tm);
 
 }  // namespace mk

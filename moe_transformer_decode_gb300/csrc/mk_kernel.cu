@@ -83,6 +83,48 @@ __device__ __forceinline__ void tma_3d_g2s(uint32_t dst, const CUtensorMap* map,
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
       : "memory");
 }
+// ------------------------------------------------------------------ tcgen05 (5th-generation tensor cores)
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle (rows of 128 bytes, 16-byte
+// units XOR-swizzled by row within 1 KB groups of 8 rows), sbo = byte distance between 8-row
+// groups along M or N (0 makes every group alias the first: 8 distinct rows).
+__device__ __forceinline__ uint64_t tc_sdesc(uint32_t addr, uint32_t sbo) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                  // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(sbo >> 4) << 32;         // stride byte offset
+  d |= (uint64_t)1 << 46;                  // descriptor version
+  d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+  return d;
+}
+// instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 accumulator, M x N
+__host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// arrive once on the mbarrier when every tcgen05.mma this thread issued so far has completed
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (lane i of the warp reads lane
+// 32 (warp % 4) + i); the wait is in the same statement, so no register is read before it lands
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(n) : "memory");
+}
+
 // L2 policy for data read once per step (weights, KV pages): evicted first, so that the code,
 // activations and counters the step keeps touching stay resident
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -235,6 +277,17 @@ __device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity) {
   }
 }
 
+// Spinning bounded mbarrier wait, for barriers whose phases complete by asynchronous arrivals
+// (tensor-core commits, copy completions) that the waiter must see at once: a warp suspended in
+// try_wait is not woken early by them.
+__device__ bool mbar_wait_spin(const Params& p, uint32_t bar, uint32_t parity) {
+  WaitClock wc;
+  for (int i = 0;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && !wc.keep_going(p, -1, (int)parity)) return false;
+  }
+}
+
 // For the consumer warps' own barrier: re-test with the default short blocking wait instead of
 // a long suspend, so the warps resume as soon as the last one arrives.
 __device__ bool mbar_wait_cta(const Params& p, uint32_t bar, uint32_t parity) {
@@ -314,6 +367,8 @@ struct Misc {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t cbar;                     // consumer-warps barrier (8 arrivals per phase)
+  uint64_t tc_acc;                   // tcgen05: a unit's products have all completed (commit)
+  uint32_t tmem_base;                // tcgen05: the block's tensor memory (kTmemCols columns)
   uint64_t gpart[kRedBufs];          // GEMV pass buffers: every consumer warp's partials are in
   uint64_t gfree[kRedBufs];          // ... and: the pass's epilogue warp has read them
   union {
@@ -346,17 +401,12 @@ struct Misc {
   int pr_n;
   int pr_expert[kMaxActive];
   int pr_ids[kIdCache];
-  // batch 1: the normalized input's mma fragments (only lanes 0-7 hold data: hi and lo of
-  // token 0), per warp and k-step
-  // batch 1: per warp, lanes 0-7 each own 128 bytes holding their (a0, a2) fragment registers of
-  // k-steps 0-15; the 16-byte chunk of k-steps (2 j, 2 j + 1) sits at chunk j ^ lane, so the eight
-  // lanes' 16-byte loads of one pair hit distinct banks
-  alignas(16) uint2 nf1[kConsumerWarps][8][16];
   // per-warp LM argmax candidates per token
   float lmw_v[kConsumerWarps][kMaxB];
   int lmw_i[kConsumerWarps][kMaxB];
 };
-constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + ((int)sizeof(Misc) + 127) / 128 * 128;
+// shared memory: the ring, the tcgen05 A operand of the normalized input, then Misc
+constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kABufBytes + ((int)sizeof(Misc) + 127) / 128 * 128;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds the sm_103a opt-in limit");
 static_assert(offsetof(Misc, red) % 16 == 0 && offsetof(Misc, st_rope) % 16 == 0 &&
                   offsetof(Misc, nsm) % 16 == 0,
@@ -528,22 +578,24 @@ struct Producer {
         return true;
       }
       case OP_GU: {
+        // unit u = (row block j = u / maxa, active expert a = u % maxa): kGuRows gate rows and the
+        // matching up rows over the hidden dim, stage s = columns [64 s, 64 s + 64): the gate
+        // rows land as rows 0..kGuRows-1 of the stage, the up rows after them (one 2D-swizzled
+        // [kTcN rows][128 bytes] tile, the tcgen05 B operand)
         if (!route(l)) return false;
-        const int na = m.pr_n, maxa = max_active(p);
-        const Geo g = geo_of(p.H);
-        const int half = g.RS / 2;
+        const int na = m.pr_n, maxa = max_active(p), nst = p.H / kTcK;
 #pragma unroll 1
         for (int u = t.a; u < t.a + t.b; ++u) {
-          const int a = u % maxa, tile = u / maxa;
+          const int a = u % maxa, j = u / maxa;
           if (a >= na) continue;
-          const int e = m.pr_expert[a];
-          // tile: gate rows [tile RS/2, +RS/2) then the matching up rows (I rows further on)
-          const uint16_t* W = p.w_gate_up + ((size_t)l * p.E + e) * 2 * p.I * p.H;
-          if (!begin((uint32_t)g.RS * p.H * 2)) return false;
-          if (lane < 2)  // lane 0: the gate rows, lane 1: the matching up rows
-            bulk_g2s(dst + (uint32_t)(lane * half * g.RST), W + ((size_t)lane * p.I + tile * half) * p.H,
-                     (uint32_t)half * p.H * 2, bar, pol);
-          end();
+          const int grow = ((l * p.E + m.pr_expert[a]) * 2 * p.I) + j * kGuRows;
+#pragma unroll 1
+          for (int st = 0; st < nst; ++st) {
+            if (!begin(kStagePayload)) return false;
+            if (lane < 2)  // lane 0: the gate rows, lane 1: the up rows (I rows further on)
+              tma_3d_g2s(dst + (uint32_t)lane * (kStagePayload / 2), &tm.gu, 0, grow + lane * p.I, st, bar, pol);
+            end();
+          }
         }
         return true;
       }
@@ -558,38 +610,39 @@ struct Producer {
         return true;
       }
       case OP_DOWN: {
+        // unit u = (row block rb = u / parts, partial j = u % parts): output rows [kTcN rb, +kTcN)
+        // over the routed experts of rank j, j + parts, ...; per expert I / 64 stages, stage s
+        // holding the kTcN weight rows' columns [64 s, 64 s + 64) and, after them, the expert's
+        // activations of those columns (the A chunk), so no stage outlives its own products
         if (!route(l)) return false;
-        const int na = m.pr_n;
-        const Geo g = geo_of(p.I);
+        const int na = m.pr_n, parts = p.moe_parts, nst = p.I / kTcK;
+        const uint32_t achunk = p.B > 4 ? 2048u : 1024u;
         bool gu_done = false;
 #pragma unroll 1
-        for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS) {  // passes of RS rows
-          const int rows = min(g.RS, t.a + t.b - r0);
+        for (int u = t.a; u < t.a + t.b; ++u) {
+          const int rb = u / parts, part = u % parts;
 #pragma unroll 1
-          for (int a = 0; a < na; ++a) {
-            const int e = m.pr_expert[a];
-            const uint16_t* W = p.w_down + (((size_t)l * p.E + e) * p.H + r0) * p.I;
-            if (!gemv_rows(W, rows, p.I, p.I * 2)) return false;
-            // then the expert's activations: row hl * B + b holds plane hl (hi, lo) of token b.
-            // They exist once every gate/up task of the layer is done (the first weight stage
-            // above is already on its way).
+          for (int a = part; a < na; a += parts) {
             if (!gu_done) {
               int fine = 1;
               if (lane == 0) fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.gu(l));
               if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
-              // p.h was written by the gate/up epilogues' generic stores (other SMs) and published by
-              // their release; lane 0's acquire made it visible to the warp, and this fence orders it
-              // before the bulk copies below, which read it through the async proxy
+              // p.hsw was written by the gate/up epilogues' generic stores (other SMs) and published
+              // by their release; lane 0's acquire made it visible to the warp, and this fence orders
+              // it before the bulk copies below, which read it through the async proxy
               __syncwarp();
               fence_proxy_async_global();
               gu_done = true;
             }
-            if (!begin((uint32_t)2 * p.B * p.I * 2)) return false;
-            const uint16_t* hp = p.h + (((size_t)l * kMaxActive + a) * 2 * kMaxB) * p.I;
-            if (lane < 2)  // plane `lane` (hi, lo): the batch's rows are consecutive
-              bulk_g2s(dst + (uint32_t)(lane * p.B * p.I * 2), hp + (size_t)lane * kMaxB * p.I, (uint32_t)p.B * p.I * 2,
-                       bar, pol);
-            end();
+            const int row = (l * p.E + m.pr_expert[a]) * p.H + rb * kTcN;
+            const uint8_t* hs = p.hsw + ((size_t)l * kMaxActive + a) * hsw_slot_bytes(p.I);
+#pragma unroll 1
+            for (int st = 0; st < nst; ++st) {
+              if (!begin(kStagePayload + achunk)) return false;
+              if (lane == 0) tma_3d_g2s(dst, &tm.dn, 0, row, st, bar, pol);
+              if (lane == 1) bulk_g2s(dst + kStagePayload, hs + (size_t)st * achunk, achunk, bar, pol);
+              end();
+            }
           }
         }
         return true;
@@ -665,20 +718,25 @@ struct Consumer {
   uint32_t gv;          // GEMV passes done (every consumer warp counts the same sequence)
   int n_layer;          // layer whose normalized input is held in `nf` (-1 none)
   int route_layer;      // layer whose routing is cached in m.rc_*
-  int gu_layer;         // layer whose expert gate/up work is known complete
   int attn_layer;       // layer of attn_ok
   uint32_t attn_ok;     // KV groups whose attention is known complete in attn_layer
   // the normalized input of layer n_layer, this warp's 256-column slice as mma A fragments:
   // lane (g, t) holds the hi (g even) or lo (g odd) part of token g/2 (registers 0, 1) and of
   // token g/2 + 4 (registers 2, 3) at columns 16 s + 2 t + {0, 1} and + {8, 9}
-  uint32_t nf[NB > 1 ? 16 : 1][AR];  // batch 1 keeps them in m.nf1 instead
+  uint32_t nf[NB > 1 ? 16 : 1][AR];  // batch 1 reads them from the A operand in shared memory
   float lm_best[NB];    // running LM-head argmax of the stages whose epilogue this lane ran
   int lm_idx[NB];
   uint64_t t_start, t_ready;
+  // tcgen05 state (used by warp 0, which runs the expert GEMVs): the A operand of the normalized
+  // input in shared memory (chunks of kAChunk bytes), the block's tensor memory, and the parity
+  // of the next completion of m.tc_acc
+  static constexpr uint32_t kAChunk = (NB > 4 ? 2u : 1u) * 1024u;
+  static constexpr int kAGroups = NB > 4 ? 2 : 1;
+  uint32_t abuf, tmem, tc_phase;
 
-  __device__ Consumer(const Params& p_, Misc& m_, Ring r_)
-      : p(p_), m(m_), r(r_), cm{p_.L, p_.nkv, p_.B}, ok(true), n_layer(-1), route_layer(-1), gu_layer(-1),
-        attn_layer(-1), attn_ok(0) {
+  __device__ Consumer(const Params& p_, Misc& m_, Ring r_, uint32_t abuf_)
+      : p(p_), m(m_), r(r_), cm{p_.L, p_.nkv, p_.B}, ok(true), n_layer(-1), route_layer(-1),
+        attn_layer(-1), attn_ok(0), abuf(abuf_), tmem(m_.tmem_base), tc_phase(0) {
     warp = threadIdx.x / 32;
     lane = threadIdx.x % 32;
     cbar = smem_addr(&m_.cbar);
@@ -693,16 +751,6 @@ struct Consumer {
 
   __device__ const uint8_t* acquire() {
     const uint32_t s = r.it % kStages, parity = (r.it / kStages) & 1u;
-    if (!mbar_wait(p, r.full + 8 * s, parity)) {
-      ok = false;
-      return nullptr;
-    }
-    return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(r.data + s * kStageBytes));
-  }
-  // the ring slot k stages after the next one (held together with it)
-  __device__ const uint8_t* acquire_at(uint32_t k) {
-    const uint32_t it = r.it + k;
-    const uint32_t s = it % kStages, parity = (it / kStages) & 1u;
     if (!mbar_wait(p, r.full + 8 * s, parity)) {
       ok = false;
       return nullptr;
@@ -763,11 +811,22 @@ struct Consumer {
         x[b][0] = bf_lo(w.x); x[b][1] = bf_hi(w.x); x[b][2] = bf_lo(w.y); x[b][3] = bf_hi(w.y);
         x[b][4] = bf_lo(w.z); x[b][5] = bf_hi(w.z); x[b][6] = bf_lo(w.w); x[b][7] = bf_hi(w.w);
       } else {
-        float a[8], mo[8];
+        float a[8], mo[8], mp[8];
         const size_t o = ((size_t)(l - 1) * p.B + b) * p.H + col;
         load8(p.xs + o, x[b]);
         load8(p.attn_out + o, a);
-        load8(p.moe_out + o, mo);
+        // the expert branch's output is the sum of its partials, added in part order
+        load8(p.moe_part + ((size_t)(l - 1) * kMoeParts * p.B + b) * p.H + col, mo);
+        for (int j = 1; j < p.moe_parts; ++j) {
+          load8(p.moe_part + (((size_t)(l - 1) * kMoeParts + j) * p.B + b) * p.H + col, mp);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mo[i] += mp[i];
+        }
+        if (write_x && warp < g.KW) {
+          float4* dm = reinterpret_cast<float4*>(p.moe_out + o);
+          __stcg(dm, make_float4(mo[0], mo[1], mo[2], mo[3]));
+          __stcg(dm + 1, make_float4(mo[4], mo[5], mo[6], mo[7]));
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[b][i] = (x[b][i] + a[i]) + mo[i];
       }
@@ -807,6 +866,22 @@ struct Consumer {
       float xn[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) xn[i] = x[b][i] * rinv * gf[i];
+      if (warp < g.KW) {
+        // tcgen05 A operand (expert gate/up): row 2 (b % 4) + {hi, lo} of group b / 4, this lane's
+        // 8 columns as one 16-byte unit of chunk col / 64 (tokens past the batch are zero rows)
+        const int q = b >> 2, r0 = 2 * (b & 3), u16 = (col & 63) >> 3;
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (b < p.B) split_pack(xn[2 * i], xn[2 * i + 1], hw[i], lw[i]);
+          else hw[i] = lw[i] = 0u;
+        }
+        const uint32_t base = abuf + (uint32_t)(col >> 6) * kAChunk + (uint32_t)q * 1024u;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + r0 * 128 + ((u16 ^ r0) << 4)), "r"(hw[0]),
+                     "r"(hw[1]), "r"(hw[2]), "r"(hw[3]) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + (r0 + 1) * 128 + ((u16 ^ (r0 + 1)) << 4)),
+                     "r"(lw[0]), "r"(lw[1]), "r"(lw[2]), "r"(lw[3]) : "memory");
+      }
       __syncwarp();
       float4* d4 = reinterpret_cast<float4*>(xw + lane * 8);
       d4[0] = make_float4(xn[0], xn[1], xn[2], xn[3]);
@@ -817,9 +892,7 @@ struct Consumer {
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
           const float4 v = *reinterpret_cast<const float4*>(xw + 32 * (s >> 1) + 8 * t4 + 4 * (s & 1));
-          if constexpr (NB == 1) {
-            m.nf1[warp][lane][2 * ((s >> 1) ^ lane) + (s & 1)] = make_uint2(pack_part(v.x, v.y, hl), pack_part(v.z, v.w, hl));
-          } else {
+          if constexpr (NB > 1) {  // batch 1 reads its fragments from the A operand in shared memory
             nf[s][0] = pack_part(v.x, v.y, hl);
             nf[s][1] = pack_part(v.z, v.w, hl);
           }
@@ -837,6 +910,17 @@ struct Consumer {
       }
     }
     __syncwarp();
+    // the A operand's groups beyond the batch's last token are zero rows too
+    if constexpr (NB % 4 != 0) {
+      if (warp < g.KW) {
+        const int u16 = (col & 63) >> 3;
+        const uint32_t base = abuf + (uint32_t)(col >> 6) * kAChunk;
+#pragma unroll
+        for (int r = 2 * NB; r < 8; ++r)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + r * 128 + ((u16 ^ r) << 4)), "r"(0u) : "memory");
+      }
+    }
+    fence_proxy_async_smem();  // generic stores that the tensor cores read through the async proxy
     if (write_x && warp < g.KW) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
@@ -965,11 +1049,15 @@ struct Consumer {
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&m.gfree[buf]));
   }
-  // batch 1: as mma_rows, A fragments of the normalized input from m.nf1, two k-steps per 16-byte
-  // load (lanes 0-7 hold the hi and lo parts of token 0; every other lane's are zero)
+  // batch 1: as mma_rows, A fragments of the normalized input read from the tcgen05 A operand in
+  // shared memory, two k-steps per 16-byte load: lane (g, t) < 8 of k-step pair q (columns
+  // [32 q, 32 q + 32) of this warp's slice) takes 16-byte unit 4 (q % 2) + t of row g (0: hi,
+  // 1: lo of token 0) of 64-column chunk 4 ks + q / 2, which holds its (a0, a2) registers of
+  // k-steps 2 q and 2 q + 1 in the column map above; every other lane's are zero
   __device__ __forceinline__ void mma_rows_nf1(const uint8_t* st, const Geo& g, int rg, int ks, float (&c)[4][4]) const {
     const uint8_t* rowp = b_row(st, g, rg, ks);
-    const uint32_t fr = (uint32_t)__cvta_generic_to_shared(&m.nf1[warp][lane & 7][0]);
+    const int r = (lane >> 2) & 1, t4 = lane & 3;
+    const uint32_t fr = abuf + (uint32_t)(4 * ks) * kAChunk + r * 128;
     const bool has = lane < 8;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
@@ -978,7 +1066,8 @@ struct Consumer {
       const uint32_t bw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int hp = 0; hp < 2; ++hp) {  // k-steps 4 jj + 2 hp and 4 jj + 2 hp + 1
-        const uint4 f = has ? lds128(fr + (((2 * jj + hp) ^ (lane & 7)) & 7) * 16) : make_uint4(0u, 0u, 0u, 0u);
+        const int q = 2 * jj + hp, unit = 4 * (q & 1) + t4;
+        const uint4 f = has ? lds128(fr + (uint32_t)(q >> 1) * kAChunk + ((unit ^ r) << 4)) : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t a0[4] = {f.x, 0u, f.y, 0u}, a1[4] = {f.z, 0u, f.w, 0u};
         mma_bf16(c[2 * hp], a0, bw[4 * hp], bw[4 * hp + 1]);
         mma_bf16(c[2 * hp + 1], a1, bw[4 * hp + 2], bw[4 * hp + 3]);
@@ -1059,12 +1148,6 @@ struct Consumer {
     route_layer = l;
     return true;
   }
-  __device__ bool wait_gu(int l) {
-    if (gu_layer == l) return true;
-    if (!block_wait(cm.gu(l))) return false;
-    gu_layer = l;
-    return true;
-  }
   __device__ bool wait_attn_group(int l, int gg) {
     if (attn_layer != l) { attn_layer = l; attn_ok = 0; }
     if (attn_ok & (1u << gg)) return true;
@@ -1084,40 +1167,6 @@ struct Consumer {
     __stcg(&p.attn_o[((size_t)l * p.B + b) * p.od + col], v);
     store_hl(p.attn_hl + ((size_t)l * 2 * p.B + b) * p.od + col, (size_t)p.B * p.od, v);
   }
-  // h planes: [layer][active expert][hi, lo][token][I]
-  __device__ __forceinline__ size_t h_plane(int l, int a) const {
-    return ((size_t)l * kMaxActive + a) * 2 * kMaxB * (size_t)p.I;
-  }
-  // As mma_rows, with the A fragments read from an activation stage in shared memory: row
-  // hl * B + b holds plane hl of token b (I bf16, I * 2 bytes apart). A row m = 2 b + hl, so the
-  // lane's rows are plane g & 1 of tokens g / 2 and g / 2 + 4; tokens outside bmask (or >= B)
-  // are zero.
-  __device__ __forceinline__ void mma_rows_sa(const uint8_t* st, const Geo& g, int rg, int ks, const uint8_t* act,
-                                              uint32_t bmask, float (&c)[4][4]) const {
-    const uint8_t* rowp = b_row(st, g, rg, ks);
-    const int g8 = lane >> 2, tb = g8 >> 1, hl = g8 & 1;
-    const bool ok0 = tb < p.B && ((bmask >> tb) & 1u);
-    const bool ok1 = NB > 4 && tb + 4 < p.B && ((bmask >> (tb + 4)) & 1u);
-    const size_t rb = (size_t)p.I * 2;
-    const uint8_t* a0p = act + (ok0 ? hl * p.B + tb : 0) * rb + ks * 512 + (lane & 3) * 16;
-    const uint8_t* a1p = act + (ok1 ? hl * p.B + tb + 4 : 0) * rb + ks * 512 + (lane & 3) * 16;
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      uint4 w0, w1, u0, u1, v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-      ld_pair(rowp, jj, w0, w1);
-      ld_pair(a0p, jj, u0, u1);
-      if (!ok0) u0 = u1 = v0;
-      if constexpr (NB > 4) {
-        ld_pair(a1p, jj, v0, v1);
-        if (!ok1) v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
-      }
-      { const uint32_t a[4] = {u0.x, v0.x, u0.y, v0.y}; mma_bf16(c[0], a, w0.x, w0.y); }
-      { const uint32_t a[4] = {u0.z, v0.z, u0.w, v0.w}; mma_bf16(c[1], a, w0.z, w0.w); }
-      { const uint32_t a[4] = {u1.x, v1.x, u1.y, v1.y}; mma_bf16(c[2], a, w1.x, w1.y); }
-      { const uint32_t a[4] = {u1.z, v1.z, u1.w, v1.w}; mma_bf16(c[3], a, w1.z, w1.w); }
-    }
-  }
-
   // A fragments from hi/lo bf16 planes (no conversion): token b's row of this warp's slice in
   // plane hl starts at element base + hl * plane + b * row (16-byte aligned); tokens outside
   // bmask are zero. One 16-byte load per 32-column group (the column map above).
@@ -1333,39 +1382,138 @@ struct Consumer {
     if (ok) release_counter(cm.qkv(l, t.c));
   }
 
+  // ---------------------------------------------------------------- expert GEMVs on tcgen05
+  // Warp 0 runs them: lane 0 issues the products (A: tokens x {hi, lo} from shared memory, 8 rows
+  // per group with the descriptor's group stride 0; B: the stage's kTcN weight rows; D: fp32 in
+  // tensor memory) and frees each ring slot by a commit when its products complete; the warp
+  // then reads the accumulators for the epilogue. The other warps step their ring position over
+  // the task's stages and wait for warp 0 at the block barrier that ends the task: ring waits
+  // test a phase's parity, so a warp must never wait on a slot more than one ring cycle ahead
+  // of the stages that are actually in it.
+
+
+  // free ring stage `it` once the products issued so far have read it (lane 0)
+  __device__ void tc_free(uint32_t it) {
+    const uint32_t bar = r.empty + 8 * (it % kStages);
+    tc_commit(bar);
+    mbar_arrive_n(bar, kConsumerWarps - 1);
+  }
+
+
+
+  // The products of one unit: nst ring stages, each issued by lane 0 as soon as it lands (kTcK
+  // columns: 4 k-steps of 16, for each group of 4 tokens), then every product completed. A of
+  // stage st is at a_base + st * a_stride; accumulation restarts at the unit's first product
+  // unless `accumulate` (down: the next expert of the same partial). The warp's ring position
+  // moves past the stages.
+  __device__ bool tc_products(int nst, uint32_t a_base, uint32_t a_stride, bool accumulate, bool last) {
+    constexpr uint32_t idesc = tc_idesc(64, kTcN);
+    int done = 1;
+    if (lane == 0) {
+#pragma unroll 1
+      for (int st = 0; st < nst; ++st) {
+        const uint32_t it = r.it + st;
+        if (!mbar_wait_spin(p, r.full + 8 * (it % kStages), (it / kStages) & 1u)) {
+          done = 0;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t wb = r.data + (it % kStages) * kStageBytes;
+        const uint32_t ab = a_base == 0 ? wb + kStagePayload : a_base + st * a_stride;  // 0: A rides in the stage
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int q = 0; q < kAGroups; ++q)
+            tc_mma(tmem + q * kTcN, tc_sdesc(ab + q * 1024 + k * 32, 0), tc_sdesc(wb + k * 32, 1024), idesc,
+                   accumulate || st != 0 || k != 0);
+        tc_free(it);
+      }
+      if (done && last) {
+        tc_commit(smem_addr(&m.tc_acc));
+        done = mbar_wait_spin(p, smem_addr(&m.tc_acc), tc_phase);
+      }
+    }
+    done = __shfl_sync(0xffffffffu, done, 0);
+    r.it += nst;
+    if (last) tc_phase ^= 1u;
+    tc_fence_after();
+    if (!done) ok = false;
+    return done != 0;
+  }
+
   __device__ void op_gu(const Task& t) {
     const int l = t.layer;
     if (!load_route(l)) return;
     t_ready = gtimer();
-    const int na = m.rc_n, maxa = max_active(p);
-    const Geo g = geo_of(p.H);
-    // a stage holds gate rows [tile RS/2, +RS/2) of active expert a, then the matching up rows;
-    // the epilogue stores SiLU(gate) * up * routing weight
-    auto epi = [&](uint32_t pid, int a, int tile) {
-      const uint32_t bm = m.rc_mask[a];
-      run_epi(pid, g, [&](auto&& R) {
-        const int half = g.RS / 2;
-        for (int i = lane; i < half * NB; i += 32) {
-          const int j = i / NB, b = i % NB;
-          if (!(bm & (1u << b))) continue;
-          const float gt = R(j, b), up = R(half + j, b);
-          store_hl(p.h + h_plane(l, a) + (size_t)b * p.I + tile * half + j, (size_t)kMaxB * p.I,
-                   gt / (1.0f + expf(-gt)) * up * m.rc_w[a][b]);
-        }
-      });
-    };
-    uint32_t prev = 0;
-    int pa = -1, ptile = 0;
-    for (int u = t.a; u < t.a + t.b && ok; ++u) {
-      const int a = u % maxa, tile = u / maxa;
+    const int na = m.rc_n, maxa = max_active(p), nst = p.H / kTcK;
+    const size_t slot_bytes = hsw_slot_bytes(p.I);
+#pragma unroll 1
+    for (int u = t.a; u < t.a + t.b; ++u) {
+      const int a = u % maxa, j = u / maxa;
       if (a >= na) continue;
-      const uint32_t pid = norm_pass(g);
-      if (!ok) return;
-      if (pa >= 0) epi(prev, pa, ptile);
-      prev = pid, pa = a, ptile = tile;
+      // warp 0 runs the unit's products; the others step over its stages. D[group q], kTcN columns
+      // at q kTcN: the unit's gate rows then its up rows, against the normalized input (A chunk st
+      // of the shared A operand)
+      if (warp == 0) tc_products(nst, abuf, kAChunk, false, true);
+      else r.it += nst;
+      tc_fence_before();
+      if (!csync() || !ok) return;
+      tc_fence_after();
+      // epilogue, warps 0-3: the descriptor's group stride 0 repeats the 8 token rows in every
+      // 16-lane group of D, so warp w reads them from its own lane quarter (tensor-memory lanes
+      // 32 w + r) and takes gate/up columns [32 w, 32 w + 32)
+      if (warp < 4) {
+        uint8_t* hs = p.hsw + ((size_t)l * kMaxActive + a) * slot_bytes;
+        const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll 1
+        for (int q = 0; q < kAGroups; ++q) {
+          const int rr = lane & 7, tok = 4 * q + (rr >> 1), hl = rr & 1;
+          const float wgt = (lane < 8 && tok < p.B) ? m.rc_w[a][tok] : 0.f;
+#pragma unroll 1
+          for (int i0 = 32 * warp; i0 < 32 * warp + 32; i0 += 16) {
+            uint32_t gv_[16], uv[16];
+            tc_ld16(tq + q * kTcN + i0, gv_);
+            tc_ld16(tq + q * kTcN + kGuRows + i0, uv);
+            // hi + lo of each gate and up value (lanes 2 t and 2 t + 1 hold the two parts of token
+            // t); lanes past the 8 token rows hold tensor-memory words no product wrote
+            float gs[16], us[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              gs[c] = lane < 8 ? __uint_as_float(gv_[c]) : 0.f;
+              us[c] = lane < 8 ? __uint_as_float(uv[c]) : 0.f;
+              gs[c] += __shfl_xor_sync(0xffffffffu, gs[c], 1);
+              us[c] += __shfl_xor_sync(0xffffffffu, us[c], 1);
+            }
+            if (lane < 8 && tok < p.B) {
+              uint32_t packed[8];
+#pragma unroll
+              for (int c = 0; c < 16; c += 2) {
+                float hv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e)  // SiLU(g) = g / (1 + e^-g), times up and the routing weight
+                  hv[e] = __fdividef(gs[c + e], 1.0f + __expf(-gs[c + e])) * us[c + e] * wgt;
+                uint32_t hi, lo;
+                split_pack(hv[0], hv[1], hi, lo);
+                packed[c / 2] = hl ? lo : hi;
+              }
+              // columns kc = j kGuRows + i0 + 0..15: chunk kc / 64, 16-byte units (kc % 64) / 8 + 0..1
+              const int kc = j * kGuRows + i0;
+              uint8_t* rowp = hs + (size_t)(kc >> 6) * kAChunk + q * 1024 + rr * 128;
+#pragma unroll
+              for (int m4 = 0; m4 < 2; ++m4) {
+                const int u16 = ((kc & 63) >> 3) + m4;
+                __stcg(reinterpret_cast<uint4*>(rowp + ((u16 ^ rr) << 4)),
+                       make_uint4(packed[4 * m4], packed[4 * m4 + 1], packed[4 * m4 + 2], packed[4 * m4 + 3]));
+              }
+            }
+          }
+        }
+        tc_fence_before();
+      }
+      // the accumulators are read before the next unit's products overwrite them
+      if (!csync()) return;
     }
-    if (pa >= 0) epi(prev, pa, ptile);
-    if (ok) release_counter(cm.gu(l));
+    release_counter(cm.gu(l));
   }
 
   __device__ void op_o(const Task& t) {
@@ -1429,41 +1577,56 @@ struct Consumer {
 
   __device__ void op_down(const Task& t) {
     const int l = t.layer;
-    if (!load_route(l) || !wait_gu(l)) return;
+    if (!load_route(l)) return;
     t_ready = gtimer();
-    const Geo g = geo_of(p.I);
-    const int rg = warp / g.KW, ks = warp % g.KW;
-    const bool active = rg < g.RG;
-    const int na = m.rc_n;
-    auto epi = [&](uint32_t pid, int r0, int rows) {
-      run_epi(pid, g, [&](auto&& R) {
-        for (int i = lane; i < rows * NB; i += 32) {
-          const int rr = i / NB, b = i % NB;
-          if (b < p.B) __stcg(&p.moe_out[((size_t)l * p.B + b) * p.H + r0 + rr], R(rr, b));
-        }
-      });
-    };
-    uint32_t prev = 0;
-    int pr0 = -1, prows = 0;
-    for (int r0 = t.a; r0 < t.a + t.b; r0 += g.RS) {  // passes of RS rows
-      const int rows = min(g.RS, t.a + t.b - r0);
-      float c[4][4] = {};
-      // per routed expert: its weight stage, then its activation stage (both held at once)
-      for (int a = 0; a < na; ++a) {
-        const uint8_t* sw = acquire();
-        const uint8_t* sa = sw ? acquire_at(1) : nullptr;
-        if (!sa) return;
-        if (active)
-          mma_rows_sa(sw, g, rg, ks, sa, m.rc_mask[a], c);
-        release();
-        release();
+    const int na = m.rc_n, parts = p.moe_parts, nst = p.I / kTcK;
+#pragma unroll 1
+    for (int u = t.a; u < t.a + t.b; ++u) {
+      const int rb = u / parts, part = u % parts;
+      // partial `part` of output rows [kTcN rb, +kTcN): the routed experts of rank part, part +
+      // parts, ..., accumulated in rank order; stage st carries the expert's kTcN weight rows'
+      // columns [64 st, +64) (B) and, after them in the slot, its activations of those columns (A)
+      int ne = 0;
+      for (int a = part; a < na; a += parts) ++ne;
+      if (warp == 0) {
+        int i = 0;
+        for (int a = part; a < na && ok; a += parts, ++i) tc_products(nst, 0, 0, i > 0, i + 1 == ne);
+      } else {
+        r.it += ne * nst;
       }
-      const uint32_t pid = post_pass(active, c);
-      if (pr0 >= 0) epi(prev, pr0, prows);
-      prev = pid, pr0 = r0, prows = rows;
+      tc_fence_before();
+      if (!csync() || !ok) return;
+      tc_fence_after();
+      // epilogue, warps 0-3 (each from its own tensor-memory lane quarter, see op_gu): output
+      // columns [64 w, 64 w + 64), zero when no routed expert falls in this partial
+      if (warp < 4) {
+        const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+        const int rr = lane & 7, hl = rr & 1;
+#pragma unroll 1
+        for (int q = 0; q < kAGroups; ++q) {
+          const int tok = 4 * q + (rr >> 1);
+          float* dst = p.moe_part + (((size_t)l * kMoeParts + part) * p.B + tok) * p.H + rb * kTcN;
+#pragma unroll 1
+          for (int i0 = 64 * warp; i0 < 64 * warp + 64; i0 += 16) {
+            uint32_t v[16];
+            if (ne > 0) tc_ld16(tq + q * kTcN + i0, v);
+            float o[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              float x = (ne == 0 || lane >= 8) ? 0.f : __uint_as_float(v[c]);
+              x += __shfl_xor_sync(0xffffffffu, x, 1);  // hi + lo
+              o[c] = x;
+            }
+            if (lane < 8 && hl == 0 && tok < p.B)
+#pragma unroll
+              for (int c = 0; c < 16; c += 4)
+                __stcg(reinterpret_cast<float4*>(dst + i0 + c), make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]));
+          }
+        }
+        tc_fence_before();
+      }
     }
-    if (pr0 >= 0) epi(prev, pr0, prows);
-    if (ok) release_counter(cm.layer(l));
+    release_counter(cm.layer(l));
   }
 
   __device__ void op_lm(const Task& t) {
@@ -1868,18 +2031,25 @@ struct Consumer {
 
 // ------------------------------------------------------------------ kernel
 
+
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_constant__ Params p,
                                                                 const __grid_constant__ TensorMaps tm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Misc& misc = *reinterpret_cast<Misc*>(base + kStages * kStageBytes);
+  Misc& misc = *reinterpret_cast<Misc*>(base + kStages * kStageBytes + kABufBytes);
+  if (threadIdx.x < 32) {  // warp 0 takes the block's tensor memory (one block per SM, so it is free)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&misc.tmem_base)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&misc.full[s]), 1);
       mbar_init(smem_addr(&misc.empty[s]), kConsumerWarps);
     }
     mbar_init(smem_addr(&misc.cbar), kConsumerWarps);
+    mbar_init(smem_addr(&misc.tc_acc), 1);
     for (int i = 0; i < kRedBufs; ++i) {
       mbar_init(smem_addr(&misc.gpart[i]), kConsumerWarps);
       mbar_init(smem_addr(&misc.gfree[i]), 1);
@@ -1887,7 +2057,9 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   Ring ring;
   ring.data = smem_addr(base);
   ring.full = smem_addr(&misc.full[0]);
@@ -1918,25 +2090,42 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-  Consumer<NB> c(p, misc, ring);
-  if (!c.load_step_cache()) return;
-  // descriptors in batches of 32 (lane j holds descriptor base + j), the next batch loaded
-  // while the current one runs; each task is broadcast from its lane
-  const uint4* src = reinterpret_cast<const uint4*>(p.tasks);
-  const int lane = threadIdx.x & 31;
-  uint4 cur = t0 + lane < t1 ? __ldg(src + t0 + lane) : make_uint4(0, 0, 0, 0);
-  for (int base = t0; base < t1 && c.ok; base += 32) {
-    const uint4 nxt = base + 32 + lane < t1 ? __ldg(src + base + 32 + lane) : make_uint4(0, 0, 0, 0);
-    const int n = min(32, t1 - base);
-    for (int j = 0; j < n && c.ok; ++j) {
-      uint4 v;
-      v.x = __shfl_sync(0xffffffffu, cur.x, j);
-      v.y = __shfl_sync(0xffffffffu, cur.y, j);
-      v.z = __shfl_sync(0xffffffffu, cur.z, j);
-      v.w = __shfl_sync(0xffffffffu, cur.w, j);
-      c.run_task(*reinterpret_cast<const Task*>(&v));
+  Consumer<NB> c(p, misc, ring, smem_addr(base + kStages * kStageBytes));
+  // The task loop, inline in the kernel (a call after setmaxnreg would hand the callee a register
+  // budget of its own): descriptors in batches of 32, lane j holding descriptor base + j, the next
+  // batch loaded while the current one runs; each task broadcast from its lane.
+  if (c.load_step_cache()) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.tasks);
+    const int lane = threadIdx.x & 31;
+    uint4 cur = t0 + lane < t1 ? __ldg(src + t0 + lane) : make_uint4(0, 0, 0, 0);
+    for (int tb = t0; tb < t1 && c.ok; tb += 32) {
+      const uint4 nxt = tb + 32 + lane < t1 ? __ldg(src + tb + 32 + lane) : make_uint4(0, 0, 0, 0);
+      const int n = min(32, t1 - tb);
+      for (int j = 0; j < n && c.ok; ++j) {
+        uint4 v;
+        v.x = __shfl_sync(0xffffffffu, cur.x, j);
+        v.y = __shfl_sync(0xffffffffu, cur.y, j);
+        v.z = __shfl_sync(0xffffffffu, cur.z, j);
+        v.w = __shfl_sync(0xffffffffu, cur.w, j);
+        c.run_task(*reinterpret_cast<const Task*>(&v));
+      }
+      cur = nxt;
     }
-    cur = nxt;
+  }
+  if (threadIdx.x < 32) {
+    // warp 0 issued every tensor-core product of the block: wait (bounded) until they have all
+    // completed, also on an abort path, then give the tensor memory back
+    __syncwarp();
+    if (!c.ok) {
+      if (threadIdx.x == 0) tc_commit(smem_addr(&misc.tc_acc));
+      __syncwarp();
+      const uint64_t tw0 = gtimer();
+      while (!mbar_try_wait(smem_addr(&misc.tc_acc), c.tc_phase) && gtimer() - tw0 < 1000000000ull) {
+      }
+      __syncwarp();
+    }
+    tc_fence_before();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(misc.tmem_base), "r"(kTmemCols));
   }
 }
 

@@ -62,19 +62,31 @@ def router_ties_ok(ref_logits_row, got_ids, ref_ids, tol=1e-3):
 
 
 def check_step(w, got_logits, got_next, ref_logits, ref_next, acts=None, tr=None, rtol_logits=3e-2):
-    """Acceptance per step: max|dlogit| <= 3e-2 * std(oracle logits) per row; top-k ids equal
-    except oracle-side ties within 1e-3. Returns (argmax agreement count, report dict)."""
-    rep = {}
+    """Acceptance per step, token by token (decode tokens never mix). Top-k ids, layer by layer:
+    equal to the oracle's, except where the oracle's router logits tie within 1e-3. If such a tie
+    made the two sides pick a different expert for token b, everything of b after that layer
+    (its residual stream, the K/V it appends, its logits) differs by design: row b is waived and
+    not compared further. Every other row: max|dlogit| <= 3e-2 * std(oracle logits).
+    acts holds host (numpy) arrays. Returns (argmax agreement over compared rows, report dict:
+    "waived" = list of waived rows, "compared" = number of rows compared)."""
+    waived = []
+    if acts is not None and tr is not None:
+        ids = acts["topk_ids"]
+        for b in range(w.B):
+            for l in range(w.L):
+                if list(ids[l, b]) == list(tr["topk_ids"][l, b]):
+                    continue
+                assert router_ties_ok(tr["router"][l, b], ids[l, b], tr["topk_ids"][l, b]), \
+                    f"layer {l} token {b}: top-k {ids[l, b]} vs oracle {tr['topk_ids'][l, b]}"
+                waived.append(b)
+                break
+    rep = {"waived": waived, "compared": w.B - len(waived)}
     for b in range(w.B):
+        if b in waived:
+            continue
         err = float(np.abs(got_logits[b] - ref_logits[b]).max())
         tol = rtol_logits * float(ref_logits[b].std())
         rep[f"row{b}_err"] = err
         assert err <= tol, f"row {b}: max |dlogit| {err:.3e} > {tol:.3e}"
-    if acts is not None and tr is not None:
-        ids = acts["topk_ids"].cpu().numpy()
-        for l in range(w.L):
-            for b in range(w.B):
-                assert router_ties_ok(tr["router"][l, b], ids[l, b], tr["topk_ids"][l, b]), \
-                    f"layer {l} token {b}: top-k {ids[l, b]} vs oracle {tr['topk_ids'][l, b]}"
-    agree = int(np.sum(got_next == ref_next))
+    agree = int(sum(got_next[b] == ref_next[b] for b in range(w.B) if b not in waived))
     return agree, rep

@@ -38,7 +38,8 @@ def test_wait_limit_runs_out_then_context_recovers():
         s.dc.set_wait_limit(2_000_000_000)
         got_logits, got_next = s.gpu_step(tokens, s.ctx)
         ref_logits, ref_next, tr = s.oracle_step(tokens, s.ctx)
-        agree, _ = check_step(w, got_logits, got_next, ref_logits, ref_next, s.dc.activations(), tr)
+        acts = {k: v.cpu().numpy() for k, v in s.dc.activations().items()}
+        agree, _ = check_step(w, got_logits, got_next, ref_logits, ref_next, acts, tr)
         assert agree == w.B
     finally:
         s.close()

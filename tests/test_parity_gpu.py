@@ -24,7 +24,7 @@ def _bits(t):
 def _run(w, steps, per_layer=False, mode=0):
     s = Setup(w, steps, mode=mode)
     tokens = W.first_tokens(w)
-    agree = total = 0
+    agree = total = waived = 0
     try:
         for i in range(steps):
             pos = s.ctx + i
@@ -35,11 +35,17 @@ def _run(w, steps, per_layer=False, mode=0):
             V_before = {pg: _bits(s.V[:, pg]) for pg in sample_pages}
             got_logits, got_next = s.gpu_step(tokens, pos)
             ref_logits, ref_next, tr = s.oracle_step(tokens, pos)
-            acts = s.dc.activations()
-            a, _ = check_step(w, got_logits, got_next, ref_logits, ref_next, acts, tr)
+            # host copies at once: no device view of the library's workspace outlives the step
+            acts = {k: v.cpu().numpy() for k, v in s.dc.activations().items()}
+            a, rep = check_step(w, got_logits, got_next, ref_logits, ref_next, acts, tr)
             agree += a
-            total += w.B
-            if per_layer:
+            total += rep["compared"]
+            waived += len(rep["waived"])
+            if rep["waived"]:
+                # a router tie changed those tokens' residual streams after the flipped layer, hence
+                # the K/V they appended there: continue from the oracle's appended values
+                _resync_new_slots(s, w, pos, tr, rep["waived"])
+            elif per_layer:
                 _check_layers(w, acts, tr, pos)
             # the appended K/V sit at (block_table[b][pos / 16], pos % 16): the rest of those
             # pages, and a sample of other pages, are unchanged (bit-exact indexing); the values
@@ -58,6 +64,8 @@ def _run(w, steps, per_layer=False, mode=0):
             # head, as in _check_layers) on top of one bf16 rounding of the value itself.
             kv_abs = 2e-4
             for b in range(w.B):
+                if b in rep["waived"]:
+                    continue
                 pg, sl = s.bt[b, pos[b] // w.page], pos[b] % w.page
                 for kv, got, ref in (("K", _bits(s.K[:, pg, :, sl]), tr["k_new"][:, b]),
                                      ("V", _bits(s.V[:, pg, :, sl]), tr["v_new"][:, b])):
@@ -76,26 +84,38 @@ def _run(w, steps, per_layer=False, mode=0):
             tokens = ref_next  # teacher forcing
     finally:
         s.close()
-    assert agree >= 0.99 * total, f"greedy agreement {agree}/{total}"
+    # a router tie within 1e-3 may pick a different expert on the two sides (allowed); the rows
+    # where that happened are not compared on logits, and they must stay a minority
+    assert waived <= max(1, (steps * w.B) // 4), f"{waived} of {steps * w.B} rows changed expert on a router tie"
+    assert total > 0 and agree >= 0.99 * total, f"greedy agreement {agree}/{total}"
+
+
+def _resync_new_slots(s, w, pos, tr, rows):
+    """Writes the oracle's appended K/V of this step (bf16 bits) for the given rows into the
+    GPU's pools."""
+    import torch
+
+    for b in rows:
+        pg, sl = int(s.bt[b, pos[b] // w.page]), int(pos[b] % w.page)
+        for pool, key in ((s.K, "k_new"), (s.V, "v_new")):
+            vals = torch.as_tensor(tr[key][:, b].astype(np.int16), device=pool.device).view(torch.bfloat16)
+            pool[:, pg, :, sl] = vals
 
 
 def _check_layers(w, acts, tr, pos):
-    x = acts["x"].cpu().numpy()
     for name, tol in (("x", 2e-4), ("attn_out", 2e-3), ("moe_out", 2e-3)):
-        got = acts[name].cpu().numpy()
+        got = acts[name]
         ref = tr[name]
         scale = np.abs(ref).max()
         err = np.abs(got - ref).max()
         assert err <= tol * max(scale, 1e-6), f"{name}: max err {err:.3e} vs scale {scale:.3e}"
-    q = acts["q"].cpu().numpy().astype(np.float64)  # before RoPE: rotate with the oracle's RoPE
+    q = acts["q"].astype(np.float64)  # before RoPE: rotate with the oracle's RoPE
     for l in range(w.L):
         for b in range(w.B):
             for h in range(w.nq):
                 q[l, b, h] = oracle.rope(q[l, b, h], int(pos[b]), w.rope_theta)
     np.testing.assert_allclose(q, tr["q"], rtol=0, atol=2e-4 * np.abs(tr["q"]).max())
-    att = acts["attn"].cpu().numpy()
-    np.testing.assert_allclose(att, tr["attn"], rtol=0, atol=2e-3 * np.abs(tr["attn"]).max())
-    del x
+    np.testing.assert_allclose(acts["attn"], tr["attn"], rtol=0, atol=2e-3 * np.abs(tr["attn"]).max())
 
 
 def test_tiny_one_step_all_layers():

@@ -56,22 +56,18 @@ def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
                 assert ch == list(range(len(ch))) and len(ch) >= 1
                 assert n is None or n == len(ch)
                 n = len(ch)
+        # gate/up: tensor-core units of 128 gate rows (and their up rows) per routed expert
         g = t[t["op"] == OP_GU]
-        assert sorted(_ranges(g).tolist()) == list(range(maxa * (w.I // (rows_per_stage(w.H) // 2))))
+        assert sorted(_ranges(g).tolist()) == list(range(maxa * (w.I // 128)))
         o = t[t["op"] == OP_O]
         rs_o = rows_per_stage(w.nq * w.d)  # O tasks: whole row blocks (the last may be short)
         assert sorted(_ranges(o).tolist()) == list(range(w.H))
         assert np.all((o["b"] % rs_o == 0) | (o["a"] + o["b"] == w.H))
+        # down: one task per (256-row block, partial) unit; a partial takes the experts of rank
+        # j, j + parts, ..., so every unit of a layer has the same share of the routed experts
         dn = t[t["op"] == OP_DOWN]
-        assert sorted(_ranges(dn).tolist()) == list(range(w.H))
-        # down: blocks of one stage's rows, or (when those outnumber the expert SMs) one task per
-        # expert SM made of 8-row blocks, so no expert SM takes two down tasks
-        n_moe = n_sm - info.n_attn_sm if info.n_attn_sm < n_sm else n_sm
-        rs_d = rows_per_stage(w.I)
-        if -(-w.H // rs_d) <= n_moe:
-            assert np.all(dn["b"] <= rs_d)
-        else:
-            assert len(dn) <= n_moe and np.all((dn["b"] % 8 == 0) | (dn["a"] + dn["b"] == w.H))
+        parts = min(8, maxa)
+        assert sorted(_ranges(dn).tolist()) == list(range((w.H // 256) * parts)) and np.all(dn["b"] == 1)
     lm = tasks[tasks["op"] == OP_LM]
     assert sorted(_ranges(lm).tolist()) == list(range(w.V))
     assert np.all(lm["flags"] & 2) and len(lm) == info.n_lm_sm and sorted(lm["c"].tolist()) == list(range(len(lm)))
