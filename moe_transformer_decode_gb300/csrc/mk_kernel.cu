@@ -1695,19 +1695,22 @@ struct Consumer {
   // group are the 16 rows of an mma A operand: rows 0..7 hold the bf16 "hi" part of q and rows
   // 8..15 its rounding residual, so S = q K^T comes out at ~fp32 accuracy; P is split the same
   // way for P V. K/V tiles arrive 128B-swizzled from the tensor maps (conflict-free ldmatrix).
-  __device__ void op_attn(const Task& t) {
+  // One attention chunk; KS = head_dim / 16 (mma k-steps over the head dim: 8 at d = 128, 4 at
+  // d = 64) is a template parameter so that every loop and register index below is static.
+  template <int KS>
+  __device__ void attn_chunk(const Task& t) {
+    constexpr int halves = KS / 4, pps = kStagePayload / (4096 * halves);
     const int l = t.layer, b = t.a, g = t.b;
     if (!block_wait(cm.qkv(l, g))) return;
     t_ready = gtimer();
     const AttnRange ar = attn_range(m.st_pos[b], m.st_cpp[b], m.st_nch[b], t.c);
     // warp (pi, sp) takes page pi of every stage s with s % npar == sp, over the whole head dim
     // (2 stage parities at d = 128, 1 at d = 64), so no two warps compute the same scores
-    const int pps = attn_pps(p), halves = p.d / 64, ksteps = p.d / 16;
-    const int npar = kConsumerWarps / pps;
+    constexpr int npar = kConsumerWarps / pps;
     const int pi = warp % pps, sp = warp / pps;
     const int head = lane >> 2, tig = lane & 3;
     const float qscale = rsqrtf((float)p.d) * 1.4426950408889634f;  // scores in log2 units
-    uint32_t qa[8][4];
+    uint32_t qa[KS][4];
     {
       // the group's q (group x d floats, contiguous) into shared memory once per block, one
       // float4 per thread, rows padded by 4 floats; the partial-sum buffers are free here (the
@@ -1725,40 +1728,35 @@ struct Consumer {
       // kk + ksteps/2), so the rotation happens here in registers
       const float* qh = qs + head * qst;
       const bool hv = head < p.group;
-      float x[8][4];
+      float x[KS][4];
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < KS; ++kk) {
         const int d0 = kk * 16 + tig * 2;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[kk][e] = (kk < ksteps && hv) ? qh[d0 + (e & 1) + (e >> 1) * 8] : 0.f;
+        for (int e = 0; e < 4; ++e) x[kk][e] = hv ? qh[d0 + (e & 1) + (e >> 1) * 8] : 0.f;
       }
-      const int half = ksteps / 2, hd = p.d / 2;
+      constexpr int half = KS / 2;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        if (kk < half) {
+      for (int kk = 0; kk < half; ++kk) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int d0 = kk * 16 + tig * 2 + (e & 1) + (e >> 1) * 8;  // < d/2
-            const float2 cs = m.st_rope[b][d0];
-            const float lo = x[kk][e], hi = x[kk + half][e];
-            x[kk][e] = lo * cs.x - hi * cs.y;
-            x[kk + half][e] = lo * cs.y + hi * cs.x;
-          }
+        for (int e = 0; e < 4; ++e) {
+          const int d0 = kk * 16 + tig * 2 + (e & 1) + (e >> 1) * 8;  // < d/2
+          const float2 cs = m.st_rope[b][d0];
+          const float lo = x[kk][e], hi = x[kk + half][e];
+          x[kk][e] = lo * cs.x - hi * cs.y;
+          x[kk + half][e] = lo * cs.y + hi * cs.x;
         }
       }
-      (void)hd;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        if (kk < ksteps) {
-          split_pack(x[kk][0] * qscale, x[kk][1] * qscale, qa[kk][0], qa[kk][1]);
-          split_pack(x[kk][2] * qscale, x[kk][3] * qscale, qa[kk][2], qa[kk][3]);
-        }
+      for (int kk = 0; kk < KS; ++kk) {
+        split_pack(x[kk][0] * qscale, x[kk][1] * qscale, qa[kk][0], qa[kk][1]);
+        split_pack(x[kk][2] * qscale, x[kk][3] * qscale, qa[kk][2], qa[kk][3]);
       }
     }
     float mrun = -INFINITY, lsum = 0.f;
-    float oacc[16][4];
+    float oacc[2 * KS][4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < 2 * KS; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) oacc[i][j] = 0.f;
 
@@ -1795,16 +1793,14 @@ struct Consumer {
           for (int j = 0; j < 4; ++j) sc[i][j] = 0.f;
         const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          if (kk < ksteps) {
-            const int prow = (mi >> 1) * 8 + rr;           // position within the page
-            const int chunk = 2 * kk + (mi & 1);          // 16-byte chunk of the head dim
-            const uint32_t addr = kt + (chunk >> 3) * 2048 + prow * 128 + (((chunk & 7) ^ (prow & 7)) << 4);
-            uint32_t bk[4];
-            ldsm_x4(addr, bk);
-            mma_bf16(sc[0], qa[kk], bk[0], bk[1]);
-            mma_bf16(sc[1], qa[kk], bk[2], bk[3]);
-          }
+        for (int kk = 0; kk < KS; ++kk) {
+          const int prow = (mi >> 1) * 8 + rr;           // position within the page
+          const int chunk = 2 * kk + (mi & 1);          // 16-byte chunk of the head dim
+          const uint32_t addr = kt + (chunk >> 3) * 2048 + prow * 128 + (((chunk & 7) ^ (prow & 7)) << 4);
+          uint32_t bk[4];
+          ldsm_x4(addr, bk);
+          mma_bf16(sc[0], qa[kk], bk[0], bk[1]);
+          mma_bf16(sc[1], qa[kk], bk[2], bk[3]);
         }
         float sv[2][2];
         float mx = -INFINITY;
@@ -1824,7 +1820,7 @@ struct Consumer {
           const float alpha = exp2f(mrun - mnew);
           lsum *= alpha;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
+          for (int i = 0; i < 2 * KS; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) oacc[i][j] *= alpha;
           mrun = mnew;
@@ -1840,8 +1836,7 @@ struct Consumer {
           split_pack(pr[0][0], pr[0][1], pa[0], pa[1]);
           split_pack(pr[1][0], pr[1][1], pa[2], pa[3]);
 #pragma unroll
-          for (int c2 = 0; c2 < 8; ++c2) {  // two 8-wide d tiles per ldmatrix.x4.trans
-            if (c2 >= ksteps) break;
+          for (int c2 = 0; c2 < KS; ++c2) {  // two 8-wide d tiles per ldmatrix.x4.trans
             const int chunk = c2 * 2 + (mi >> 1);
             const int prow = (mi & 1) * 8 + rr;
             const uint32_t addr = vt + (chunk >> 3) * 2048 + prow * 128 + (((chunk & 7) ^ (prow & 7)) << 4);
@@ -1866,8 +1861,7 @@ struct Consumer {
       // per warp: m[8], l[8], O[8][64] of this round's dims
       float* mine = scr + warp * (16 + 8 * 64);
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        if (r >= halves) break;
+      for (int r = 0; r < halves; ++r) {
         if (!csync()) return;
         if (tig == 0) { mine[head] = mrun; mine[8 + head] = lsum; }
 #pragma unroll
@@ -2019,7 +2013,10 @@ struct Consumer {
     switch (t.op) {
       case OP_ROUTER: op_router(t); break;
       case OP_QKV: op_qkv(t); break;
-      case OP_ATTN: op_attn(t); break;
+      case OP_ATTN:
+        if (p.d == 128) attn_chunk<8>(t);
+        else attn_chunk<4>(t);
+        break;
       case OP_GU: op_gu(t); break;
       case OP_O: op_o(t); break;
       case OP_DOWN: op_down(t); break;
