@@ -762,6 +762,22 @@ struct Consumer {
     if (lane == 0) mbar_arrive(r.empty + 8 * (r.it % kStages));
     ++r.it;
   }
+  // For a warp that takes only some of a task's stages: stage `it` explicitly, and `n` of the
+  // slot's kConsumerWarps arrivals at once. The ring position is moved past the task by the caller.
+  // Parity waits stay exact as long as every slot a warp waits on is one whose previous stage it
+  // also waited on (or that was consumed before a block barrier the warp passed).
+  __device__ const uint8_t* acquire_at(uint32_t it) {
+    const uint32_t s = it % kStages, parity = (it / kStages) & 1u;
+    if (!mbar_wait(p, r.full + 8 * s, parity)) {
+      ok = false;
+      return nullptr;
+    }
+    return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(r.data + s * kStageBytes));
+  }
+  __device__ void release_at(uint32_t it, uint32_t n) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive_n(r.empty + 8 * (it % kStages), n);
+  }
   __device__ uint32_t bmask_all() const { return (1u << p.B) - 1u; }
 
   // Barrier of the 8 consumer warps on an mbarrier, with the same time limit as every other
@@ -1760,13 +1776,18 @@ struct Consumer {
 #pragma unroll
       for (int j = 0; j < 4; ++j) oacc[i][j] = 0.f;
 
+    // Warp (pi, sp) waits only on the stages of its parity sp and gives each slot its group's
+    // share of the arrivals. With 4 slots and 2 parities, stages s and s + 4 of one slot have the
+    // same parity, so each slot is waited on by one group of warps only (and the block barrier of
+    // the q load precedes the loop), which keeps every parity wait exact.
+    static_assert(kStages % npar == 0, "a ring slot must serve stages of one parity");
     const int nst = (ar.cp1 - ar.cp0 + pps - 1) / pps;
-    uint32_t last_slot = 0;
-    for (int s = 0; s < nst; ++s) {
-      const uint8_t* st = acquire();
+    const uint32_t it0 = r.it;
+    for (int s = sp; s < nst; s += npar) {
+      const uint8_t* st = acquire_at(it0 + s);
       if (!st) return;
       const int page = ar.cp0 + s * pps + pi;
-      if (s % npar == sp && page < ar.cp1) {
+      if (page < ar.cp1) {
         const uint32_t kt = smem_addr(st) + (uint32_t)pi * 4096 * halves;
         const uint32_t vt = kt + (uint32_t)halves * 2048;
         // Rows of the sequence's last page at or past the new token's position are masked out of
@@ -1847,53 +1868,52 @@ struct Consumer {
           }
         }
       }
-      if (s + 1 < nst) release();
-      else last_slot = smem_addr(st);
+      release_at(it0 + s, npar);
     }
+    r.it = it0 + nst;
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
 
-    // merge the 8 warps (disjoint pages) in rounds of 64 head dims, using the last slot as scratch
+    // merge the 8 warps (disjoint pages) in one round through the A buffer: within a layer no
+    // task after attention reads the normalized input (down carries its activations in the ring,
+    // O-proj reads the attention output), and the next task that needs it rebuilds it
     const size_t pidx = (((size_t)l * p.B + b) * p.nkv + g) * p.max_chunks + t.c;
     float* part = p.apart + pidx * (16 + 8 * (size_t)p.d);
     if (nst > 0) {
-      float* scr = reinterpret_cast<float*>(__cvta_shared_to_generic(last_slot));
-      // per warp: m[8], l[8], O[8][64] of this round's dims
-      float* mine = scr + warp * (16 + 8 * 64);
+      constexpr int d = 16 * KS, q4 = d / 4, kW = 16 + 8 * d;  // per warp: m[8], l[8], O[8][d]
+      static_assert(kConsumerWarps * kW * 4 <= kABufBytes, "merge scratch exceeds the A buffer");
+      float* scr = reinterpret_cast<float*>(__cvta_shared_to_generic(abuf));
+      float* mine = scr + warp * kW;
+      // (the q load's block barriers put every earlier reader of the buffer behind this point)
+      if (tig == 0) { mine[head] = mrun; mine[8 + head] = lsum; }
 #pragma unroll
-      for (int r = 0; r < halves; ++r) {
-        if (!csync()) return;
-        if (tig == 0) { mine[head] = mrun; mine[8 + head] = lsum; }
+      for (int nt = 0; nt < 2 * KS; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            mine[16 + head * 64 + nt * 8 + tig * 2 + e] = oacc[8 * r + nt][e] + oacc[8 * r + nt][e + 2];
-        if (!csync()) return;
-        for (int i = threadIdx.x; i < 8 * 64; i += 256) {
-          const int h = i / 64, dl = i % 64;
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, scr[w * (16 + 512) + h]);
-          float L = 0.f, O = 0.f;
-          if (M != -INFINITY)
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              const float* src = scr + w * (16 + 512);
-              if (src[h] == -INFINITY) continue;
-              const float f = exp2f(src[h] - M);
-              L += src[8 + h] * f;
-              O += src[16 + h * 64 + dl] * f;
-            }
-          if (r == 0 && dl == 0) { __stcg(part + h, M); __stcg(part + 8 + h, L); }
-          __stcg(part + 16 + h * p.d + 64 * r + dl, O);
-        }
-      }
-      // the slot was scratch for generic stores; the producer's next copy into it is an
-      // async-proxy write, ordered after them by this fence (every writer thread) and the release
-      fence_proxy_async_smem();
+        for (int e = 0; e < 2; ++e) mine[16 + head * d + nt * 8 + tig * 2 + e] = oacc[nt][e] + oacc[nt][e + 2];
+      n_layer = -1;
       if (!csync()) return;
-      release();
+      if (threadIdx.x < 8 * q4) {  // head h, dims [dd, dd + 4)
+        const int h = threadIdx.x / q4, dd = 4 * (threadIdx.x % q4);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, scr[w * kW + h]);
+        float L = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY)
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = scr[w * kW + h];
+            const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+            L += scr[w * kW + 8 + h] * f;
+            const float4 v = *reinterpret_cast<const float4*>(scr + w * kW + 16 + h * d + dd);
+            O.x = fmaf(v.x, f, O.x);
+            O.y = fmaf(v.y, f, O.y);
+            O.z = fmaf(v.z, f, O.z);
+            O.w = fmaf(v.w, f, O.w);
+          }
+        if (dd == 0) { __stcg(part + h, M); __stcg(part + 8 + h, L); }
+        __stcg(reinterpret_cast<float4*>(part + 16 + h * d + dd), O);
+      }
     } else {
       for (int i = threadIdx.x; i < 16 + 8 * p.d; i += 256) __stcg(part + i, i < 8 ? -INFINITY : 0.f);
     }
