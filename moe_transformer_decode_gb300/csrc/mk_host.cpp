@@ -79,7 +79,8 @@ struct mk_ctx {
 };
 
 // The expert weights as 3D bf16 views {64, rows, K / 64} (strides: a row, 128 bytes) with 128B
-// swizzle, so that one box lands kGuRows or kTcN rows x 64 columns as the tcgen05 B operand.
+// swizzle: a gate/up box lands kGuRows rows x 64 columns, a down box kDnRows rows x 128 columns
+// as two [rows][128 bytes] chunks, the layout of the tcgen05 B operand.
 mk_status mk::encode_expert_maps(void* encode_fn, const mk_model_cfg& m, const mk_weight_ptrs* w, TensorMaps& tm) {
   EncodeTiledFn enc = (EncodeTiledFn)encode_fn;
   const uint64_t gu_rows = (uint64_t)m.n_layers * m.n_experts * 2 * m.expert_inter;
@@ -98,7 +99,7 @@ mk_status mk::encode_expert_maps(void* encode_fn, const mk_model_cfg& m, const m
   {
     cuuint64_t dims[3] = {64, (cuuint64_t)dn_rows, (cuuint64_t)m.expert_inter / 64};
     cuuint64_t strides[2] = {(cuuint64_t)m.expert_inter * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)kTcN, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)kDnRows, (cuuint32_t)(kStageK / 64)};
     if (enc(&tm.dn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w->w_down), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -460,7 +461,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   }
 
   // expert GEMVs (tcgen05): gate/up units of kGuRows gate rows + the matching up rows over H;
-  // down units of kTcN output rows for one of `parts` partials (experts of rank j mod parts)
+  // down units of kDnRows output rows for one of `parts` partials (experts of rank j mod parts)
   const int tiles = I / kGuRows;
   const int parts = std::min(kMoeParts, maxa);
   // Per layer, gate/up tasks are sized to about two per expert SM and QKV tasks to about two
@@ -549,11 +550,11 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
       per_op.push_back(std::move(lists));
     }
     for (int g = 0; g < nkv; ++g) cnt[cmap.attn(l, g)] = B;
-    // expert down: units u = row block * parts + part (kTcN rows over the routed experts of rank
-    // part, part + parts, ...), one per task
+    // expert down: units u = row block * parts + part (kDnRows rows over the routed experts of
+    // rank part, part + parts, ...), one per task
     int n_down = 0;
-    for (int u = 0; u < (H / kTcN) * parts; ++u, ++n_down)
-      ts.push_back({mkt(OP_DOWN, l, u, 1, 0), (long long)((double)kTcN * I * 2 * live * maxa / parts)});
+    for (int u = 0; u < (H / kDnRows) * parts; ++u, ++n_down)
+      ts.push_back({mkt(OP_DOWN, l, u, 1, 0), (long long)((double)kDnRows * I * 2 * live * maxa / parts)});
     emit(ts, PM);
     // O-proj: blocks of RS rows; at batch <= 4 (and at most two 2048-column chunks) a task takes
     // several blocks, reusing one load of the attention output, about one task per SM

@@ -20,15 +20,17 @@ static_assert(kConsumerWarps == 8, "two consumer warpgroups");
 static_assert(kProducerRegs * 128 + kConsumerRegs * 256 <= (65536 / kThreads) / 8 * 8 * kThreads,
               "register split exceeds the launch's allotment");
 constexpr int kStagePayload = 32768;                 // data bytes of a ring stage
-// ring slot: a stage, plus room for the tcgen05 A chunk (2 KB) an expert-down stage carries
-constexpr int kStageBytes = kStagePayload + 2048;
+// ring slot: a stage, plus room for the tcgen05 A chunks (up to 4 KB) an expert-down stage carries
+constexpr int kStageBytes = kStagePayload + 4096;
 constexpr int kStages = 4;
-// Expert GEMVs on tcgen05 (weights as the N operand, tokens x {hi, lo} as M): a stage is
-// kTcN weight rows x kTcK columns; a gate/up unit is kGuRows gate rows and the matching up rows
-// (N = kTcN); a down unit is kTcN output rows over the experts of one of kMoeParts partials.
-constexpr int kTcN = 256;
+// Expert GEMVs on tcgen05 (weights as the N operand, tokens x {hi, lo} as M). A stage holds
+// kStageK = 128 columns of its weight rows as two 64-column (128-byte, swizzled) chunks. A gate/up
+// unit is kGuRows gate rows and the matching up rows (two N = 64 products per k-step); a down unit
+// is kDnRows output rows (N = 128) over the experts of one of kMoeParts partials.
 constexpr int kTcK = 64;
-constexpr int kGuRows = kTcN / 2;
+constexpr int kStageK = 2 * kTcK;
+constexpr int kGuRows = 64;
+constexpr int kDnRows = 128;
 constexpr int kMoeParts = 8;
 constexpr int kTmemCols = 512;
 // the A operand (tokens x {hi, lo}, 8 rows per group, groups of 4 tokens) for one 64-column
@@ -168,7 +170,7 @@ struct TensorMaps {
   CUtensorMap k, v;
   // expert weights as 3D {64, rows, K / 64} bf16 views with 128B swizzle (the tcgen05 operand
   // layout): gate/up rows [L][E][2I] over K = hidden, box {64, kGuRows, 1}; down rows [L][E][H]
-  // over K = I, box {64, kTcN, 1}
+  // over K = I, box {64, kDnRows, 2}
   CUtensorMap gu, dn;
 };
 // bytes of one expert's activation slot in Params::hsw

@@ -104,9 +104,26 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
+// The same, issued from a converged warp: every lane computes the (warp-uniform) operands and
+// the elected lane (the lowest, lane 0) issues. Keeping the operands warp-uniform lets the
+// compiler hold them where the tensor-core issue reads them; one lane alone under a branch issues
+// about 45 % slower (measured).
+__device__ __forceinline__ void tc_mma_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
 // arrive once on the mbarrier when every tcgen05.mma this thread issued so far has completed
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// the same from a converged warp, by the elected lane (the one that issued the products)
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -243,6 +260,8 @@ struct WaitClock {
   }
 };
 
+constexpr uint32_t kPollSuspendNs = 200;  // suspend limit of the producer's free-slot waits
+
 // single-thread bounded wait; false on timeout or abort
 __device__ bool wait_counter(const Params& p, int idx) {
   const uint32_t tgt = target_of(p, idx);
@@ -285,6 +304,19 @@ __device__ bool mbar_wait_spin(const Params& p, uint32_t bar, uint32_t parity) {
   for (int i = 0;; ++i) {
     if (mbar_test_wait(bar, parity)) return true;
     if ((i & 63) == 63 && !wc.keep_going(p, -1, (int)parity)) return false;
+  }
+}
+
+// Bounded wait with a short suspend limit, for the producer's free-slot waits: a slot of a
+// tensor-core stage is freed by a commit (an asynchronous arrival), which does not wake a warp
+// suspended in try_wait, so the suspension must end by itself soon; the consumers' own arrivals
+// wake it at once.
+__device__ bool mbar_wait_poll(const Params& p, uint32_t bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  WaitClock wc;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kPollSuspendNs)) return true;
+    if (!wc.keep_going(p, -1, (int)parity)) return false;
   }
 }
 
@@ -361,13 +393,15 @@ __device__ __forceinline__ int max_active(const Params& p) { return min(p.B * p.
 // ------------------------------------------------------------------ shared memory
 
 constexpr int kRedBufs = 4;    // GEMV partial-sum buffers in flight
-constexpr int kIdCache = 256;  // page ids the producer keeps (the same pages serve every layer)
+constexpr int kIdCache = 128;  // page ids the producer keeps (the same pages serve every layer)
 
 struct Misc {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t cbar;                     // consumer-warps barrier (8 arrivals per phase)
   uint64_t tc_acc;                   // tcgen05: a unit's products have all completed (commit)
+  uint64_t acc_full[2];              // gate/up: accumulator buffer b holds a unit's finished products
+  uint64_t acc_empty[2];             // gate/up: the epilogue warps have read buffer b
   uint32_t tmem_base;                // tcgen05: the block's tensor memory (kTmemCols columns)
   uint64_t gpart[kRedBufs];          // GEMV pass buffers: every consumer warp's partials are in
   uint64_t gfree[kRedBufs];          // ... and: the pass's epilogue warp has read them
@@ -401,6 +435,9 @@ struct Misc {
   int pr_n;
   int pr_expert[kMaxActive];
   int pr_ids[kIdCache];
+  // expert-down stages whose weight copy is out but whose activation copy waits for gate/up
+  uint32_t pend_dst[kStages], pend_bar[kStages];
+  const uint8_t* pend_src[kStages];
   // per-warp LM argmax candidates per token
   float lmw_v[kConsumerWarps][kMaxB];
   int lmw_i[kConsumerWarps][kMaxB];
@@ -471,7 +508,7 @@ struct Producer {
     dst = r.data + s * kStageBytes;
     int fine = 1;
     if (lane == 0) {
-      fine = mbar_wait(p, r.empty + 8 * s, parity);
+      fine = mbar_wait_poll(p, r.empty + 8 * s, parity);
       if (fine) mbar_expect_tx(bar, bytes);
     }
     fine = __shfl_sync(0xffffffffu, fine, 0);
@@ -579,11 +616,11 @@ struct Producer {
       }
       case OP_GU: {
         // unit u = (row block j = u / maxa, active expert a = u % maxa): kGuRows gate rows and the
-        // matching up rows over the hidden dim, stage s = columns [64 s, 64 s + 64): the gate
-        // rows land as rows 0..kGuRows-1 of the stage, the up rows after them (one 2D-swizzled
-        // [kTcN rows][128 bytes] tile, the tcgen05 B operand)
+        // matching up rows over the hidden dim; stage s = columns [128 s, 128 s + 128) as two
+        // 64-column chunks, each [kGuRows gate rows | kGuRows up rows][128 bytes] (swizzled), the
+        // same B layout as a down stage: four tensor copies, lane 2 c + g for chunk c, gate (0) or up (1)
         if (!route(l)) return false;
-        const int na = m.pr_n, maxa = max_active(p), nst = p.H / kTcK;
+        const int na = m.pr_n, maxa = max_active(p), nst = p.H / kStageK;
 #pragma unroll 1
         for (int u = t.a; u < t.a + t.b; ++u) {
           const int a = u % maxa, j = u / maxa;
@@ -592,8 +629,9 @@ struct Producer {
 #pragma unroll 1
           for (int st = 0; st < nst; ++st) {
             if (!begin(kStagePayload)) return false;
-            if (lane < 2)  // lane 0: the gate rows, lane 1: the up rows (I rows further on)
-              tma_3d_g2s(dst + (uint32_t)lane * (kStagePayload / 2), &tm.gu, 0, grow + lane * p.I, st, bar, pol);
+            if (lane < 4)  // up rows are I rows after their gate rows
+              tma_3d_g2s(dst + (uint32_t)(lane >> 1) * (kStagePayload / 2) + (uint32_t)(lane & 1) * (kGuRows * 128), &tm.gu,
+                         0, grow + (lane & 1) * p.I, 2 * st + (lane >> 1), bar, pol);
             end();
           }
         }
@@ -610,42 +648,66 @@ struct Producer {
         return true;
       }
       case OP_DOWN: {
-        // unit u = (row block rb = u / parts, partial j = u % parts): output rows [kTcN rb, +kTcN)
-        // over the routed experts of rank j, j + parts, ...; per expert I / 64 stages, stage s
-        // holding the kTcN weight rows' columns [64 s, 64 s + 64) and, after them, the expert's
-        // activations of those columns (the A chunk), so no stage outlives its own products
+        // unit u = (row block rb = u / parts, partial j = u % parts): output rows [kDnRows rb, +kDnRows)
+        // over the routed experts of rank j, j + parts, ...; per expert I / kStageK stages, stage s
+        // holding the rows' columns [128 s, 128 s + 128) as two swizzled 64-column chunks and,
+        // after them, the expert's activations of those columns (two A chunks), so no stage
+        // outlives its own products.
+        // The weight copy of a stage goes out as soon as its slot is free, before the layer's
+        // gate/up is complete; the activation copy (other blocks' gate/up output) only after it.
+        // Until then the activation copies wait in a list of at most kStages - 1 stages, so the
+        // slot the next stage needs never holds a stage whose copy is still pending.
         if (!route(l)) return false;
-        const int na = m.pr_n, parts = p.moe_parts, nst = p.I / kTcK;
-        const uint32_t achunk = p.B > 4 ? 2048u : 1024u;
+        const int na = m.pr_n, parts = p.moe_parts, nst = p.I / kStageK;
+        const uint32_t abytes = 2u * (p.B > 4 ? 2048u : 1024u);
+        int npend = 0;
         bool gu_done = false;
+        auto flush = [&]() -> bool {
+          if (!gu_done) {
+            int fine = 1;
+            if (lane == 0) fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.gu(l));
+            if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
+            // p.hsw was written by the gate/up epilogues' generic stores (other SMs) and published
+            // by their release; lane 0's acquire made it visible to the warp, and this fence
+            // orders it before the bulk copies below, which read it through the async proxy
+            __syncwarp();
+            fence_proxy_async_global();
+            gu_done = true;
+          }
+          if (lane == 1)
+            for (int i = 0; i < npend; ++i) bulk_g2s(m.pend_dst[i], m.pend_src[i], abytes, m.pend_bar[i], pol);
+          npend = 0;
+          __syncwarp();
+          return true;
+        };
 #pragma unroll 1
         for (int u = t.a; u < t.a + t.b; ++u) {
           const int rb = u / parts, part = u % parts;
 #pragma unroll 1
           for (int a = part; a < na; a += parts) {
-            if (!gu_done) {
-              int fine = 1;
-              if (lane == 0) fine = wait_counter(p, CounterMap{p.L, p.nkv, p.B}.gu(l));
-              if (!__shfl_sync(0xffffffffu, fine, 0)) return false;
-              // p.hsw was written by the gate/up epilogues' generic stores (other SMs) and published
-              // by their release; lane 0's acquire made it visible to the warp, and this fence orders
-              // it before the bulk copies below, which read it through the async proxy
-              __syncwarp();
-              fence_proxy_async_global();
-              gu_done = true;
-            }
-            const int row = (l * p.E + m.pr_expert[a]) * p.H + rb * kTcN;
+            const int row = (l * p.E + m.pr_expert[a]) * p.H + rb * kDnRows;
             const uint8_t* hs = p.hsw + ((size_t)l * kMaxActive + a) * hsw_slot_bytes(p.I);
 #pragma unroll 1
             for (int st = 0; st < nst; ++st) {
-              if (!begin(kStagePayload + achunk)) return false;
-              if (lane == 0) tma_3d_g2s(dst, &tm.dn, 0, row, st, bar, pol);
-              if (lane == 1) bulk_g2s(dst + kStagePayload, hs + (size_t)st * achunk, achunk, bar, pol);
+              if (!gu_done && npend == kStages - 1 && !flush()) return false;
+              if (!begin(kStagePayload + abytes)) return false;
+              if (lane == 0) tma_3d_g2s(dst, &tm.dn, 0, row, 2 * st, bar, pol);
+              const uint8_t* src = hs + (size_t)st * abytes;
+              if (gu_done) {
+                if (lane == 1) bulk_g2s(dst + kStagePayload, src, abytes, bar, pol);
+              } else {
+                if (lane == 1) {
+                  m.pend_dst[npend] = dst + kStagePayload;
+                  m.pend_bar[npend] = bar;
+                  m.pend_src[npend] = src;
+                }
+                ++npend;
+              }
               end();
             }
           }
         }
-        return true;
+        return npend == 0 || flush();
       }
     }
     return true;
@@ -733,10 +795,11 @@ struct Consumer {
   static constexpr uint32_t kAChunk = (NB > 4 ? 2u : 1u) * 1024u;
   static constexpr int kAGroups = NB > 4 ? 2 : 1;
   uint32_t abuf, tmem, tc_phase;
+  uint32_t gu_units;  // gate/up units run so far (unit n uses accumulator buffer n & 1)
 
   __device__ Consumer(const Params& p_, Misc& m_, Ring r_, uint32_t abuf_)
       : p(p_), m(m_), r(r_), cm{p_.L, p_.nkv, p_.B}, ok(true), n_layer(-1), route_layer(-1),
-        attn_layer(-1), attn_ok(0), abuf(abuf_), tmem(m_.tmem_base), tc_phase(0) {
+        attn_layer(-1), attn_ok(0), abuf(abuf_), tmem(m_.tmem_base), tc_phase(0), gu_units(0) {
     warp = threadIdx.x / 32;
     lane = threadIdx.x % 32;
     cbar = smem_addr(&m_.cbar);
@@ -1400,58 +1463,81 @@ struct Consumer {
 
   // ---------------------------------------------------------------- expert GEMVs on tcgen05
   // Warp 0 runs them: lane 0 issues the products (A: tokens x {hi, lo} from shared memory, 8 rows
-  // per group with the descriptor's group stride 0; B: the stage's kTcN weight rows; D: fp32 in
-  // tensor memory) and frees each ring slot by a commit when its products complete; the warp
+  // per group with the descriptor's group stride 0; B: the stage's weight rows; D: fp32 in
+  // tensor memory, 128 columns per token group) and frees each ring slot by a commit when its products complete; the warp
   // then reads the accumulators for the epilogue. The other warps step their ring position over
   // the task's stages and wait for warp 0 at the block barrier that ends the task: ring waits
   // test a phase's parity, so a warp must never wait on a slot more than one ring cycle ahead
   // of the stages that are actually in it.
 
 
-  // free ring stage `it` once the products issued so far have read it (lane 0)
+  // free ring stage `it` once the products issued so far have read it (warp 0, converged)
   __device__ void tc_free(uint32_t it) {
     const uint32_t bar = r.empty + 8 * (it % kStages);
-    tc_commit(bar);
-    mbar_arrive_n(bar, kConsumerWarps - 1);
+    tc_commit_warp(bar);
+    if (lane == 0) mbar_arrive_n(bar, kConsumerWarps - 1);
+    __syncwarp();
   }
 
 
 
-  // The products of one unit: nst ring stages, each issued by lane 0 as soon as it lands (kTcK
-  // columns: 4 k-steps of 16, for each group of 4 tokens), then every product completed. A of
-  // stage st is at a_base + st * a_stride; accumulation restarts at the unit's first product
-  // unless `accumulate` (down: the next expert of the same partial). The warp's ring position
-  // moves past the stages.
-  __device__ bool tc_products(int nst, uint32_t a_base, uint32_t a_stride, bool accumulate, bool last) {
-    constexpr uint32_t idesc = tc_idesc(64, kTcN);
+  // The products of one unit, issued by warp 0 (converged; lane 0 waits, the elected lane issues):
+  // nst ring stages, each as soon as it lands, then (if `last`) every product completed. A stage
+  // holds kStageK columns as two 64-column chunks of 4 k-steps of 16; B = the chunk's 128 weight
+  // rows (gate/up: kGuRows gate rows then kGuRows up rows; down: kDnRows output rows), one N = 128
+  // product per chunk and k-step. A is the token rows: at batch <= 4 one group of 8 rows (4 tokens
+  // x {hi, lo}) that a group stride of 0 repeats in every 8-row group of M; at batch 8 two groups,
+  // 1 KB apart, as rows 0-15 of M (the rows after them read whatever follows in shared memory and
+  // are never read back). So one product serves all tokens, and the tensor pipe takes 512 cycles
+  // per 32 KB stage (measured). A of stage st: the chunks at a_base + st * a_step (a_base 0: the
+  // activations riding in the stage after its payload). Gate/up and down share this one loop, so
+  // its instructions stay cached from one to the other.
+  // Accumulation restarts at the unit's first product unless `accumulate` (down: the next expert
+  // of the same partial). D starts at tensor-memory column dcol. With done_bar set, the last
+  // products' completion is signalled there by a commit and not awaited. The warp's ring
+  // position moves past the stages.
+  __device__ bool tc_products(int nst, uint32_t a_base, uint32_t a_step, bool accumulate, bool last,
+                              uint32_t dcol = 0, uint32_t done_bar = 0) {
+    static_assert(kGuRows * 2 == 128 && kDnRows == 128, "one N = 128 product per chunk");
+    constexpr uint32_t idesc = tc_idesc(64, 128);
+    constexpr uint32_t kASbo = NB > 4 ? 1024u : 0u;
     int done = 1;
-    if (lane == 0) {
 #pragma unroll 1
-      for (int st = 0; st < nst; ++st) {
-        const uint32_t it = r.it + st;
-        if (!mbar_wait_spin(p, r.full + 8 * (it % kStages), (it / kStages) & 1u)) {
-          done = 0;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t wb = r.data + (it % kStages) * kStageBytes;
-        const uint32_t ab = a_base == 0 ? wb + kStagePayload : a_base + st * a_stride;  // 0: A rides in the stage
+    for (int st = 0; st < nst; ++st) {
+      const uint32_t it = r.it + st;
+      int fine = 1;
+      if (lane == 0) fine = mbar_wait_spin(p, r.full + 8 * (it % kStages), (it / kStages) & 1u);
+      if (!__shfl_sync(0xffffffffu, fine, 0)) {
+        done = 0;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t wb = r.data + (it % kStages) * kStageBytes;
+      const uint32_t ab = a_base ? a_base + (uint32_t)st * a_step : wb + kStagePayload;
+      // descriptors built once per stage; offsets go into the 14-bit address field (byte address
+      // / 16; shared addresses stay below 256 KB, so the field never carries)
+      const uint64_t a0 = tc_sdesc(ab, kASbo), b0 = tc_sdesc(wb, 1024);
+#pragma unroll
+      for (int c = 0; c < kStageK / kTcK; ++c)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int q = 0; q < kAGroups; ++q)
-            tc_mma(tmem + q * kTcN, tc_sdesc(ab + q * 1024 + k * 32, 0), tc_sdesc(wb + k * 32, 1024), idesc,
-                   accumulate || st != 0 || k != 0);
-        tc_free(it);
-      }
-      if (done && last) {
-        tc_commit(smem_addr(&m.tc_acc));
-        done = mbar_wait_spin(p, smem_addr(&m.tc_acc), tc_phase);
+          tc_mma_warp(tmem + dcol, a0 + (uint64_t)((c * kAChunk + k * 32) >> 4),
+                      b0 + (uint64_t)((c * 128 * 128 + k * 32) >> 4), idesc,
+                      (accumulate || st != 0 || c != 0 || k != 0) ? 1u : 0u);
+      tc_free(it);
+    }
+    if (done && last) {
+      if (done_bar) {
+        tc_commit_warp(done_bar);
+      } else {
+        tc_commit_warp(smem_addr(&m.tc_acc));
+        int fine = 1;
+        if (lane == 0) fine = mbar_wait_spin(p, smem_addr(&m.tc_acc), tc_phase);
+        done = __shfl_sync(0xffffffffu, fine, 0);
       }
     }
-    done = __shfl_sync(0xffffffffu, done, 0);
     r.it += nst;
-    if (last) tc_phase ^= 1u;
+    if (last && !done_bar) tc_phase ^= 1u;
     tc_fence_after();
     if (!done) ok = false;
     return done != 0;
@@ -1461,74 +1547,105 @@ struct Consumer {
     const int l = t.layer;
     if (!load_route(l)) return;
     t_ready = gtimer();
-    const int na = m.rc_n, maxa = max_active(p), nst = p.H / kTcK;
+    const int na = m.rc_n, maxa = max_active(p), nst = p.H / kStageK;
     const size_t slot_bytes = hsw_slot_bytes(p.I);
-#pragma unroll 1
-    for (int u = t.a; u < t.a + t.b; ++u) {
-      const int a = u % maxa, j = u / maxa;
-      if (a >= na) continue;
-      // warp 0 runs the unit's products; the others step over its stages. D[group q], kTcN columns
-      // at q kTcN: the unit's gate rows then its up rows, against the normalized input (A chunk st
-      // of the shared A operand)
-      if (warp == 0) tc_products(nst, abuf, kAChunk, false, true);
-      else r.it += nst;
-      tc_fence_before();
-      if (!csync() || !ok) return;
+    // Units alternate between two accumulator buffers, tensor-memory columns [256 b, 256 b + 256):
+    // warp 0 issues unit n's products into buffer n & 1 (D of token group q at 128 q: the unit's
+    // gate rows, then its up rows) and signals acc_full[n & 1] by a commit without waiting, while
+    // warps 4-7 run unit n - 1's epilogue from the other buffer and hand it back through
+    // acc_empty. The j-th use of a buffer completes phase j of both its barriers (parity j & 1).
+    // Warps 1-7 step their ring position over the stages; the block barrier at the end keeps the
+    // ring waits of the next task exact.
+    auto epilogue = [&](uint32_t n, int a, int j) {
+      // D row r holds token 4 (r / 8) + (r % 8) / 2, part r % 2 (hi, lo). At batch <= 4 the A
+      // group stride 0 repeats rows 0-7 in every 16-lane group of D, so warp w (4-7) reads them
+      // from its own lane quarter (tensor-memory lanes 32 (w - 4) + r) and takes gate/up columns
+      // [16 (w - 4), +16); at batch 8 rows 0-15 sit in lane quarter 0 only, and warp 4 takes all
+      // 64 columns (acc_empty then counts one arrival per phase instead of four).
+      constexpr int kRows = NB > 4 ? 16 : 8;
+      const uint32_t buf = n & 1u, wq = (uint32_t)warp & 3u;
+      if (NB > 4 && wq != 0) return;
+      int fine = 1;
+      if (lane == 0) fine = mbar_wait_spin(p, smem_addr(&m.acc_full[buf]), (n >> 1) & 1u);
+      if (!__shfl_sync(0xffffffffu, fine, 0)) {
+        ok = false;
+        return;
+      }
       tc_fence_after();
-      // epilogue, warps 0-3: the descriptor's group stride 0 repeats the 8 token rows in every
-      // 16-lane group of D, so warp w reads them from its own lane quarter (tensor-memory lanes
-      // 32 w + r) and takes gate/up columns [32 w, 32 w + 32)
-      if (warp < 4) {
-        uint8_t* hs = p.hsw + ((size_t)l * kMaxActive + a) * slot_bytes;
-        const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+      uint8_t* hs = p.hsw + ((size_t)l * kMaxActive + a) * slot_bytes;
+      const uint32_t tq = tmem + buf * 256u + ((32u * wq) << 16);
+      const int q = (lane >> 3) & 1, rr = lane & 7, tok = 4 * q + (rr >> 1), hl = rr & 1;
+      const bool row_ok = lane < kRows && tok < p.B;
+      const float wgt = row_ok ? m.rc_w[a][tok] : 0.f;
+      const int c0 = NB > 4 ? 0 : 16 * (int)wq, c1 = NB > 4 ? kGuRows : c0 + 16;
 #pragma unroll 1
-        for (int q = 0; q < kAGroups; ++q) {
-          const int rr = lane & 7, tok = 4 * q + (rr >> 1), hl = rr & 1;
-          const float wgt = (lane < 8 && tok < p.B) ? m.rc_w[a][tok] : 0.f;
-#pragma unroll 1
-          for (int i0 = 32 * warp; i0 < 32 * warp + 32; i0 += 16) {
-            uint32_t gv_[16], uv[16];
-            tc_ld16(tq + q * kTcN + i0, gv_);
-            tc_ld16(tq + q * kTcN + kGuRows + i0, uv);
-            // hi + lo of each gate and up value (lanes 2 t and 2 t + 1 hold the two parts of token
-            // t); lanes past the 8 token rows hold tensor-memory words no product wrote
-            float gs[16], us[16];
+      for (int i0 = c0; i0 < c1; i0 += 16) {
+        uint32_t gv_[16], uv[16];
+        tc_ld16(tq + i0, gv_);
+        tc_ld16(tq + kGuRows + i0, uv);
+        // hi + lo of each gate and up value (lanes 2 t and 2 t + 1 hold the two parts of token
+        // t); lanes past the token rows hold tensor-memory words no product wrote
+        float gs[16], us[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              gs[c] = lane < 8 ? __uint_as_float(gv_[c]) : 0.f;
-              us[c] = lane < 8 ? __uint_as_float(uv[c]) : 0.f;
-              gs[c] += __shfl_xor_sync(0xffffffffu, gs[c], 1);
-              us[c] += __shfl_xor_sync(0xffffffffu, us[c], 1);
-            }
-            if (lane < 8 && tok < p.B) {
-              uint32_t packed[8];
+        for (int c = 0; c < 16; ++c) {
+          gs[c] = lane < kRows ? __uint_as_float(gv_[c]) : 0.f;
+          us[c] = lane < kRows ? __uint_as_float(uv[c]) : 0.f;
+          gs[c] += __shfl_xor_sync(0xffffffffu, gs[c], 1);
+          us[c] += __shfl_xor_sync(0xffffffffu, us[c], 1);
+        }
+        if (row_ok) {
+          uint32_t packed[8];
 #pragma unroll
-              for (int c = 0; c < 16; c += 2) {
-                float hv[2];
+          for (int c = 0; c < 16; c += 2) {
+            float hv[2];
 #pragma unroll
-                for (int e = 0; e < 2; ++e)  // SiLU(g) = g / (1 + e^-g), times up and the routing weight
-                  hv[e] = __fdividef(gs[c + e], 1.0f + __expf(-gs[c + e])) * us[c + e] * wgt;
-                uint32_t hi, lo;
-                split_pack(hv[0], hv[1], hi, lo);
-                packed[c / 2] = hl ? lo : hi;
-              }
-              // columns kc = j kGuRows + i0 + 0..15: chunk kc / 64, 16-byte units (kc % 64) / 8 + 0..1
-              const int kc = j * kGuRows + i0;
-              uint8_t* rowp = hs + (size_t)(kc >> 6) * kAChunk + q * 1024 + rr * 128;
+            for (int e = 0; e < 2; ++e)  // SiLU(g) = g / (1 + e^-g), times up and the routing weight
+              hv[e] = __fdividef(gs[c + e], 1.0f + __expf(-gs[c + e])) * us[c + e] * wgt;
+            uint32_t hi, lo;
+            split_pack(hv[0], hv[1], hi, lo);
+            packed[c / 2] = hl ? lo : hi;
+          }
+          // columns kc = j kGuRows + i0 + 0..15: chunk kc / 64, 16-byte units (kc % 64) / 8 + 0..1
+          const int kc = j * kGuRows + i0;
+          uint8_t* rowp = hs + (size_t)(kc >> 6) * kAChunk + q * 1024 + rr * 128;
 #pragma unroll
-              for (int m4 = 0; m4 < 2; ++m4) {
-                const int u16 = ((kc & 63) >> 3) + m4;
-                __stcg(reinterpret_cast<uint4*>(rowp + ((u16 ^ rr) << 4)),
-                       make_uint4(packed[4 * m4], packed[4 * m4 + 1], packed[4 * m4 + 2], packed[4 * m4 + 3]));
-              }
-            }
+          for (int m4 = 0; m4 < 2; ++m4) {
+            const int u16 = ((kc & 63) >> 3) + m4;
+            __stcg(reinterpret_cast<uint4*>(rowp + ((u16 ^ rr) << 4)),
+                   make_uint4(packed[4 * m4], packed[4 * m4 + 1], packed[4 * m4 + 2], packed[4 * m4 + 3]));
           }
         }
-        tc_fence_before();
       }
-      // the accumulators are read before the next unit's products overwrite them
-      if (!csync()) return;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&m.acc_empty[buf]));
+    };
+    uint32_t n = gu_units;
+    int pa = -1, pj = 0;
+#pragma unroll 1
+    for (int u = t.a; u < t.a + t.b && ok; ++u) {
+      const int a = u % maxa, j = u / maxa;
+      if (a >= na) continue;
+      if (warp == 0) {
+        // buffer n & 1 is free once unit n - 2's epilogue has read it
+        int fine = 1;
+        if (lane == 0 && n >= 2) fine = mbar_wait_spin(p, smem_addr(&m.acc_empty[n & 1u]), ((n >> 1) & 1u) ^ 1u);
+        if (!__shfl_sync(0xffffffffu, fine, 0)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        tc_products(nst, abuf, 2 * kAChunk, false, true, (n & 1u) * 256u, smem_addr(&m.acc_full[n & 1u]));
+      } else {
+        r.it += nst;
+      }
+      if (warp >= 4 && pa >= 0) epilogue(n - 1, pa, pj);
+      pa = a, pj = j;
+      ++n;
     }
+    if (warp >= 4 && pa >= 0 && ok) epilogue(n - 1, pa, pj);
+    gu_units = n;
+    if (!csync()) return;
     release_counter(cm.gu(l));
   }
 
@@ -1595,13 +1712,13 @@ struct Consumer {
     const int l = t.layer;
     if (!load_route(l)) return;
     t_ready = gtimer();
-    const int na = m.rc_n, parts = p.moe_parts, nst = p.I / kTcK;
+    const int na = m.rc_n, parts = p.moe_parts, nst = p.I / kStageK;
 #pragma unroll 1
     for (int u = t.a; u < t.a + t.b; ++u) {
       const int rb = u / parts, part = u % parts;
-      // partial `part` of output rows [kTcN rb, +kTcN): the routed experts of rank part, part +
-      // parts, ..., accumulated in rank order; stage st carries the expert's kTcN weight rows'
-      // columns [64 st, +64) (B) and, after them in the slot, its activations of those columns (A)
+      // partial `part` of output rows [kDnRows rb, +kDnRows): the routed experts of rank part,
+      // part + parts, ..., accumulated in rank order; stage st carries the expert's weight rows'
+      // columns [128 st, +128) (B) and, after them in the slot, its activations of those columns (A)
       int ne = 0;
       for (int a = part; a < na; a += parts) ++ne;
       if (warp == 0) {
@@ -1613,34 +1730,36 @@ struct Consumer {
       tc_fence_before();
       if (!csync() || !ok) return;
       tc_fence_after();
-      // epilogue, warps 0-3 (each from its own tensor-memory lane quarter, see op_gu): output
-      // columns [64 w, 64 w + 64), zero when no routed expert falls in this partial
-      if (warp < 4) {
+      // epilogue (D rows as in op_gu): at batch <= 4 warps 0-3, each from its own tensor-memory
+      // lane quarter, output columns [32 w, 32 w + 32); at batch 8 warp 0 (rows 0-15 in lane
+      // quarter 0) all kDnRows columns. Zero when no routed expert falls in this partial.
+      constexpr int kRows = NB > 4 ? 16 : 8;
+      if (NB > 4 ? warp == 0 : warp < 4) {
         const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
-        const int rr = lane & 7, hl = rr & 1;
+        const int q = (lane >> 3) & 1, rr = lane & 7, hl = rr & 1, tok = 4 * q + (rr >> 1);
+        float* dst = p.moe_part + (((size_t)l * kMoeParts + part) * p.B + tok) * p.H + rb * kDnRows;
+        const int c0 = NB > 4 ? 0 : 32 * warp, c1 = NB > 4 ? kDnRows : c0 + 32;
 #pragma unroll 1
-        for (int q = 0; q < kAGroups; ++q) {
-          const int tok = 4 * q + (rr >> 1);
-          float* dst = p.moe_part + (((size_t)l * kMoeParts + part) * p.B + tok) * p.H + rb * kTcN;
-#pragma unroll 1
-          for (int i0 = 64 * warp; i0 < 64 * warp + 64; i0 += 16) {
-            uint32_t v[16];
-            if (ne > 0) tc_ld16(tq + q * kTcN + i0, v);
-            float o[16];
+        for (int i0 = c0; i0 < c1; i0 += 16) {
+          uint32_t v[16];
+          if (ne > 0) tc_ld16(tq + i0, v);
+          float o[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              float x = (ne == 0 || lane >= 8) ? 0.f : __uint_as_float(v[c]);
-              x += __shfl_xor_sync(0xffffffffu, x, 1);  // hi + lo
-              o[c] = x;
-            }
-            if (lane < 8 && hl == 0 && tok < p.B)
-#pragma unroll
-              for (int c = 0; c < 16; c += 4)
-                __stcg(reinterpret_cast<float4*>(dst + i0 + c), make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]));
+          for (int c = 0; c < 16; ++c) {
+            float x = (ne == 0 || lane >= kRows) ? 0.f : __uint_as_float(v[c]);
+            x += __shfl_xor_sync(0xffffffffu, x, 1);  // hi + lo
+            o[c] = x;
           }
+          if (lane < kRows && hl == 0 && tok < p.B)
+#pragma unroll
+            for (int c = 0; c < 16; c += 4)
+              __stcg(reinterpret_cast<float4*>(dst + i0 + c), make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]));
         }
-        tc_fence_before();
       }
+      // the accumulator is read before warp 0 issues the next products into it (the next unit's,
+      // or those of the block's next tensor-core task)
+      tc_fence_before();
+      if (!csync()) return;
     }
     release_counter(cm.layer(l));
   }
@@ -2067,6 +2186,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_decode_kernel(const __grid_con
     }
     mbar_init(smem_addr(&misc.cbar), kConsumerWarps);
     mbar_init(smem_addr(&misc.tc_acc), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&misc.acc_full[b]), 1);
+      mbar_init(smem_addr(&misc.acc_empty[b]), NB > 4 ? 1 : 4);  // the epilogue's reading warps
+    }
     for (int i = 0; i < kRedBufs; ++i) {
       mbar_init(smem_addr(&misc.gpart[i]), kConsumerWarps);
       mbar_init(smem_addr(&misc.gfree[i]), 1);

@@ -56,18 +56,18 @@ def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
                 assert ch == list(range(len(ch))) and len(ch) >= 1
                 assert n is None or n == len(ch)
                 n = len(ch)
-        # gate/up: tensor-core units of 128 gate rows (and their up rows) per routed expert
+        # gate/up: tensor-core units of 64 gate rows (and their up rows) per routed expert
         g = t[t["op"] == OP_GU]
-        assert sorted(_ranges(g).tolist()) == list(range(maxa * (w.I // 128)))
+        assert sorted(_ranges(g).tolist()) == list(range(maxa * (w.I // 64)))
         o = t[t["op"] == OP_O]
         rs_o = rows_per_stage(w.nq * w.d)  # O tasks: whole row blocks (the last may be short)
         assert sorted(_ranges(o).tolist()) == list(range(w.H))
         assert np.all((o["b"] % rs_o == 0) | (o["a"] + o["b"] == w.H))
-        # down: one task per (256-row block, partial) unit; a partial takes the experts of rank
+        # down: one task per (128-row block, partial) unit; a partial takes the experts of rank
         # j, j + parts, ..., so every unit of a layer has the same share of the routed experts
         dn = t[t["op"] == OP_DOWN]
         parts = min(8, maxa)
-        assert sorted(_ranges(dn).tolist()) == list(range((w.H // 256) * parts)) and np.all(dn["b"] == 1)
+        assert sorted(_ranges(dn).tolist()) == list(range((w.H // 128) * parts)) and np.all(dn["b"] == 1)
     lm = tasks[tasks["op"] == OP_LM]
     assert sorted(_ranges(lm).tolist()) == list(range(w.V))
     assert np.all(lm["flags"] & 2) and len(lm) == info.n_lm_sm and sorted(lm["c"].tolist()) == list(range(len(lm)))
@@ -114,15 +114,17 @@ def test_plan_splits_branches_over_disjoint_sms(w, n_sm):
         assert np.bincount(q, minlength=n_sm).max() <= 1
     if w.H < 2048:  # the small models have fewer tasks than SMs
         return
-    # every SM of a partition gets work of its branch in every layer, and no SM takes two
-    # attention chunks, two O-proj tasks or two down tasks of one layer (a second one would
-    # double that phase on its SM)
+    # every SM of a partition gets work of its branch in every layer, no SM takes two attention
+    # chunks or two O-proj tasks of one layer (a second one would double that phase on its SM),
+    # and the down units spread evenly over the expert SMs
     for l in (0, w.L - 1):
         lay = tasks["layer"] == l
         assert set(owner[attn & lay].tolist()) == set(range(na))
         assert set(owner[moe & lay].tolist()) == set(range(na, n_sm))
-        for op in (OP_ATTN, OP_O, OP_DOWN):
+        for op in (OP_ATTN, OP_O):
             assert np.bincount(owner[(tasks["op"] == op) & lay], minlength=n_sm).max() == 1, op
+        dn = owner[(tasks["op"] == OP_DOWN) & lay]
+        assert np.bincount(dn, minlength=n_sm).max() == -(-len(dn) // (n_sm - na))
 
 
 @pytest.mark.parametrize("ctx_len", [100, 1000, 4096, 8192, 16384, 30000])
