@@ -105,9 +105,8 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 // The same, issued from a converged warp: every lane computes the (warp-uniform) operands and
-// the elected lane (the lowest, lane 0) issues. Keeping the operands warp-uniform lets the
-// compiler hold them where the tensor-core issue reads them; one lane alone under a branch issues
-// about 45 % slower (measured).
+// the elected lane (the lowest, lane 0) issues. In isolation (one warp issuing back to back) this
+// form issued about 30 % faster than lane 0 alone under a branch (measured).
 __device__ __forceinline__ void tc_mma_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
@@ -1471,17 +1470,35 @@ struct Consumer {
   // of the stages that are actually in it.
 
 
+  // Product issue and commits of warp 0 (converged). At batch 8 the elected lane issues from
+  // warp-uniform operands; at batch <= 4 lane 0 issues under a branch. Both run the same products
+  // from lane 0; measured on the 30B-shaped model, each form is the faster one at its batch size
+  // (batch 1 at 8K: 1.995 vs 2.250 ms per step; batch 8: 9.97 vs 10.68 ms).
+  __device__ __forceinline__ void tc_issue(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    if constexpr (NB > 4) {
+      tc_mma_warp(d, a, b, idesc, acc);
+    } else {
+      if (lane == 0) tc_mma(d, a, b, idesc, acc);
+    }
+  }
+  __device__ __forceinline__ void tc_commit_w0(uint32_t bar) {
+    if constexpr (NB > 4) {
+      tc_commit_warp(bar);
+    } else {
+      if (lane == 0) tc_commit(bar);
+    }
+  }
   // free ring stage `it` once the products issued so far have read it (warp 0, converged)
   __device__ void tc_free(uint32_t it) {
     const uint32_t bar = r.empty + 8 * (it % kStages);
-    tc_commit_warp(bar);
+    tc_commit_w0(bar);
     if (lane == 0) mbar_arrive_n(bar, kConsumerWarps - 1);
     __syncwarp();
   }
 
 
 
-  // The products of one unit, issued by warp 0 (converged; lane 0 waits, the elected lane issues):
+  // The products of one unit, issued by warp 0 (converged; lane 0 waits and issues, see tc_issue):
   // nst ring stages, each as soon as it lands, then (if `last`) every product completed. A stage
   // holds kStageK columns as two 64-column chunks of 4 k-steps of 16; B = the chunk's 128 weight
   // rows (gate/up: kGuRows gate rows then kGuRows up rows; down: kDnRows output rows), one N = 128
@@ -1521,16 +1538,16 @@ struct Consumer {
       for (int c = 0; c < kStageK / kTcK; ++c)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc_mma_warp(tmem + dcol, a0 + (uint64_t)((c * kAChunk + k * 32) >> 4),
-                      b0 + (uint64_t)((c * 128 * 128 + k * 32) >> 4), idesc,
-                      (accumulate || st != 0 || c != 0 || k != 0) ? 1u : 0u);
+          tc_issue(tmem + dcol, a0 + (uint64_t)((c * kAChunk + k * 32) >> 4),
+                   b0 + (uint64_t)((c * 128 * 128 + k * 32) >> 4), idesc,
+                   (accumulate || st != 0 || c != 0 || k != 0) ? 1u : 0u);
       tc_free(it);
     }
     if (done && last) {
       if (done_bar) {
-        tc_commit_warp(done_bar);
+        tc_commit_w0(done_bar);
       } else {
-        tc_commit_warp(smem_addr(&m.tc_acc));
+        tc_commit_w0(smem_addr(&m.tc_acc));
         int fine = 1;
         if (lane == 0) fine = mbar_wait_spin(p, smem_addr(&m.tc_acc), tc_phase);
         done = __shfl_sync(0xffffffffu, fine, 0);
