@@ -472,7 +472,9 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   const int qkv_tasks = n_attn < n_sm ? n_sm - (E + gh.RS - 1) / gh.RS : 2 * n_attn;
   int qkv_per_task = std::max(1, (nkv * upg_ + qkv_tasks - 1) / qkv_tasks);
   qkv_per_task = std::max(gh.RG, (qkv_per_task + gh.RG - 1) / gh.RG * gh.RG);
-  const int gu_per_task = std::max(1, (maxa * tiles + n_moe - 1) / n_moe);
+  // gate/up tasks: at most one per expert SM; each takes an equal share of the units of the
+  // experts the step actually routes to (known on the device only), see the kernel's op_gu
+  const int n_gu_tasks = std::max(1, std::min(n_moe, maxa * tiles));
   const long long row_h = 2LL * H;
 
   Assigner as(n_sm, part, PM + 1);
@@ -526,12 +528,11 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
       cnt[cmap.qkv(l, g)] = n;
     }
     emit(ts, n_attn < n_sm ? -1 : PA);
-    // expert gate/up: units u = tile * maxa + active_rank, about one task per expert SM
-    int n_gu = 0;
-    for (int u = 0; u < maxa * tiles; u += gu_per_task, ++n_gu) {
-      const int n = std::min(gu_per_task, maxa * tiles - u);
-      ts.push_back({mkt(OP_GU, l, u, n, 0), (long long)(n * live * 2 * kGuRows * row_h)});
-    }
+    // expert gate/up: task k of n takes units [k U / n, (k + 1) U / n) of the U = active experts
+    // x tiles units of the step
+    const int n_gu = n_gu_tasks;
+    for (int k = 0; k < n_gu; ++k)
+      ts.push_back({mkt(OP_GU, l, k, n_gu, 0), (long long)(live * maxa * tiles * 2 * kGuRows * row_h / n_gu)});
     cnt[cmap.gu(l)] = n_gu;
     emit(ts, PM);
     // attention chunks: task i of every layer on the same attention SM (i mod n_attn), which then

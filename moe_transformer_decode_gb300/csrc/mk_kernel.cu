@@ -387,6 +387,18 @@ __device__ __forceinline__ AttnRange attn_range(int pos, int cpp, int nch, int c
 }
 __device__ __forceinline__ int attn_pps(const Params& p) { return kStagePayload / (4096 * (p.d / 64)); }
 
+// Gate/up task t.a of t.b (a layer's tasks) takes units [v0, v1) of the step's na x tiles units,
+// unit v = (routed expert rank v % na, row block v / na): an equal share of the experts the step
+// actually routes to, however many that is. Producer and consumers compute it alike from the
+// layer's routing, so the split is deterministic and needs no claim counter.
+struct GuRange {
+  int v0, v1;
+};
+__device__ __forceinline__ GuRange gu_range(const Task& t, int na, int tiles) {
+  const long long total = (long long)na * tiles;
+  return GuRange{(int)(total * t.a / t.b), (int)(total * (t.a + 1) / t.b)};
+}
+
 __device__ __forceinline__ int max_active(const Params& p) { return min(p.B * p.topk, p.E); }
 
 // ------------------------------------------------------------------ shared memory
@@ -619,11 +631,11 @@ struct Producer {
         // 64-column chunks, each [kGuRows gate rows | kGuRows up rows][128 bytes] (swizzled), the
         // same B layout as a down stage: four tensor copies, lane 2 c + g for chunk c, gate (0) or up (1)
         if (!route(l)) return false;
-        const int na = m.pr_n, maxa = max_active(p), nst = p.H / kStageK;
+        const int na = m.pr_n, nst = p.H / kStageK;
+        const GuRange gr = gu_range(t, na, p.I / kGuRows);
 #pragma unroll 1
-        for (int u = t.a; u < t.a + t.b; ++u) {
-          const int a = u % maxa, j = u / maxa;
-          if (a >= na) continue;
+        for (int v = gr.v0; v < gr.v1; ++v) {
+          const int a = v % na, j = v / na;
           const int grow = ((l * p.E + m.pr_expert[a]) * 2 * p.I) + j * kGuRows;
 #pragma unroll 1
           for (int st = 0; st < nst; ++st) {
@@ -1564,8 +1576,9 @@ struct Consumer {
     const int l = t.layer;
     if (!load_route(l)) return;
     t_ready = gtimer();
-    const int na = m.rc_n, maxa = max_active(p), nst = p.H / kStageK;
+    const int na = m.rc_n, nst = p.H / kStageK;
     const size_t slot_bytes = hsw_slot_bytes(p.I);
+    const GuRange gr = gu_range(t, na, p.I / kGuRows);
     // Units alternate between two accumulator buffers, tensor-memory columns [256 b, 256 b + 256):
     // warp 0 issues unit n's products into buffer n & 1 (D of token group q at 128 q: the unit's
     // gate rows, then its up rows) and signals acc_full[n & 1] by a commit without waiting, while
@@ -1640,9 +1653,8 @@ struct Consumer {
     uint32_t n = gu_units;
     int pa = -1, pj = 0;
 #pragma unroll 1
-    for (int u = t.a; u < t.a + t.b && ok; ++u) {
-      const int a = u % maxa, j = u / maxa;
-      if (a >= na) continue;
+    for (int v = gr.v0; v < gr.v1 && ok; ++v) {
+      const int a = v % na, j = v / na;
       if (warp == 0) {
         // buffer n & 1 is free once unit n - 2's epilogue has read it
         int fine = 1;

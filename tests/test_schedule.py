@@ -56,9 +56,12 @@ def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
                 assert ch == list(range(len(ch))) and len(ch) >= 1
                 assert n is None or n == len(ch)
                 n = len(ch)
-        # gate/up: tensor-core units of 64 gate rows (and their up rows) per routed expert
+        # gate/up: task k of n takes an equal share of the routed experts' units (64 gate rows
+        # and their up rows each), so the tasks are k = 0 .. n - 1 of n, at most one per SM and
+        # no more than there are units
         g = t[t["op"] == OP_GU]
-        assert sorted(_ranges(g).tolist()) == list(range(maxa * (w.I // 64)))
+        assert sorted(g["a"].tolist()) == list(range(len(g))) and np.all(g["b"] == len(g))
+        assert 1 <= len(g) <= min(n_sm, maxa * (w.I // 64))
         o = t[t["op"] == OP_O]
         rs_o = rows_per_stage(w.nq * w.d)  # O tasks: whole row blocks (the last may be short)
         assert sorted(_ranges(o).tolist()) == list(range(w.H))
