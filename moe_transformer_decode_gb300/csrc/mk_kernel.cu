@@ -1144,10 +1144,12 @@ struct Consumer {
   // [32 q, 32 q + 32) of this warp's slice) takes 16-byte unit 4 (q % 2) + t of row g (0: hi,
   // 1: lo of token 0) of 64-column chunk 4 ks + q / 2, which holds its (a0, a2) registers of
   // k-steps 2 q and 2 q + 1 in the column map above; every other lane's are zero
-  __device__ __forceinline__ void mma_rows_nf1(const uint8_t* st, const Geo& g, int rg, int ks, float (&c)[4][4]) const {
+  // (cbase: the A-buffer chunk of the stage's first column, for inputs wider than one stage)
+  __device__ __forceinline__ void mma_rows_nf1(const uint8_t* st, const Geo& g, int rg, int ks, float (&c)[4][4],
+                                               int cbase = 0) const {
     const uint8_t* rowp = b_row(st, g, rg, ks);
     const int r = (lane >> 2) & 1, t4 = lane & 3;
-    const uint32_t fr = abuf + (uint32_t)(4 * ks) * kAChunk + r * 128;
+    const uint32_t fr = abuf + (uint32_t)(cbase + 4 * ks) * kAChunk + r * 128;
     const bool has = lane < 8;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
@@ -1702,6 +1704,43 @@ struct Consumer {
       });
     };
     t_ready = 0;
+    if (NB == 1 && p.od / 64 * kAChunk <= kABufBytes) {
+      // Batch 1: the attention output (hi, lo) goes into the A buffer once, as rows 0 and 1 of its
+      // 64-column chunks (the layout mma_rows_nf1 reads). Nothing in the layer reads the buffer
+      // after attention, and the next layer's norm rebuilds it.
+      for (int gg = 0; gg < p.nkv; ++gg)
+        if (!wait_attn_group(l, gg)) return;
+      t_ready = gtimer();
+      const uint16_t* src = p.attn_hl + (size_t)l * 2 * p.od;  // [hi | lo][od] of token 0
+      for (int i = threadIdx.x; i < p.od / 4; i += kConsumerWarps * 32) {
+        const int hl = i / (p.od / 8), col = (i % (p.od / 8)) * 8;
+        const uint4 v = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)hl * p.od + col));
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(abuf + (uint32_t)(col >> 6) * kAChunk + hl * 128 +
+                                                                      ((((col & 63) >> 3) ^ hl) << 4)),
+                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+      n_layer = -1;
+      if (!csync()) return;
+      uint32_t prev = 0;
+      int pr0 = -1, prows = 0;
+      for (int r0 = 0; r0 < t.b && ok; r0 += g.RS) {
+        float c[4][4] = {};
+        for (int cs = 0; cs < g.NCS; ++cs) {
+          const uint8_t* st = acquire();
+          if (!st) return;
+          if (active) mma_rows_nf1(st, g, rg, ks, c, cs * (g.KS / 64));
+          release();
+        }
+        const uint32_t pid = post_pass(active, c);
+        if (!ok) return;
+        if (pr0 >= 0) epi(prev, pr0, prows);
+        prev = pid, pr0 = r0, prows = min(g.RS, t.b - r0);
+      }
+      if (pr0 >= 0) epi(prev, pr0, prows);
+      if (ok) release_counter(cm.layer(l));
+      return;
+    }
     // At batch <= 4 with at most two column chunks, both chunks' fragments are loaded once and
     // reused by every row block of the task; otherwise (one block per task) chunk by chunk.
     constexpr bool kHold = AR == 2;
