@@ -296,6 +296,17 @@ def measure(w, args, device, world):
     e2e_s = time.perf_counter() - t0
     dc.sync()
     e2e_s = ranks_max(e2e_s, device)
+    timeline_summary = None
+    if getattr(args, "timeline", False):
+        # after every timed region: two traced steps (the first warms the trace path), per-op phase
+        # times and SM idle shares from the kernel's own per-task records
+        from moe_transformer_decode_gb300 import timeline
+
+        for i in range(2):
+            h_pos.numpy()[:] = ctx_np + done + n_e2e + i
+            d_pos.copy_(h_pos)
+            ent = timeline.trace_step(dc, w, d_tok, d_pos, K, V, None, d_out)
+        timeline_summary = timeline.summarize(ent, w.L)
     dc.close()
     del dc, model, K, V
     torch.cuda.empty_cache()
@@ -320,6 +331,7 @@ def measure(w, args, device, world):
                 "d2h_bytes_per_step": 4 * w.B},
         "clocks": clk.summary(),
         "config": bench_config(w, args.mode, world),
+        **({"timeline": timeline_summary} if timeline_summary is not None else {}),
     }
 
 
@@ -339,6 +351,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only (no by_config lines)")
     ap.add_argument("--mode", default="megakernel", choices=["megakernel", "per_op"])
+    ap.add_argument("--timeline", action="store_true",
+                    help="after the timed region, trace two steps and print per-op phase times and SM idle "
+                         "shares (stderr)")
     args = ap.parse_args()
 
     from synth import workloads as W
@@ -360,6 +375,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device(device))
     assert args.warmup >= 3, "at least 3 warm-up steps"
     head = measure(w, args, device, world)
+    if rank == 0 and "timeline" in head:
+        print("timeline " + json.dumps({"workload": w.name, **head["timeline"]}), file=sys.stderr, flush=True)
     line = {"metric": METRIC, "value": head["value"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
