@@ -463,7 +463,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   // expert GEMVs (tcgen05): gate/up units of kGuRows gate rows + the matching up rows over H;
   // down units of kDnRows output rows for one of `parts` partials (experts of rank j mod parts)
   const int tiles = I / kGuRows;
-  const int parts = std::min(kMoeParts, maxa);
+  const int parts = moe_parts_for(B, m.top_k, E);
   // Per layer, gate/up tasks are sized to about two per expert SM and QKV tasks to about two
   // per SM (whole stages each, rounded up so that no SM gets a third). When the SMs are
   // partitioned, QKV runs on every SM but the router's, about one task each: it needs only the
@@ -728,7 +728,7 @@ static Params make_params(mk_ctx* c, const int32_t* tokens, const int32_t* posit
   p.chunk_pages = c->d_chunk_pages; p.n_chunks = c->d_n_chunks;
   p.xs = c->xs; p.q = c->q; p.knew = c->knew; p.vnew = c->vnew; p.apart = c->apart; p.attn_o = c->attn_o;
   p.attn_out = c->attn_out; p.rlogits = c->rlogits; p.hsw = c->hsw; p.attn_hl = c->attn_hl; p.moe_out = c->moe_out;
-  p.moe_part = c->moe_part; p.moe_parts = std::min(kMoeParts, std::min(c->B * m.top_k, m.n_experts)); p.route = c->route;
+  p.moe_part = c->moe_part; p.moe_parts = moe_parts_for(c->B, m.top_k, m.n_experts); p.route = c->route;
   p.lm_best_v = c->lm_best_v; p.lm_best_i = c->lm_best_i; p.counters = c->counters; p.status = c->status;
   p.status_host = c->status_host_dev; p.topk_ids = c->topk_ids; p.topk_w = c->topk_w;
   p.trace = c->trace; p.trace_count = c->trace_count; p.trace_cap = c->trace_cap;

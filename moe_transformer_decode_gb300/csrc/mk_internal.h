@@ -32,6 +32,16 @@ constexpr int kStageK = 2 * kTcK;
 constexpr int kGuRows = 64;
 constexpr int kDnRows = 128;
 constexpr int kMoeParts = 8;
+// Expert-down partials of a step: partial j sums the routed experts of rank j, j + parts, ... in
+// rank order, and the next layer's norm adds the partials in order. More partials give down more
+// units (parallelism); fewer make the norm read less. At batch <= 4 kMoePartsSmall, at batch 8
+// kMoeParts; never more than the experts a step can route to.
+constexpr int kMoePartsSmall = 4;
+__host__ __device__ constexpr int moe_parts_for(int batch, int top_k, int n_experts) {
+  return (batch <= 4 ? kMoePartsSmall : kMoeParts) < (batch * top_k < n_experts ? batch * top_k : n_experts)
+             ? (batch <= 4 ? kMoePartsSmall : kMoeParts)
+             : (batch * top_k < n_experts ? batch * top_k : n_experts);
+}
 constexpr int kTmemCols = 512;
 // the A operand (tokens x {hi, lo}, 8 rows per group, groups of 4 tokens) for one 64-column
 // chunk: kMaxB / 4 groups of 1 KB

@@ -243,7 +243,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_we
   p.xs = (float*)(s + o_xs); p.q = (float*)(s + o_q); p.knew = (float*)(s + o_knew); p.vnew = (float*)(s + o_vnew);
   p.apart = (float*)(s + o_apart); p.attn_o = (float*)(s + o_attn_o); p.attn_out = (float*)(s + o_attn_out);
   p.rlogits = (float*)(s + o_rl); p.hsw = (uint8_t*)(s + o_hsw);
-  p.moe_part = (float*)(s + o_moep); p.moe_parts = std::min(kMoeParts, std::min(batch * m.top_k, m.n_experts)); p.attn_hl = (uint16_t*)(s + o_attn_hl); p.moe_out = (float*)(s + o_moe);
+  p.moe_part = (float*)(s + o_moep); p.moe_parts = moe_parts_for(batch, m.top_k, m.n_experts); p.attn_hl = (uint16_t*)(s + o_attn_hl); p.moe_out = (float*)(s + o_moe);
   p.route = (Route*)(s + o_route); p.lm_best_v = (float*)(s + o_lmv); p.lm_best_i = (int32_t*)(s + o_lmi);
   p.topk_ids = (int32_t*)(s + o_tki); p.topk_w = (float*)(s + o_tkw);
   p.counters = (uint32_t*)(s + o_cnt); p.status = (int32_t*)(s + o_status);
