@@ -789,14 +789,10 @@ struct Consumer {
   uint32_t cbar, cphase;
   static constexpr int AR = NB > 4 ? 4 : 2;  // mma A-fragment registers per k-step
   uint32_t gv;          // GEMV passes done (every consumer warp counts the same sequence)
-  int n_layer;          // layer whose normalized input is held in `nf` (-1 none)
+  int n_layer;          // layer whose normalized input is held in the A buffer (-1 none)
   int route_layer;      // layer whose routing is cached in m.rc_*
   int attn_layer;       // layer of attn_ok
   uint32_t attn_ok;     // KV groups whose attention is known complete in attn_layer
-  // the normalized input of layer n_layer, this warp's 256-column slice as mma A fragments:
-  // lane (g, t) holds the hi (g even) or lo (g odd) part of token g/2 (registers 0, 1) and of
-  // token g/2 + 4 (registers 2, 3) at columns 16 s + 2 t + {0, 1} and + {8, 9}
-  uint32_t nf[NB > 1 ? 16 : 1][AR];  // batch 1 reads them from the A operand in shared memory
   float lm_best[NB];    // running LM-head argmax of the stages whose epilogue this lane ran
   int lm_idx[NB];
   uint64_t t_start, t_ready;
@@ -939,15 +935,7 @@ struct Consumer {
     const uint4 gw = *reinterpret_cast<const uint4*>(gain + col);
     const float gf[8] = {bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y),
                          bf_lo(gw.z), bf_hi(gw.z), bf_lo(gw.w), bf_hi(gw.w)};
-    // normalized input into mma fragments, one token at a time through this warp's exchange area
-    float* xw = m.nsm + warp * 256;
-    const int g8 = lane >> 2, t4 = lane & 3, hl = g8 & 1, tb = g8 >> 1;
-    if constexpr (NB > 1) {
-#pragma unroll
-      for (int s = 0; s < 16; ++s)
-#pragma unroll
-        for (int r = 0; r < AR; ++r) nf[s][r] = 0u;
-    }
+    // the normalized input into the A buffer (the GEMVs and the tensor-core products read it there)
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       float tot = 0.f;
@@ -971,32 +959,6 @@ struct Consumer {
                      "r"(hw[1]), "r"(hw[2]), "r"(hw[3]) : "memory");
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + (r0 + 1) * 128 + ((u16 ^ (r0 + 1)) << 4)),
                      "r"(lw[0]), "r"(lw[1]), "r"(lw[2]), "r"(lw[3]) : "memory");
-      }
-      __syncwarp();
-      float4* d4 = reinterpret_cast<float4*>(xw + lane * 8);
-      d4[0] = make_float4(xn[0], xn[1], xn[2], xn[3]);
-      d4[1] = make_float4(xn[4], xn[5], xn[6], xn[7]);
-      __syncwarp();
-      // k-step s = 2 j + h of group j: columns 32 j + 8 t + 4 h + {0, 1} and {2, 3}
-      if (tb == b) {
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          const float4 v = *reinterpret_cast<const float4*>(xw + 32 * (s >> 1) + 8 * t4 + 4 * (s & 1));
-          if constexpr (NB > 1) {  // batch 1 reads its fragments from the A operand in shared memory
-            nf[s][0] = pack_part(v.x, v.y, hl);
-            nf[s][1] = pack_part(v.z, v.w, hl);
-          }
-        }
-      }
-      if constexpr (AR == 4) {
-        if (tb + 4 == b) {
-#pragma unroll
-          for (int s = 0; s < 16; ++s) {
-            const float4 v = *reinterpret_cast<const float4*>(xw + 32 * (s >> 1) + 8 * t4 + 4 * (s & 1));
-            nf[s][2] = pack_part(v.x, v.y, hl);
-            nf[s][3] = pack_part(v.z, v.w, hl);
-          }
-        }
       }
     }
     __syncwarp();
@@ -1144,13 +1106,19 @@ struct Consumer {
   // [32 q, 32 q + 32) of this warp's slice) takes 16-byte unit 4 (q % 2) + t of row g (0: hi,
   // 1: lo of token 0) of 64-column chunk 4 ks + q / 2, which holds its (a0, a2) registers of
   // k-steps 2 q and 2 q + 1 in the column map above; every other lane's are zero
-  // (cbase: the A-buffer chunk of the stage's first column, for inputs wider than one stage)
-  __device__ __forceinline__ void mma_rows_nf1(const uint8_t* st, const Geo& g, int rg, int ks, float (&c)[4][4],
-                                               int cbase = 0) const {
+  // The GEMV core with its A fragments read from the A buffer (the tensor-core A layout: per
+  // 64-column chunk, 8-row groups of 4 tokens x {hi, lo}, 128-byte swizzled) instead of registers:
+  // mma row g < 8 is row g of token group 0 (tokens 0-3), row g + 8 row g of group 1 (tokens 4-7),
+  // the row order of the C fragments' epilogue. One 16-byte load gives a lane its 8 columns of
+  // two k-steps; lanes whose rows hold no token load nothing. cbase: the A-buffer chunk of the
+  // stage's first column, for inputs wider than one stage.
+  __device__ __forceinline__ void mma_rows_sm(const uint8_t* st, const Geo& g, int rg, int ks, float (&c)[4][4],
+                                              int cbase = 0) const {
+    constexpr int kRows = 2 * (NB < 4 ? NB : 4);  // rows of a token group that hold tokens
     const uint8_t* rowp = b_row(st, g, rg, ks);
-    const int r = (lane >> 2) & 1, t4 = lane & 3;
+    const int r = lane >> 2, t4 = lane & 3;
     const uint32_t fr = abuf + (uint32_t)(cbase + 4 * ks) * kAChunk + r * 128;
-    const bool has = lane < 8;
+    const bool has = r < kRows;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       uint4 w0, w1;
@@ -1159,8 +1127,11 @@ struct Consumer {
 #pragma unroll
       for (int hp = 0; hp < 2; ++hp) {  // k-steps 4 jj + 2 hp and 4 jj + 2 hp + 1
         const int q = 2 * jj + hp, unit = 4 * (q & 1) + t4;
-        const uint4 f = has ? lds128(fr + (uint32_t)(q >> 1) * kAChunk + ((unit ^ r) << 4)) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t a0[4] = {f.x, 0u, f.y, 0u}, a1[4] = {f.z, 0u, f.w, 0u};
+        const uint32_t off = (uint32_t)(q >> 1) * kAChunk + ((unit ^ r) << 4);
+        const uint4 f0 = has ? lds128(fr + off) : make_uint4(0u, 0u, 0u, 0u);
+        uint4 f1 = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (NB > 4) f1 = lds128(fr + 1024u + off);
+        const uint32_t a0[4] = {f0.x, f1.x, f0.y, f1.y}, a1[4] = {f0.z, f1.z, f0.w, f1.w};
         mma_bf16(c[2 * hp], a0, bw[4 * hp], bw[4 * hp + 1]);
         mma_bf16(c[2 * hp + 1], a1, bw[4 * hp + 2], bw[4 * hp + 3]);
       }
@@ -1173,11 +1144,7 @@ struct Consumer {
     float c[4][4] = {};
     const uint8_t* st = acquire();
     if (!st) return gv;
-    if constexpr (NB == 1) {
-      if (active) mma_rows_nf1(st, g, rg, ks, c);
-    } else {
-      if (active) mma_rows(st, g, rg, ks, nf, c);
-    }
+    if (active) mma_rows_sm(st, g, rg, ks, c);
     release();
     return post_pass(active, c);
   }
@@ -1729,7 +1696,7 @@ struct Consumer {
         for (int cs = 0; cs < g.NCS; ++cs) {
           const uint8_t* st = acquire();
           if (!st) return;
-          if (active) mma_rows_nf1(st, g, rg, ks, c, cs * (g.KS / 64));
+          if (active) mma_rows_sm(st, g, rg, ks, c, cs * (g.KS / 64));
           release();
         }
         const uint32_t pid = post_pass(active, c);
