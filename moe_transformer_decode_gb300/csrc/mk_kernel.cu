@@ -1278,25 +1278,16 @@ struct Consumer {
     }
     if (pr0 >= 0) epi(prev, pr0, prows);
     if (!ok) return;
-    if (arrive_last_w0(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) publish_routing(l);
+    if (arrive_last(cm.router_arrive(l), p.cnt_per_step[cm.router_arrive(l)])) publish_routing(l);
   }
 
-  // Arrival on `idx` once every consumer warp's writes are done; true in warp 0 of the task
-  // that arrived last (the other warps get false and go on to their next task).
-  __device__ bool arrive_last_w0(int idx, int count) {
-    if (!csync()) return false;
-    if (warp != 0) return false;
-    uint32_t last = 0;
-    if (lane == 0) last = ((atom_acq_rel_add(p.counters + (size_t)idx * kCounterStride, 1u) + 1u) % (uint32_t)count) == 0u;
-    return __shfl_sync(0xffffffffu, last, 0) != 0u;
-  }
-
-  // Routing of layer l by warp 0 alone, then published with one release of the route counter.
-  // Per token: top-k (value descending, lower expert id first on ties), softmax over the k
-  // selected logits. Then the distinct routed experts in ascending id, each with its token
-  // mask and per-token weights. Lane owns experts lane + 32 i. This runs on the critical path
-  // of every layer, so each pick is two warp reductions (redux.sync) on an order-preserving
-  // integer image of the logit, and the lists are built with ballots, not per-lane loops.
+  // Routing of layer l by the block whose router task arrived last, then published with one
+  // release of the route counter. Per token (warp b takes token b): top-k (value descending,
+  // lower expert id first on ties), softmax over the k selected logits. Then (warp 0) the
+  // distinct routed experts in ascending id, each with its token mask and per-token weights.
+  // Lane owns experts lane + 32 i. This runs on the critical path of every layer, so each pick
+  // is two warp reductions (redux.sync) on an order-preserving integer image of the logit, and
+  // the lists are built with ballots, not per-lane loops.
   __device__ static __forceinline__ uint32_t order_key(float x) {
     // +0 and -0 compare equal as logits, so both map to the image of +0
     const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);
@@ -1308,22 +1299,21 @@ struct Consumer {
   __device__ void publish_routing(int l) {
     constexpr int NE = kMaxExperts / 32;
     const int E = p.E, K = p.topk, B = p.B;
-    uint32_t key[NB][NE];
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
+    // every consumer warp of the block that arrived last: warp b routes token b (the tokens are
+    // independent, and a token's picks are a serial chain of warp reductions), marking its picks
+    // in m.em (bit b per expert); warp 0 then builds the distinct list
+    for (int i = threadIdx.x; i < kMaxExperts; i += kConsumerWarps * 32) m.em[i] = 0u;
+    if (!csync()) return;
+    if (warp < B) {
+      const int b = warp;
+      uint32_t key[NE];
 #pragma unroll
       for (int i = 0; i < NE; ++i) {
         const int e = lane + 32 * i;
-        const float x = (b < B && e < E) ? __ldcg(&p.rlogits[((size_t)l * B + b) * E + e]) : -INFINITY;
+        const float x = e < E ? __ldcg(&p.rlogits[((size_t)l * B + b) * E + e]) : -INFINITY;
         // a NaN logit ranks last (with -inf); 0 marks "no expert" and is never picked
-        key[b][i] = e < E ? order_key(x == x ? x : -INFINITY) : 0u;
+        key[i] = e < E ? order_key(x == x ? x : -INFINITY) : 0u;
       }
-    uint32_t emask[NE];  // bit b: token b picked expert lane + 32 i
-#pragma unroll
-    for (int i = 0; i < NE; ++i) emask[i] = 0u;
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      if (b >= B) break;
       float top0 = 0.f, z = 0.f, my_w = 0.f;
       int my_id = 0;
       for (int j = 0; j < K; ++j) {
@@ -1331,13 +1321,14 @@ struct Consumer {
         int be = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < NE; ++i)
-          if (key[b][i] > bk) { bk = key[b][i]; be = lane + 32 * i; }  // ascending e: ties keep the lower id
+          if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }  // ascending e: ties keep the lower id
         const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
         const int pick = (int)__reduce_min_sync(0xffffffffu, bk == kmax ? (uint32_t)be : 0xffffffffu);
         if ((pick & 31) == lane) {
 #pragma unroll
           for (int i = 0; i < NE; ++i)
-            if (i == (pick >> 5)) { key[b][i] = 0u; emask[i] |= 1u << b; }
+            if (i == (pick >> 5)) key[i] = 0u;
+          atomicOr(&m.em[pick], 1u << b);
         }
         const float bv = key_value(kmax);
         if (j == 0) top0 = bv;
@@ -1347,6 +1338,11 @@ struct Consumer {
       }
       if (lane < K) { m.ids[b][lane] = my_id; m.wk[b][lane] = my_w / z; }
     }
+    if (!csync() || warp != 0) return;
+    uint32_t emask[NE];  // bit b: token b picked expert lane + 32 i
+#pragma unroll
+    for (int i = 0; i < NE; ++i) emask[i] = m.em[lane + 32 * i];
+    __syncwarp();
     // the distinct experts in ascending id; m.em[e] holds e's rank for the weight scatter
     Route* rt = p.route + l;
     int na = 0;
