@@ -43,7 +43,7 @@ struct mk_ctx {
   long long wait_ns = 2000000000LL;  // device-side wait limit
   std::string err;
   // workspace (device)
-  float *xs, *q, *knew, *vnew, *attn_o, *attn_out, *rlogits, *moe_out, *moe_part, *apart, *lm_best_v;
+  float *xs, *q, *knew, *vnew, *attn_o, *attn_out, *rlogits, *moe_out, *moe_part, *apart, *lm_best_v, *css;
   uint16_t* attn_hl;
   uint8_t* hsw;
   int32_t* lm_best_i;
@@ -148,7 +148,7 @@ extern "C" void mk_destroy(mk_ctx* c) {
   if (!c) return;
   free_schedule(c);
   cudaFree(c->xs); cudaFree(c->q); cudaFree(c->knew); cudaFree(c->vnew); cudaFree(c->attn_o); cudaFree(c->attn_out);
-  cudaFree(c->rlogits); cudaFree(c->hsw); cudaFree(c->attn_hl); cudaFree(c->moe_out); cudaFree(c->moe_part); cudaFree(c->lm_best_v); cudaFree(c->lm_best_i);
+  cudaFree(c->rlogits); cudaFree(c->hsw); cudaFree(c->attn_hl); cudaFree(c->moe_out); cudaFree(c->moe_part); cudaFree(c->css); cudaFree(c->lm_best_v); cudaFree(c->lm_best_i);
   cudaFree(c->route); cudaFree(c->rope); cudaFree(c->status); cudaFree(c->topk_ids); cudaFree(c->topk_w);
   if (c->status_host) cudaFreeHost(c->status_host);
   delete c;
@@ -244,6 +244,7 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
              dalloc(&c->rlogits, L * Bm * m.n_experts) == cudaSuccess &&
              dalloc(&c->hsw, L * kMaxActive * hsw_slot_bytes(m.expert_inter)) == cudaSuccess &&
              dalloc(&c->moe_part, L * kMoeParts * Bm * H) == cudaSuccess &&
+             dalloc(&c->css, (L + 1) * kMaxCombineSlices * Bm) == cudaSuccess &&
              dalloc(&c->route, L) == cudaSuccess && dalloc(&c->lm_best_v, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
              dalloc(&c->lm_best_i, (size_t)c->n_sm * kMaxB) == cudaSuccess &&
              dalloc(&c->rope, (size_t)c->max_pos * (d / 2)) == cudaSuccess && dalloc(&c->status, ST_WORDS) == cudaSuccess &&
@@ -502,9 +503,22 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   };
 
   std::vector<std::pair<Task, long long>> ts;
+  // Batch 5-8: the input of layer l >= 1 (and the final norm's) is combined once, by column
+  // slices, before the layer's other tasks: slice s writes the residual x = x + attn + sum of the
+  // expert partials for its columns and each token's square sum over them; every norm then reads
+  // only x and those sums (at batch 8 each block would otherwise read every input of every token)
+  const int n_slices = combine_slices_for(B, H);
+  auto emit_combine = [&](int l) {
+    if (n_slices == 0) return;
+    for (int sl = 0; sl < n_slices; ++sl)
+      ts.push_back({mkt(OP_COMBINE, l, sl, n_slices, 0), (long long)(2 + kMoeParts) * kCombineCols * B * 4});
+    cnt[cmap.combine(l)] = n_slices;
+    emit(ts, PA);
+  };
   for (int l = 0; l < L; ++l) {
     std::fill(router_sm.begin(), router_sm.end(), 0);
     as.new_layer();
+    if (l > 0) emit_combine(l);
     // Per layer, in an order that is a topological order of the dependencies (so no SM can
     // wait on work listed after its own): router, QKV, expert gate/up (needs the routing),
     // attention (needs its group's QKV), expert down (needs all gate/up), O-proj (needs
@@ -567,6 +581,8 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     emit(ts, PA);
     cnt[cmap.layer(l)] = n_o + n_down;
   }
+  as.new_layer();
+  emit_combine(L);
   as.new_layer();
   // LM head: contiguous row ranges of whole stages, at most one task per SM (on the least
   // loaded SMs): the argmax takes one candidate per LM task
@@ -729,6 +745,7 @@ static Params make_params(mk_ctx* c, const int32_t* tokens, const int32_t* posit
   p.xs = c->xs; p.q = c->q; p.knew = c->knew; p.vnew = c->vnew; p.apart = c->apart; p.attn_o = c->attn_o;
   p.attn_out = c->attn_out; p.rlogits = c->rlogits; p.hsw = c->hsw; p.attn_hl = c->attn_hl; p.moe_out = c->moe_out;
   p.moe_part = c->moe_part; p.moe_parts = moe_parts_for(c->B, m.top_k, m.n_experts); p.route = c->route;
+  p.combine_slices = combine_slices_for(c->B, m.hidden); p.css = c->css;
   p.lm_best_v = c->lm_best_v; p.lm_best_i = c->lm_best_i; p.counters = c->counters; p.status = c->status;
   p.status_host = c->status_host_dev; p.topk_ids = c->topk_ids; p.topk_w = c->topk_w;
   p.trace = c->trace; p.trace_count = c->trace_count; p.trace_cap = c->trace_cap;

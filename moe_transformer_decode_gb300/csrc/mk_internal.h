@@ -64,8 +64,16 @@ enum Op : uint8_t {
   OP_GU = 4,      // expert gate/up + SiLU*mul, a range of (row block, active expert) units
   OP_O = 5,       // O-proj rows, each warp released by its KV group's counter
   OP_DOWN = 6,    // expert down: (row block, partial) units, each over its share of the experts
-  OP_LM = 7       // LM-head rows + running argmax; the last LM task of the step reduces
+  OP_LM = 7,      // LM-head rows + running argmax; the last LM task of the step reduces
+  OP_COMBINE = 8  // batch 5-8: the residual of a layer's input for one column slice, written once
 };
+// Combine slices (batch 5-8): kCombineCols columns of the residual stream each. At batch <= 4
+// there are none: every block combines the whole residual itself (small enough at that batch).
+constexpr int kCombineCols = 16;
+constexpr int kMaxCombineSlices = 2048 / kCombineCols;  // hidden <= 2048
+__host__ __device__ constexpr int combine_slices_for(int batch, int hidden) {
+  return batch > 4 ? hidden / kCombineCols : 0;
+}
 enum TaskFlag : uint8_t {
   TF_WRITE_X = 1,  // this task's block stores the residual stream x of its layer
   TF_LAST_LM = 2   // this SM's last LM task: publish its argmax candidate
@@ -100,7 +108,9 @@ struct CounterMap {
   __host__ __device__ int attn(int l, int g) const { return 4 * L + L * nkv + l * nkv + g; }
   __host__ __device__ int attn_arrive(int l, int b, int g) const { return 4 * L + 2 * L * nkv + (l * B + b) * nkv + g; }
   __host__ __device__ int lm_arrive() const { return 4 * L + 2 * L * nkv + L * B * nkv; }
-  __host__ __device__ int count() const { return lm_arrive() + 1; }
+  // combine slices done for the input of layer l, l = 1 .. L (L: the final norm's input)
+  __host__ __device__ int combine(int l) const { return lm_arrive() + l; }
+  __host__ __device__ int count() const { return lm_arrive() + L + 1; }
 };
 
 // Device status words.
@@ -138,6 +148,10 @@ struct Params {
   // experts of rank j mod parts), added in order by the next layer's residual + norm
   float* moe_part;
   int moe_parts;
+  // batch 5-8: combine slices per layer input (0: every block combines the whole residual
+  // itself) and their per-token square sums, [L + 1][kMaxCombineSlices][kMaxB]
+  int combine_slices;
+  float* css;
   // activations stored as bf16 hi/lo planes (hi = bf16(v), lo = bf16(v - hi)), the form the
   // tensor-core GEMV consumes: attention output [L][2][B][n_q d]
   uint16_t* attn_hl;

@@ -566,7 +566,7 @@ struct Producer {
   // Issues every copy of task t into the ring, in order. Warp-uniform; false once a wait gave up.
   __device__ bool run_task(const Task& t) {
     const int l = t.layer;
-    switch (t.op) {
+    switch (t.op) {  // (combine tasks carry no weights: nothing of theirs goes through the ring)
       case OP_ROUTER:
       case OP_LM: {
         const Geo g = geo_of(p.H);
@@ -880,7 +880,10 @@ struct Consumer {
     const Geo g = geo_of(p.H);
     const int ks = warp % g.KW;
     const int col = ks * 256 + lane * 8;
-    if (l > 0 && !block_wait(cm.layer(l - 1))) return;
+    // batch 5-8, layer input past the embedding: the combine slices wrote the residual and the
+    // per-slice square sums; only those are read here
+    const bool combined = NB > 4 && l > 0 && p.combine_slices > 0;  // (batch <= 4: compiled out)
+    if (l > 0 && !block_wait(combined ? cm.combine(l) : cm.layer(l - 1))) return;
     float x[NB][8];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -896,6 +899,8 @@ struct Consumer {
         const uint4 w = *reinterpret_cast<const uint4*>(p.embed + (size_t)tok * p.H + col);
         x[b][0] = bf_lo(w.x); x[b][1] = bf_hi(w.x); x[b][2] = bf_lo(w.y); x[b][3] = bf_hi(w.y);
         x[b][4] = bf_lo(w.z); x[b][5] = bf_hi(w.z); x[b][6] = bf_lo(w.w); x[b][7] = bf_hi(w.w);
+      } else if (combined) {
+        load8(p.xs + ((size_t)l * p.B + b) * p.H + col, x[b]);
       } else {
         float a[8], mo[8], mp[8];
         const size_t o = ((size_t)(l - 1) * p.B + b) * p.H + col;
@@ -927,9 +932,22 @@ struct Consumer {
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       ss[b] = s;
     }
-    if (lane == 0 && warp < g.KW)
+    if (combined) {
+      // token b's square sum on warp b: the slices' sums in slice order within a lane, then a
+      // fixed shuffle tree (the same order in every block); the other warps' shares are zero
+      if (warp < NB && warp < p.B) {
+        float tot = 0.f;
+        for (int sl = lane; sl < p.combine_slices; sl += 32)
+          tot += __ldcg(&p.css[((size_t)l * kMaxCombineSlices + sl) * kMaxB + warp]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (lane == 0) m.norm[0][warp] = tot;
+        if (lane > 0 && lane < g.KW) m.norm[lane][warp] = 0.f;
+      }
+    } else if (lane == 0 && warp < g.KW) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) m.norm[warp][b] = ss[b];
+    }
     if (!csync()) return;
     const uint16_t* gain = (l < p.L) ? p.norm_gain + (size_t)l * p.H : p.final_gain;
     const uint4 gw = *reinterpret_cast<const uint4*>(gain + col);
@@ -973,7 +991,7 @@ struct Consumer {
       }
     }
     fence_proxy_async_smem();  // generic stores that the tensor cores read through the async proxy
-    if (write_x && warp < g.KW) {
+    if (write_x && !combined && warp < g.KW) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         if (b >= p.B) continue;
@@ -2171,6 +2189,44 @@ struct Consumer {
     release_counter(cm.attn(l, g));
   }
 
+  // Combine slice t.a of layer t.layer's input (batch 5-8): for its kCombineCols columns and every
+  // token, the residual x = (x + attn_out) + (sum of the expert partials in part order) of the
+  // previous layer, stored once, and each token's square sum over those columns. Warp 0: lane
+  // (b, q) takes token b = lane / 4, columns [c0 + 4 q, + 4).
+  __device__ void op_combine(const Task& t) {
+    const int l = t.layer, c0 = t.a * kCombineCols;
+    if (!block_wait(cm.layer(l - 1))) return;
+    t_ready = gtimer();
+    if (warp == 0) {
+      const int b = lane >> 2, c = c0 + 4 * (lane & 3);
+      float sq = 0.f;
+      if (b < p.B) {
+        const size_t o = ((size_t)(l - 1) * p.B + b) * p.H + c;
+        float4 x = __ldcg(reinterpret_cast<const float4*>(p.xs + o));
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.attn_out + o));
+        float4 mo = __ldcg(reinterpret_cast<const float4*>(p.moe_part + ((size_t)(l - 1) * kMoeParts * p.B + b) * p.H + c));
+        float4 mp[kMoeParts - 1];
+#pragma unroll
+        for (int j = 1; j < kMoeParts; ++j)
+          if (j < p.moe_parts)
+            mp[j - 1] = __ldcg(reinterpret_cast<const float4*>(p.moe_part + (((size_t)(l - 1) * kMoeParts + j) * p.B + b) * p.H + c));
+#pragma unroll
+        for (int j = 1; j < kMoeParts; ++j)
+          if (j < p.moe_parts) {
+            mo.x += mp[j - 1].x; mo.y += mp[j - 1].y; mo.z += mp[j - 1].z; mo.w += mp[j - 1].w;
+          }
+        __stcg(reinterpret_cast<float4*>(p.moe_out + o), mo);
+        x.x = (x.x + a.x) + mo.x; x.y = (x.y + a.y) + mo.y; x.z = (x.z + a.z) + mo.z; x.w = (x.w + a.w) + mo.w;
+        __stcg(reinterpret_cast<float4*>(p.xs + ((size_t)l * p.B + b) * p.H + c), x);
+        sq = fmaf(x.x, x.x, sq); sq = fmaf(x.y, x.y, sq); sq = fmaf(x.z, x.z, sq); sq = fmaf(x.w, x.w, sq);
+      }
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+      if ((lane & 3) == 0 && b < p.B) __stcg(&p.css[((size_t)l * kMaxCombineSlices + t.a) * kMaxB + b], sq);
+    }
+    release_counter(cm.combine(l));
+  }
+
   __device__ void run_task(const Task& t) {
     t_start = gtimer();
     t_ready = t_start;
@@ -2191,6 +2247,9 @@ struct Consumer {
       case OP_O: op_o(t); break;
       case OP_DOWN: op_down(t); break;
       case OP_LM: op_lm(t); break;
+      case OP_COMBINE:
+        if constexpr (NB > 4) op_combine(t);  // only batch 5-8 plans hold combine tasks
+        break;
     }
     if (ok) trace_task(p, t, t_start, t_ready ? t_ready : t_start);
   }

@@ -150,6 +150,7 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_we
   const size_t o_rl = cv.take<float>(L * B * m.n_experts);
   const size_t o_hsw = cv.take<uint8_t>(L * kMaxActive * hsw_slot_bytes(m.expert_inter));
   const size_t o_moep = cv.take<float>(L * kMoeParts * B * H);
+  const size_t o_css = cv.take<float>((L + 1) * kMaxCombineSlices * kMaxB);
   const size_t o_attn_hl = cv.take<uint16_t>(L * 2 * B * od);
   const size_t o_moe = cv.take<float>(L * B * H), o_route = cv.take<Route>(L);
   const size_t o_lmv = cv.take<float>((size_t)ds.n_sm * kMaxB), o_lmi = cv.take<int32_t>((size_t)ds.n_sm * kMaxB);
@@ -243,7 +244,8 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_we
   p.xs = (float*)(s + o_xs); p.q = (float*)(s + o_q); p.knew = (float*)(s + o_knew); p.vnew = (float*)(s + o_vnew);
   p.apart = (float*)(s + o_apart); p.attn_o = (float*)(s + o_attn_o); p.attn_out = (float*)(s + o_attn_out);
   p.rlogits = (float*)(s + o_rl); p.hsw = (uint8_t*)(s + o_hsw);
-  p.moe_part = (float*)(s + o_moep); p.moe_parts = moe_parts_for(batch, m.top_k, m.n_experts); p.attn_hl = (uint16_t*)(s + o_attn_hl); p.moe_out = (float*)(s + o_moe);
+  p.moe_part = (float*)(s + o_moep); p.moe_parts = moe_parts_for(batch, m.top_k, m.n_experts);
+  p.combine_slices = combine_slices_for(batch, m.hidden); p.css = (float*)(s + o_css); p.attn_hl = (uint16_t*)(s + o_attn_hl); p.moe_out = (float*)(s + o_moe);
   p.route = (Route*)(s + o_route); p.lm_best_v = (float*)(s + o_lmv); p.lm_best_i = (int32_t*)(s + o_lmi);
   p.topk_ids = (int32_t*)(s + o_tki); p.topk_w = (float*)(s + o_tkw);
   p.counters = (uint32_t*)(s + o_cnt); p.status = (int32_t*)(s + o_status);

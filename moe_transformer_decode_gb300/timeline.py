@@ -12,7 +12,7 @@ import numpy as np
 
 from . import binding as B
 
-OP_NAMES = {1: "router", 2: "qkv", 3: "attn", 4: "gu", 5: "o", 6: "down", 7: "lm"}
+OP_NAMES = {1: "router", 2: "qkv", 3: "attn", 4: "gu", 5: "o", 6: "down", 7: "lm", 8: "combine"}
 
 TRACE_DTYPE = np.dtype([("t", "<u8"), ("wait", "<u4"), ("run", "<u4"), ("sm", "<u2"), ("op", "<u2"),
                         ("layer", "<u2"), ("pad", "<u2"), ("a", "<i4"), ("b", "<i4")])

@@ -7,8 +7,8 @@ import pytest
 from moe_transformer_decode_gb300 import binding as B
 from synth import workloads as W
 
-OP_ROUTER, OP_QKV, OP_ATTN, OP_GU, OP_O, OP_DOWN, OP_LM = range(1, 8)
-RANK = {OP_ROUTER: 0, OP_QKV: 1, OP_GU: 2, OP_ATTN: 3, OP_DOWN: 4, OP_O: 5, OP_LM: 6}
+OP_ROUTER, OP_QKV, OP_ATTN, OP_GU, OP_O, OP_DOWN, OP_LM, OP_COMBINE = range(1, 9)
+RANK = {OP_COMBINE: -1, OP_ROUTER: 0, OP_QKV: 1, OP_GU: 2, OP_ATTN: 3, OP_DOWN: 4, OP_O: 5, OP_LM: 6}
 
 
 def cfg_of(w, max_pages):
@@ -38,6 +38,16 @@ def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
         assert np.all(np.diff(key) >= 0), f"SM {s} list out of order"
     maxa = min(w.B * w.topk, w.E)
     upg = (w.nq // w.nkv + 2) * (w.d // 8)
+    # batch 5-8: the input of every layer past the first, and the final norm's, is combined by
+    # slices of 16 columns, each exactly once
+    cb = tasks[tasks["op"] == OP_COMBINE]
+    if w.B > 4:
+        for l in range(1, w.L + 1):
+            c = cb[cb["layer"] == l]
+            assert sorted(c["a"].tolist()) == list(range(w.H // 16)) and np.all(c["b"] == w.H // 16)
+        assert np.all(cb["layer"] >= 1)
+    else:
+        assert cb.size == 0
     for l in range(w.L):
         t = tasks[tasks["layer"] == l]
         r = t[t["op"] == OP_ROUTER]
