@@ -31,7 +31,7 @@ constexpr int kTcK = 64;
 constexpr int kStageK = 2 * kTcK;
 constexpr int kGuRows = 64;
 constexpr int kDnRows = 128;
-constexpr int kMoeParts = 8;
+constexpr int kMoeParts = 9;
 // Expert-down partials of a step: partial j sums the routed experts of rank j, j + parts, ... in
 // rank order, and the next layer's norm adds the partials in order. More partials give down more
 // units (parallelism); fewer make the norm read less. At batch <= 4 kMoePartsSmall, at batch 8

@@ -79,7 +79,7 @@ def test_plan_covers_everything_once_in_dependency_order(w, n_sm):
         # down: one task per (128-row block, partial) unit; a partial takes the experts of rank
         # j, j + parts, ..., so every unit of a layer has the same share of the routed experts
         dn = t[t["op"] == OP_DOWN]
-        parts = min(4 if w.B <= 4 else 8, maxa)  # expert-down partials: 4 at batch <= 4, 8 at batch 8
+        parts = min(4 if w.B <= 4 else 9, maxa)  # expert-down partials: 4 at batch <= 4, 9 at batch 8
         assert sorted(_ranges(dn).tolist()) == list(range((w.H // 128) * parts)) and np.all(dn["b"] == 1)
     lm = tasks[tasks["op"] == OP_LM]
     assert sorted(_ranges(lm).tolist()) == list(range(w.V))
