@@ -883,6 +883,9 @@ struct Consumer {
     // batch 5-8, layer input past the embedding: the combine slices wrote the residual and the
     // per-slice square sums; only those are read here
     const bool combined = NB > 4 && l > 0 && p.combine_slices > 0;  // (batch <= 4: compiled out)
+    // the gain (static) is read before the wait, off the layer's dependency chain
+    const uint16_t* gain = (l < p.L) ? p.norm_gain + (size_t)l * p.H : p.final_gain;
+    const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gain + col));
     if (l > 0 && !block_wait(combined ? cm.combine(l) : cm.layer(l - 1))) return;
     float x[NB][8];
 #pragma unroll
@@ -949,8 +952,6 @@ struct Consumer {
       for (int b = 0; b < NB; ++b) m.norm[warp][b] = ss[b];
     }
     if (!csync()) return;
-    const uint16_t* gain = (l < p.L) ? p.norm_gain + (size_t)l * p.H : p.final_gain;
-    const uint4 gw = *reinterpret_cast<const uint4*>(gain + col);
     const float gf[8] = {bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y),
                          bf_lo(gw.z), bf_hi(gw.z), bf_lo(gw.w), bf_hi(gw.w)};
     // the normalized input into the A buffer (the GEMVs and the tensor-core products read it there)
@@ -2088,86 +2089,97 @@ struct Consumer {
     const int arr = cm.attn_arrive(l, b, g);
     if (!arrive_last(arr, m.st_nch[b])) return;
 
-    // combine the chunks of (b, g) with the new token (position pos, read from knew / vnew):
-    // the chunk maxima and sums and the new token's scores in one round of loads, then the chunk
-    // outputs in one round (a float4 of one head per thread)
+    // combine the chunks of (b, g) with the new token (position pos, read from knew / vnew)
     const int nch = m.st_nch[b];
     const float* pbase = p.apart + (((size_t)l * p.B + b) * p.nkv + g) * p.max_chunks * (16 + 8 * (size_t)p.d);
     const size_t cstride = 16 + 8 * (size_t)p.d;
     const float* vn = p.vnew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
-    float* sc = &m.red[2][0][0];  // [0, 8): new token's scores, [8, 16): its factor, [16, 24): 1 / sum
-    float* sm_m = &m.red[0][0][0];  // [nch][8]: chunk max, then its scale factor
-    float* sm_l = &m.red[1][0][0];  // [nch][8]: chunk sum
-    const bool few = nch <= 64;
-    if (few)
-      for (int i = threadIdx.x; i < nch * 8; i += 256) {
-        const float* src = pbase + (size_t)(i / 8) * cstride;
-        sm_m[i] = __ldcg(src + (i % 8));
-        sm_l[i] = __ldcg(src + 8 + (i % 8));
-      }
-    if (warp < p.group) {  // s_new of head `warp`
-      const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + warp) * p.d;
-      const float* kn = p.knew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
-      float s = 0.f;
-      const int hd = p.d / 2;
-      for (int i = lane; i < hd; i += 32) {  // q before RoPE: rotate pair (i, i + d/2)
-        const float2 cs = m.st_rope[b][i];
-        const float q0 = __ldcg(qh + i), q1 = __ldcg(qh + i + hd);
-        s = fmaf(q0 * cs.x - q1 * cs.y, __ldcg(kn + i), s);
-        s = fmaf(q0 * cs.y + q1 * cs.x, __ldcg(kn + i + hd), s);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) sc[warp] = s * qscale;
-    }
-    if (!csync()) return;
-    if (few) {
-      if (threadIdx.x < p.group) {
-        const int h = threadIdx.x;
-        const float sn = sc[h];
-        float M = sn;
-        for (int c = 0; c < nch; ++c) M = fmaxf(M, sm_m[c * 8 + h]);
-        const float fn = exp2f(sn - M);
-        float L = fn;
-        for (int c = 0; c < nch; ++c) {
-          const float mc = sm_m[c * 8 + h];
-          const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
-          L += sm_l[c * 8 + h] * f;
-          sm_m[c * 8 + h] = f;
-        }
-        sc[8 + h] = fn;
-        sc[16 + h] = 1.0f / L;
-      }
-      if (!csync()) return;
-      for (int i = threadIdx.x; i < p.group * p.d / 4; i += 256) {
-        const int h = 4 * i / p.d, dd = 4 * i % p.d;
+    const float* kn = p.knew + (((size_t)l * p.B + b) * p.nkv + g) * p.d;
+    const int hd = p.d / 2;
+    if (nch <= 64) {
+      // Warp h combines head h on its own, with no block barrier: one round of loads brings the
+      // new token's q and k, every chunk's max and sum (lane j: chunks j and j + 32) and the
+      // first 16 chunks' outputs of the lane's 4 columns; the scale factors reach the other
+      // lanes by shuffles. (group <= 8: one head per warp at most)
+      const int h = warp;
+      if (h < p.group) {
+        const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + h) * p.d;
+        const int dd = 4 * lane;
+        const bool has = dd < p.d;
         const float* src = pbase + 16 + h * p.d + dd;
-        const float fn = sc[8 + h];
-        const float4 vv = __ldcg(reinterpret_cast<const float4*>(vn + dd));
+        float4 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j] = (j < nch && has) ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)j * cstride))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float m0 = lane < nch ? __ldcg(pbase + (size_t)lane * cstride + h) : -INFINITY;
+        const float l0 = lane < nch ? __ldcg(pbase + (size_t)lane * cstride + 8 + h) : 0.f;
+        const float m1 = lane + 32 < nch ? __ldcg(pbase + (size_t)(lane + 32) * cstride + h) : -INFINITY;
+        const float l1 = lane + 32 < nch ? __ldcg(pbase + (size_t)(lane + 32) * cstride + 8 + h) : 0.f;
+        const float4 vv = has ? __ldcg(reinterpret_cast<const float4*>(vn + dd)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float s = 0.f;
+        for (int i = lane; i < hd; i += 32) {  // q before RoPE: rotate pair (i, i + d/2)
+          const float2 cs = m.st_rope[b][i];
+          const float q0 = __ldcg(qh + i), q1 = __ldcg(qh + i + hd);
+          s = fmaf(q0 * cs.x - q1 * cs.y, __ldcg(kn + i), s);
+          s = fmaf(q0 * cs.y + q1 * cs.x, __ldcg(kn + i + hd), s);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float sn = s * qscale;
+        float M = fmaxf(sn, fmaxf(m0, m1));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float fn = exp2f(sn - M);
+        const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+        const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+        float L = l0 * f0 + l1 * f1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        L += fn;
         float4 O = make_float4(fn * vv.x, fn * vv.y, fn * vv.z, fn * vv.w);
         for (int c0 = 0; c0 < nch; c0 += 16) {
-          float4 v[16];
+          if (c0 > 0)
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            v[j] = c0 + j < nch ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)(c0 + j) * cstride))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 16; ++j)
+              v[j] = (c0 + j < nch && has) ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)(c0 + j) * cstride))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float fsrc = c0 < 32 ? f0 : f1;  // chunks [c0, c0 + 16) lie in one half
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float f = c0 + j < nch ? sm_m[(c0 + j) * 8 + h] : 0.f;
+            const float f = __shfl_sync(0xffffffffu, fsrc, (c0 + j) & 31);
             O.x = fmaf(v[j].x, f, O.x);
             O.y = fmaf(v[j].y, f, O.y);
             O.z = fmaf(v[j].z, f, O.z);
             O.w = fmaf(v[j].w, f, O.w);
           }
         }
-        const float inv = sc[16 + h];
-        const int col = (g * p.group + h) * p.d + dd;
-        store_attn(l, b, col, O.x * inv);
-        store_attn(l, b, col + 1, O.y * inv);
-        store_attn(l, b, col + 2, O.z * inv);
-        store_attn(l, b, col + 3, O.w * inv);
+        if (has) {
+          const float inv = 1.0f / L;
+          const int col = (g * p.group + h) * p.d + dd;
+          store_attn(l, b, col, O.x * inv);
+          store_attn(l, b, col + 1, O.y * inv);
+          store_attn(l, b, col + 2, O.z * inv);
+          store_attn(l, b, col + 3, O.w * inv);
+        }
       }
     } else {
+      // many chunks: the new token's scores first (warp h: head h), then one thread per output
+      float* sc = &m.red[2][0][0];
+      if (warp < p.group) {
+        const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + warp) * p.d;
+        float s = 0.f;
+        for (int i = lane; i < hd; i += 32) {
+          const float2 cs = m.st_rope[b][i];
+          const float q0 = __ldcg(qh + i), q1 = __ldcg(qh + i + hd);
+          s = fmaf(q0 * cs.x - q1 * cs.y, __ldcg(kn + i), s);
+          s = fmaf(q0 * cs.y + q1 * cs.x, __ldcg(kn + i + hd), s);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) sc[warp] = s * qscale;
+      }
+      if (!csync()) return;
       for (int i = threadIdx.x; i < p.group * p.d; i += 256) {
         const int h = i / p.d, dd = i % p.d;
         const float sn = sc[h];
