@@ -80,8 +80,11 @@ struct mk_ctx {
 
 // The expert weights as 3D bf16 views {64, rows, K / 64} (strides: a row, 128 bytes) with 128B
 // swizzle: a gate/up box lands kGuRows rows x 64 columns, a down box kDnRows rows x 128 columns
-// as two [rows][128 bytes] chunks, the layout of the tcgen05 B operand.
-mk_status mk::encode_expert_maps(void* encode_fn, const mk_model_cfg& m, const mk_weight_ptrs* w, TensorMaps& tm) {
+// as two [rows][128 bytes] chunks, the layout of the tcgen05 B operand. The O-proj weights as a
+// 3D view {256, od / 256, rows} (strides: 512 bytes, a row) without swizzle: a box of RS rows x
+// KS / 256 column blocks lands a row-major GEMV stage in one copy (a bulk copy per row would
+// take RS copies, and a copy's issue time grows with their number).
+mk_status mk::encode_weight_maps(void* encode_fn, const mk_model_cfg& m, const mk_weight_ptrs* w, TensorMaps& tm) {
   EncodeTiledFn enc = (EncodeTiledFn)encode_fn;
   const uint64_t gu_rows = (uint64_t)m.n_layers * m.n_experts * 2 * m.expert_inter;
   const uint64_t dn_rows = (uint64_t)m.n_layers * m.n_experts * m.hidden;
@@ -102,6 +105,21 @@ mk_status mk::encode_expert_maps(void* encode_fn, const mk_model_cfg& m, const m
     cuuint32_t box[3] = {64, (cuuint32_t)kDnRows, (cuuint32_t)(kStageK / 64)};
     if (enc(&tm.dn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w->w_down), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MK_ERR_CUDA;
+  }
+  {
+    // the GEMV geometry of K = od (KS = min(od, 2048) columns, RS = 8 * 8 / (KS / 256) rows; od is a
+    // multiple of 256): the box is RS x KS elements, 32 KB
+    const uint64_t od = (uint64_t)m.n_q_heads * m.head_dim;
+    const uint64_t o_rows = (uint64_t)m.n_layers * m.hidden;
+    const uint32_t ks = od < 2048 ? (uint32_t)od : 2048u, kw = ks / 256, rs = 8u * (8u / kw);
+    if (o_rows >= (1ull << 31)) return MK_ERR_UNSUPPORTED;
+    cuuint64_t dims[3] = {256, (cuuint64_t)(od / 256), (cuuint64_t)o_rows};
+    cuuint64_t strides[2] = {512, (cuuint64_t)od * 2};
+    cuuint32_t box[3] = {256, kw, rs};
+    if (enc(&tm.wo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w->w_o), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MK_ERR_CUDA;
   }
@@ -277,9 +295,10 @@ extern "C" mk_status mk_create(const mk_model_cfg* cfg, const mk_weight_ptrs* w,
     e = cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) { mk_destroy(c); return MK_ERR_CUDA; }
   }
-  // the expert weights as tcgen05 B operand tiles (3D views {64, rows, K / 64}, 128B swizzle)
+  // the expert weights as tcgen05 B operand tiles (3D views {64, rows, K / 64}, 128B swizzle) and
+  // the O-proj weights as whole GEMV stages
   {
-    const mk_status ts = encode_expert_maps((void*)c->encode, m, w, c->tm);
+    const mk_status ts = encode_weight_maps((void*)c->encode, m, w, c->tm);
     if (ts != MK_OK) {
       mk_destroy(c);
       return ts;

@@ -196,10 +196,13 @@ struct TensorMaps {
   // layout): gate/up rows [L][E][2I] over K = hidden, box {64, kGuRows, 1}; down rows [L][E][H]
   // over K = I, box {64, kDnRows, 2}
   CUtensorMap gu, dn;
+  // O-proj weights [L][H][od] as a 3D {256, od / 256, L H} bf16 view without swizzle, box
+  // {256, KS / 256, RS}: one copy lands a GEMV stage (RS rows x KS columns, row-major)
+  CUtensorMap wo;
 };
 // bytes of one expert's activation slot in Params::hsw
 inline __host__ __device__ size_t hsw_slot_bytes(int I) { return (size_t)(I / 64) * kAChunkMax; }
-// encodes TensorMaps::gu and ::dn over the caller's expert weights (encode_fn: cuTensorMapEncodeTiled)
-mk_status encode_expert_maps(void* encode_fn, const mk_model_cfg& m, const mk_weight_ptrs* w, TensorMaps& tm);
+// encodes TensorMaps::gu, ::dn and ::wo over the caller's weights (encode_fn: cuTensorMapEncodeTiled)
+mk_status encode_weight_maps(void* encode_fn, const mk_model_cfg& m, const mk_weight_ptrs* w, TensorMaps& tm);
 
 }  // namespace mk

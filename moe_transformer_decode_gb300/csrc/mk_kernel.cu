@@ -649,13 +649,17 @@ struct Producer {
         return true;
       }
       case OP_O: {
+        // row blocks, each over the column chunks; a stage is one tensor copy of RS rows x KS
+        // columns (rows past the task's last one land too and are not read)
         const Geo g = geo_of(p.od);
-        const uint16_t* W = p.w_o + ((size_t)l * p.H + t.a) * p.od;
 #pragma unroll 1
-        for (int r0 = 0; r0 < t.b; r0 += g.RS)  // row blocks, each over the column chunks
+        for (int r0 = 0; r0 < t.b; r0 += g.RS)
 #pragma unroll 1
-          for (int cs = 0; cs < g.NCS; ++cs)
-            if (!gemv_rows(W + (size_t)r0 * p.od + cs * g.KS, min(g.RS, t.b - r0), p.od, g.KS * 2)) return false;
+          for (int cs = 0; cs < g.NCS; ++cs) {
+            if (!begin(kStagePayload)) return false;
+            if (lane == 0) tma_3d_g2s(dst, &tm.wo, 0, cs * g.KW, l * p.H + t.a + r0, bar, pol);
+            end();
+          }
         return true;
       }
       case OP_DOWN: {
@@ -887,6 +891,57 @@ struct Consumer {
     const uint16_t* gain = (l < p.L) ? p.norm_gain + (size_t)l * p.H : p.final_gain;
     const uint4 gw = __ldg(reinterpret_cast<const uint4*>(gain + col));
     if (l > 0 && !block_wait(combined ? cm.combine(l) : cm.layer(l - 1))) return;
+    // combined: token `warp`'s per-slice square sums (lane j: slices j, j + 32, ...), all in one
+    // round of loads right after the wait
+    constexpr int kCsPerLane = kMaxCombineSlices / 32;
+    float csq[kCsPerLane];
+#pragma unroll
+    for (int j = 0; j < kCsPerLane; ++j) {
+      const int sl = lane + 32 * j;
+      csq[j] = (combined && warp < NB && warp < p.B && sl < p.combine_slices)
+                   ? __ldcg(&p.css[((size_t)l * kMaxCombineSlices + sl) * kMaxB + warp])
+                   : 0.f;
+    }
+    if (combined) {
+      // warp b normalizes token b over every column: its square sum is the slices' sums in slice
+      // order within a lane, then a fixed shuffle tree (the same order in every block), so no
+      // block barrier sits between the sums and the normalization; tokens past the batch write
+      // zero rows of the A operand
+      const int b = warp;
+      float tot = 0.f;
+#pragma unroll
+      for (int j = 0; j < kCsPerLane; ++j) tot += csq[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      const float rinv = 1.0f / sqrtf(tot / (float)p.H + p.eps);
+      const bool live = b < p.B;
+      const int q = b >> 2, r0 = 2 * (b & 3);
+      const float* xrow = p.xs + ((size_t)l * p.B + (live ? b : 0)) * p.H;
+#pragma unroll 4
+      for (int c = lane * 8; c < p.H; c += 256) {
+        float xv[8];
+        if (live) load8(xrow + c, xv);
+        const uint4 gc = __ldg(reinterpret_cast<const uint4*>(gain + c));
+        const float gf[8] = {bf_lo(gc.x), bf_hi(gc.x), bf_lo(gc.y), bf_hi(gc.y),
+                             bf_lo(gc.z), bf_hi(gc.z), bf_lo(gc.w), bf_hi(gc.w)};
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (live) split_pack(xv[2 * i] * rinv * gf[2 * i], xv[2 * i + 1] * rinv * gf[2 * i + 1], hw[i], lw[i]);
+          else hw[i] = lw[i] = 0u;
+        }
+        const int u16 = (c & 63) >> 3;
+        const uint32_t base = abuf + (uint32_t)(c >> 6) * kAChunk + (uint32_t)q * 1024u;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + r0 * 128 + ((u16 ^ r0) << 4)), "r"(hw[0]),
+                     "r"(hw[1]), "r"(hw[2]), "r"(hw[3]) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + (r0 + 1) * 128 + ((u16 ^ (r0 + 1)) << 4)),
+                     "r"(lw[0]), "r"(lw[1]), "r"(lw[2]), "r"(lw[3]) : "memory");
+      }
+      fence_proxy_async_smem();  // generic stores that the tensor cores read through the async proxy
+      if (!csync()) return;
+      n_layer = l;
+      return;
+    }
     float x[NB][8];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -902,8 +957,6 @@ struct Consumer {
         const uint4 w = *reinterpret_cast<const uint4*>(p.embed + (size_t)tok * p.H + col);
         x[b][0] = bf_lo(w.x); x[b][1] = bf_hi(w.x); x[b][2] = bf_lo(w.y); x[b][3] = bf_hi(w.y);
         x[b][4] = bf_lo(w.z); x[b][5] = bf_hi(w.z); x[b][6] = bf_lo(w.w); x[b][7] = bf_hi(w.w);
-      } else if (combined) {
-        load8(p.xs + ((size_t)l * p.B + b) * p.H + col, x[b]);
       } else {
         float a[8], mo[8], mp[8];
         const size_t o = ((size_t)(l - 1) * p.B + b) * p.H + col;
@@ -925,31 +978,20 @@ struct Consumer {
         for (int i = 0; i < 8; ++i) x[b][i] = (x[b][i] + a[i]) + mo[i];
       }
     }
-    float ss[NB];
+    {
+      float ss[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float s = 0.f;
+      for (int b = 0; b < NB; ++b) {
+        float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s = fmaf(x[b][i], x[b][i], s);
+        for (int i = 0; i < 8; ++i) s = fmaf(x[b][i], x[b][i], s);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      ss[b] = s;
-    }
-    if (combined) {
-      // token b's square sum on warp b: the slices' sums in slice order within a lane, then a
-      // fixed shuffle tree (the same order in every block); the other warps' shares are zero
-      if (warp < NB && warp < p.B) {
-        float tot = 0.f;
-        for (int sl = lane; sl < p.combine_slices; sl += 32)
-          tot += __ldcg(&p.css[((size_t)l * kMaxCombineSlices + sl) * kMaxB + warp]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        if (lane == 0) m.norm[0][warp] = tot;
-        if (lane > 0 && lane < g.KW) m.norm[lane][warp] = 0.f;
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        ss[b] = s;
       }
-    } else if (lane == 0 && warp < g.KW) {
+      if (lane == 0 && warp < g.KW)
 #pragma unroll
-      for (int b = 0; b < NB; ++b) m.norm[warp][b] = ss[b];
+        for (int b = 0; b < NB; ++b) m.norm[warp][b] = ss[b];
     }
     if (!csync()) return;
     const float gf[8] = {bf_lo(gw.x), bf_hi(gw.x), bf_lo(gw.y), bf_hi(gw.y),
@@ -992,7 +1034,7 @@ struct Consumer {
       }
     }
     fence_proxy_async_smem();  // generic stores that the tensor cores read through the async proxy
-    if (write_x && !combined && warp < g.KW) {
+    if (write_x && warp < g.KW) {
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         if (b >= p.B) continue;

@@ -202,8 +202,8 @@ extern "C" mk_status mk_decode_step_noalloc(const mk_model_cfg* cfg, const mk_we
   }
 
   TensorMaps tm;
-  if (encode_expert_maps((void*)g_encode, m, w, tm) != MK_OK) {
-    set_msg(msg, msg_len, "cuTensorMapEncodeTiled failed for the expert weights");
+  if (encode_weight_maps((void*)g_encode, m, w, tm) != MK_OK) {
+    set_msg(msg, msg_len, "cuTensorMapEncodeTiled failed for the expert or O-proj weights");
     return MK_ERR_INVALID_ARG;
   }
   {
