@@ -342,18 +342,21 @@ Geo geo_of(int K) {
 // Least-loaded assignment within a partition of the SMs. Loads are counted per phase
 // (new_layer() restarts them), so each phase's work is spread evenly over the partition; ties
 // go to the SM with the least bytes over the whole step (`total`), so no SM takes the extra
-// task in every phase.
+// task in every phase. `layer` counts each SM's bytes since begin_layer(): put_layer breaks the
+// phase's ties by it instead, so a phase's extra tasks land on the SMs with the least work in the
+// layer so far.
 struct Assigner {
   int n_sm;
   std::vector<int> part;  // partition of each SM
-  std::vector<long long> load, total;
+  std::vector<long long> load, total, layer;
   std::vector<std::vector<Task>> lists;
   typedef std::tuple<long long, long long, int> Key;
   std::vector<std::priority_queue<Key, std::vector<Key>, std::greater<>>> heaps;
   Assigner(int n, std::vector<int> part_, int n_parts)
-      : n_sm(n), part(std::move(part_)), load(n, 0), total(n, 0), lists(n), heaps(n_parts) {
+      : n_sm(n), part(std::move(part_)), load(n, 0), total(n, 0), layer(n, 0), lists(n), heaps(n_parts) {
     new_layer();
   }
+  void begin_layer() { std::fill(layer.begin(), layer.end(), 0LL); }
   void new_layer() {
     for (auto& h : heaps) h = std::priority_queue<Key, std::vector<Key>, std::greater<>>();
     for (int s = 0; s < n_sm; ++s) {
@@ -366,6 +369,7 @@ struct Assigner {
     lists[s].push_back(t);
     load[s] += bytes;
     total[s] += bytes;
+    layer[s] += bytes;
     auto& heap = heaps[part[s]];
     std::vector<Key> keep;
     while (!heap.empty()) {
@@ -393,8 +397,18 @@ struct Assigner {
     lists[s].push_back(t);
     load[s] += bytes;
     total[s] += bytes;
+    layer[s] += bytes;
     heap.push(Key(load[s], total[s], s));
     return s;
+  }
+  // onto the least-loaded SM of partition pt in this phase, ties to the least bytes in the layer
+  int put_layer(const Task& t, long long bytes, int pt) {
+    int best = -1;
+    for (int s = 0; s < n_sm; ++s)
+      if (part[s] == pt && (best < 0 || std::make_tuple(load[s], layer[s], s) < std::make_tuple(load[best], layer[best], best)))
+        best = s;
+    put_on(t, bytes, best);
+    return best;
   }
 };
 
@@ -505,11 +519,14 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   // SMs holding a router task of the current layer (QKV avoids them: one of them computes the
   // routing right after its router task)
   std::vector<char> router_sm(n_sm, 0);
-  auto emit = [&](std::vector<std::pair<Task, long long>>& ts, int pt) {  // pt < 0: any SM
+  // pt < 0: any SM; by_layer: least bytes in the layer so far (put_layer), not in the phase
+  auto emit = [&](std::vector<std::pair<Task, long long>>& ts, int pt, bool by_layer = false) {
     as.new_layer();
     for (auto& x : ts) {
       if (pt < 0) {
         as.put_any(x.first, x.second, router_sm);
+      } else if (by_layer) {
+        as.put_layer(x.first, x.second, pt);
       } else {
         const int s = as.put(x.first, x.second, pt);
         if (x.first.op == OP_ROUTER) router_sm[s] = 1;
@@ -537,6 +554,7 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
   for (int l = 0; l < L; ++l) {
     std::fill(router_sm.begin(), router_sm.end(), 0);
     as.new_layer();
+    as.begin_layer();
     if (l > 0) emit_combine(l);
     // Per layer, in an order that is a topological order of the dependencies (so no SM can
     // wait on work listed after its own): router, QKV, expert gate/up (needs the routing),
@@ -585,11 +603,12 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     }
     for (int g = 0; g < nkv; ++g) cnt[cmap.attn(l, g)] = B;
     // expert down: units u = row block * parts + part (kDnRows rows over the routed experts of
-    // rank part, part + parts, ...), one per task
+    // rank part, part + parts, ...), one per task; without a partition, the SMs with the fewest
+    // bytes in the layer so far take the phase's extra tasks (as for O-proj below)
     int n_down = 0;
     for (int u = 0; u < (H / kDnRows) * parts; ++u, ++n_down)
       ts.push_back({mkt(OP_DOWN, l, u, 1, 0), (long long)((double)kDnRows * I * 2 * live * maxa / parts)});
-    emit(ts, PM);
+    emit(ts, PM, n_attn == n_sm);
     // O-proj: blocks of RS rows; at batch <= 4 (and at most two 2048-column chunks) a task takes
     // several blocks, reusing one load of the attention output, about one task per SM
     const int o_blocks = (H + go.RS - 1) / go.RS;
@@ -597,7 +616,11 @@ mk_status mk::plan_schedule(const mk_model_cfg& m, int n_sm, int B, const int32_
     int n_o = 0;
     for (int r0 = 0; r0 < H; r0 += o_per * go.RS, ++n_o)
       ts.push_back({mkt(OP_O, l, r0, std::min(o_per * go.RS, H - r0), 0), std::min(o_per * go.RS, H - r0) * 2LL * od});
-    emit(ts, PA);
+    // when every SM takes both branches, O-proj is the layer's last phase and each SM reaches it
+    // after its own gate/up, attention and down work: the SMs with the fewest bytes in the layer
+    // so far take the phase's extra tasks (by step totals, the SMs whose down work ended last
+    // took two O-proj tasks each at batch 8, ~10 us after the others)
+    emit(ts, PA, n_attn == n_sm);
     cnt[cmap.layer(l)] = n_o + n_down;
   }
   as.new_layer();
