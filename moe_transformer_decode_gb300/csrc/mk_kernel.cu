@@ -1939,28 +1939,18 @@ struct Consumer {
     const float qscale = rsqrtf((float)p.d) * 1.4426950408889634f;  // scores in log2 units
     uint32_t qa[KS][4];
     {
-      // the group's q (group x d floats, contiguous) into shared memory once per block, one
-      // float4 per thread, rows padded by 4 floats; the partial-sum buffers are free here (the
-      // barrier waits for the previous task's last epilogue)
-      float* qs = &m.red[1][0][0];
-      const int qst = p.d + 4;
-      if (!csync()) return;
-      const float4* qg = reinterpret_cast<const float4*>(p.q + (((size_t)l * p.B + b) * p.nq + g * p.group) * p.d);
-      for (int i = threadIdx.x; i < p.group * p.d / 4; i += 256) {
-        const int hh = 4 * i / p.d, dd = 4 * i % p.d;
-        *reinterpret_cast<float4*>(qs + hh * qst + dd) = __ldcg(qg + i);
-      }
-      if (!csync()) return;
-      // q arrives before RoPE: element d pairs with d + d/2, which this lane also holds (k-step
+      // this lane's q elements straight from global memory (one round of 8-byte loads); q
+      // arrives before RoPE: element d pairs with d + d/2, which this lane also holds (k-step
       // kk + ksteps/2), so the rotation happens here in registers
-      const float* qh = qs + head * qst;
       const bool hv = head < p.group;
+      const float* qh = p.q + (((size_t)l * p.B + b) * p.nq + g * p.group + (hv ? head : 0)) * p.d;
       float x[KS][4];
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         const int d0 = kk * 16 + tig * 2;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[kk][e] = hv ? qh[d0 + (e & 1) + (e >> 1) * 8] : 0.f;
+        const float2 lo = hv ? __ldcg(reinterpret_cast<const float2*>(qh + d0)) : make_float2(0.f, 0.f);
+        const float2 hi = hv ? __ldcg(reinterpret_cast<const float2*>(qh + d0 + 8)) : make_float2(0.f, 0.f);
+        x[kk][0] = lo.x; x[kk][1] = lo.y; x[kk][2] = hi.x; x[kk][3] = hi.y;
       }
       constexpr int half = KS / 2;
 #pragma unroll
@@ -2095,7 +2085,7 @@ struct Consumer {
       static_assert(kConsumerWarps * kW * 4 <= kABufBytes, "merge scratch exceeds the A buffer");
       float* scr = reinterpret_cast<float*>(__cvta_shared_to_generic(abuf));
       float* mine = scr + warp * kW;
-      // (the q load's block barriers put every earlier reader of the buffer behind this point)
+      // (every earlier reader of the buffer finished before the block barrier that ended its task)
       if (tig == 0) { mine[head] = mrun; mine[8 + head] = lsum; }
 #pragma unroll
       for (int nt = 0; nt < 2 * KS; ++nt)
